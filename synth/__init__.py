@@ -1,0 +1,100 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module only draws random numbers and places them into byte records.  It
+holds none of the mat-vec's arithmetic (no decoding, no dot products, no
+quantization rounding): the oracle quantizes, the CUDA library decodes.
+
+Generators (numpy PCG64 via ``default_rng``):
+
+* ``normal_weights``  W ~ N(0, 0.02) drawn in f64, stored f32, row-chunked
+  so that the 128256 x 4096 output-head shape never holds f64 for the whole
+  matrix at once.
+* ``normal_x``        x ~ N(0, 1) drawn in f64, stored f32, shape [batch, k].
+* ``q8_0_random``     Q8_0 records drawn directly: q uniform in [-127, 127],
+  d = float16(max of 32 |N(0, 0.02)| draws / 127), the d field first
+  (bytes 0-1, little-endian) then the 32 codes.
+* ``random_records``  records of any format with every byte uniform except
+  the fp16 scale fields, which get finite positive values from a stated
+  range: every bit pattern of the packed scales, mins and codes occurs, so
+  decoders see all of them.
+
+Byte offsets of the fp16 fields (the only layout facts used here):
+Q8_0 d @0; Q4_K d @0, dmin @2; Q6_K d @208.  Per-row int8: codes
+[n_out*k] then f32 scales at the next 16-byte boundary.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = {"q8_0": (32, 34), "q4_k": (256, 144), "q6_k": (256, 210), "i8_row": (1, 1)}
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.default_rng(seed)
+
+
+def normal_weights(n_out: int, k: int, seed: int, std: float = 0.02,
+                   chunk_rows: int = 4096) -> np.ndarray:
+    g = rng(seed)
+    out = np.empty((n_out, k), dtype=np.float32)
+    for r0 in range(0, n_out, chunk_rows):
+        r1 = min(n_out, r0 + chunk_rows)
+        out[r0:r1] = g.normal(0.0, std, size=(r1 - r0, k))
+    return out
+
+
+def normal_x(batch: int, k: int, seed: int) -> np.ndarray:
+    return rng(seed).normal(0.0, 1.0, size=(batch, k)).astype(np.float32)
+
+
+def weight_bytes(fmt: str, n_out: int, k: int) -> int:
+    if fmt == "i8_row":
+        return (n_out * k + 15) // 16 * 16 + 4 * n_out
+    qk, bb = BLOCK[fmt]
+    assert k % qk == 0
+    return n_out * (k // qk) * bb
+
+
+def q8_0_random(n_out: int, k: int, seed: int) -> np.ndarray:
+    """Q8_0 records with q ~ U{-127..127} and d = f16(max|N(0,0.02)|/127)."""
+    assert k % 32 == 0
+    g = rng(seed)
+    nblk = n_out * (k // 32)
+    q = g.integers(-127, 128, size=(nblk, 32), dtype=np.int64).astype(np.int8)
+    n = g.normal(0.0, 0.02, size=(nblk, 32))
+    d = (np.abs(n).max(axis=1) / 127.0).astype(np.float16)
+    rec = np.empty((nblk, 34), dtype=np.uint8)
+    rec[:, 0:2] = d.astype("<f2").view(np.uint8).reshape(nblk, 2)
+    rec[:, 2:34] = q.view(np.uint8)
+    return rec.reshape(-1)
+
+
+def _f16_field(g: np.random.Generator, n: int, lo: float, hi: float) -> np.ndarray:
+    v = g.uniform(lo, hi, size=n).astype(np.float16)
+    return v.astype("<f2").view(np.uint8).reshape(n, 2)
+
+
+def random_records(fmt: str, n_out: int, k: int, seed: int,
+                   d_range=(2e-5, 4e-4), dmin_range=(1e-4, 2e-3)) -> np.ndarray:
+    """Uniform random bytes with finite positive fp16 scale fields."""
+    g = rng(seed)
+    if fmt == "i8_row":
+        total = weight_bytes(fmt, n_out, k)
+        buf = np.zeros(total, dtype=np.uint8)
+        buf[: n_out * k] = g.integers(0, 256, size=n_out * k, dtype=np.int64).astype(np.uint8)
+        soff = (n_out * k + 15) // 16 * 16
+        s = g.uniform(1e-4, 4e-4, size=n_out).astype(np.float32)
+        buf[soff: soff + 4 * n_out] = s.astype("<f4").view(np.uint8)
+        return buf
+    qk, bb = BLOCK[fmt]
+    assert k % qk == 0
+    nblk = n_out * (k // qk)
+    rec = g.integers(0, 256, size=(nblk, bb), dtype=np.int64).astype(np.uint8)
+    if fmt == "q8_0":
+        rec[:, 0:2] = _f16_field(g, nblk, *d_range)
+    elif fmt == "q4_k":
+        rec[:, 0:2] = _f16_field(g, nblk, *d_range)
+        rec[:, 2:4] = _f16_field(g, nblk, *dmin_range)
+    elif fmt == "q6_k":
+        rec[:, 208:210] = _f16_field(g, nblk, *d_range)
+    return rec.reshape(-1)
