@@ -1,0 +1,131 @@
+/*
+ * pq.h -- C ABI of the block-quantized mat-vec library for GB300 (sm_103a).
+ *
+ * The operation: the decode-step mat-vec y = W x with W kept in
+ * block-quantized form and decoded on the fly, "a fused dequantize+mat-vec
+ * that never expands weights back to f32" (ember pull request "Project
+ * scaffold: modules, CLI, and correctness harness", quant.rs description),
+ * applied to the row-major mat-vec "that dominates a decode step" (same
+ * page, tensor.rs description).  The block formats are the K-family and
+ * Q8_0 formats that the PESTI README ("What This Is", "Architecture")
+ * dequantizes byte-exactly, plus the per-row symmetric int8 format of the
+ * ember page.  The inferno README ("Design notes") fixes the boundary
+ * style: contiguous row-major buffers in and out.
+ *
+ * Layouts (all little-endian; the pages print none, these are the public
+ * GGUF layouts read as a byte specification):
+ *   PQ_Q8_0   34 B per 32 weights: f16 d, int8 q[32].        w = d*q
+ *   PQ_Q4_K  144 B per 256 weights: f16 d, f16 dmin, 12 B of packed 6-bit
+ *            (scale, min) pairs for 8 sub-blocks of 32, 128 B of 4-bit q.
+ *            w = (d*sc)*q - dmin*m
+ *   PQ_Q6_K  210 B per 256 weights: 128 B low 4 bits, 64 B high 2 bits,
+ *            int8 sc[16] (one per 16 weights), f16 d.   w = (d*sc)*(q-32)
+ *   PQ_I8_ROW per-row symmetric int8: int8 q[n_out*k] row-major, then at the
+ *            next 16-byte boundary f32 scale[n_out].      w = scale[r]*q
+ * W is n_out rows; row r holds k/QK consecutive blocks (QK = 32, 256, 256, 1),
+ * rows contiguous, no padding.
+ *
+ * Ownership and threading: the caller allocates and owns every buffer (device
+ * memory, e.g. from cudaMalloc or a framework allocator).  The library
+ * allocates nothing and keeps no state beyond a per-device record of the
+ * device's properties, so calls are reentrant and may run concurrently on
+ * different streams.  Calls are asynchronous on `stream` (NULL = legacy
+ * default stream); a fault during execution surfaces at the caller's next
+ * synchronization.  All argument checks run on the host before any launch,
+ * so a rejected call launches nothing.
+ */
+#ifndef PQ_H
+#define PQ_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* == cudaStream_t */
+
+typedef enum {
+    PQ_Q8_0 = 0,
+    PQ_Q4_K = 1,
+    PQ_Q6_K = 2,
+    PQ_I8_ROW = 3
+} pq_fmt;
+
+/* Status codes. */
+#define PQ_OK 0
+#define PQ_ERR_ARG (-1)      /* null pointer, or n_out / k / batch <= 0, or y aliases x or w */
+#define PQ_ERR_FMT (-2)      /* unknown format */
+#define PQ_ERR_K (-3)        /* k not a multiple of the format's block size QK */
+#define PQ_ERR_ALIGN (-4)    /* w_blocks or x not 16-byte aligned, y/out not 4-byte aligned */
+#define PQ_ERR_SIZE (-5)     /* byte or element counts overflow 64-bit arithmetic */
+#define PQ_ERR_DEVICE (-6)   /* current device is not compute capability 10.3 (sm_103) */
+#define PQ_ERR_LAUNCH (-7)   /* the CUDA launch itself failed (cudaGetLastError after launch) */
+#define PQ_ERR_KERNEL (-8)   /* unknown kernel id passed to pq_gemv_kernel */
+
+/*
+ * y[b][r] = sum_i w(r, i) * x[b][i]   for b < batch, r < n_out.
+ *
+ *   w_blocks  device, pq_weight_bytes(fmt, n_out, k) bytes in the layout above,
+ *             16-byte aligned.  Read only.
+ *   x         device f32 [batch][k] row-major, 16-byte aligned.  Read only.
+ *   y         device f32 [batch][n_out] row-major; fully overwritten (not
+ *             accumulated into).  Must not overlap w_blocks or x.
+ *   batch     >= 1.  Batches above 16 are processed in chunks of at most 16.
+ *
+ * Accuracy: partial sums are accumulated in f32; the result agrees with the
+ * exact dot product of the decoded f32 weights within
+ * 2e-3 * RMS(y) + 1e-6 (see the tests).  Deterministic: repeated calls with the
+ * same inputs give bit-identical y.  There is no host fallback: every step
+ * runs in this library's CUDA kernels.
+ */
+int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k,
+            const float *x, int batch, float *y, struct CUstream_st *stream);
+
+/*
+ * out[r][i] = w(r, i) as f32, row-major [n_out][k], bit-identical to the
+ * layout rules above (one f32 rounding for Q4_K's final subtraction and for
+ * PQ_I8_ROW's product; every other step is exact).
+ *   out  device, 4 * n_out * k bytes, 4-byte aligned, must not overlap w_blocks.
+ */
+int pq_dequant(pq_fmt fmt, const void *w_blocks, int n_out, int k,
+               float *out, struct CUstream_st *stream);
+
+/* Bytes of a whole W in the given format; 0 when fmt is unknown, n_out or k
+ * is <= 0, or k is not a multiple of the block size. */
+size_t pq_weight_bytes(pq_fmt fmt, int n_out, int k);
+
+/* Static description of a status code (never NULL). */
+const char *pq_strerror(int status);
+
+/*
+ * Kernel selection, for tests and tuning.  pq_gemv picks a kernel from
+ * (fmt, batch, n_out, k); pq_gemv_kernel runs a named one instead:
+ *   PQ_KERNEL_AUTO     the same choice pq_gemv makes
+ *   PQ_KERNEL_GENERIC  warp-per-row kernel, any format / shape / batch
+ *   PQ_KERNEL_STREAM   bulk-copy ring + integer dot products (Q4_K, Q8_0,
+ *                      Q6_K, I8_ROW; batch <= 4)
+ *   PQ_KERNEL_TC       tcgen05 tensor-core kernel (Q4_K, batch >= 2)
+ * A kernel that cannot run the given case returns PQ_ERR_KERNEL without
+ * launching anything.
+ */
+#define PQ_KERNEL_AUTO (-1)
+#define PQ_KERNEL_GENERIC 0
+#define PQ_KERNEL_STREAM 1
+#define PQ_KERNEL_TC 2
+int pq_gemv_kernel(pq_fmt fmt, const void *w_blocks, int n_out, int k,
+                   const float *x, int batch, float *y, struct CUstream_st *stream,
+                   int kernel);
+
+/* The kernel id pq_gemv would choose for this case (>= 0), or a status < 0
+ * for arguments it would reject. */
+int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch);
+
+/* Number of kernel launches one pq_gemv call with these arguments makes. */
+int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQ_H */

@@ -1,0 +1,240 @@
+// Generic fused dequant + mat-vec: one warp per output row, any format,
+// any shape, batch processed in chunks of up to 4 columns.
+//
+// This is the plain form of the operation (ember pull request, quant.rs:
+// "fused dequantize+mat-vec that never expands weights back to f32"): the
+// warp walks its row's blocks, each lane decodes 8 weights per Q4_K / Q6_K
+// super-block (or per Q8_0 block group) to f32 in registers, multiplies by
+// x (read through the read-only cache; x is small and shared by every warp
+// of the SM) and accumulates in f32; a shuffle tree reduces the 32 lanes.
+// It serves every case the specialised kernels do not, and is their
+// reference point in the tests.
+
+#include "pq_device.cuh"
+#include "pq_internal.h"
+
+namespace pqk {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <int NB>
+__device__ __forceinline__ void fma8(float (&acc)[NB], const float (&wv)[8], const float *x,
+                                     int64_t k, int64_t i0, bool split4) {
+    // weights i0..i0+7, or (split4) i0..i0+3 and i0+32..i0+35
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float *xb = x + b * k + i0;
+        const float4 a = ldg_f4(xb);
+        const float4 c = ldg_f4(xb + (split4 ? 32 : 4));
+        acc[b] = fmaf(wv[0], a.x, acc[b]);
+        acc[b] = fmaf(wv[1], a.y, acc[b]);
+        acc[b] = fmaf(wv[2], a.z, acc[b]);
+        acc[b] = fmaf(wv[3], a.w, acc[b]);
+        acc[b] = fmaf(wv[4], c.x, acc[b]);
+        acc[b] = fmaf(wv[5], c.y, acc[b]);
+        acc[b] = fmaf(wv[6], c.z, acc[b]);
+        acc[b] = fmaf(wv[7], c.w, acc[b]);
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_q4_k(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                      float *__restrict__ y, int64_t ldy) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const int nb = k / 256;
+    const uint8_t *wr = w + (int64_t)row * nb * 144;
+    const int c = lane >> 3, p0 = (lane & 7) * 4;
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+#pragma unroll 2
+    for (int blk = 0; blk < nb; ++blk) {
+        const uint8_t *bp = wr + (int64_t)blk * 144;
+        const uint32_t dd = ldg_u32(bp);
+        const uint32_t s0 = ldg_u32(bp + 4), s1 = ldg_u32(bp + 8), s2 = ldg_u32(bp + 12);
+        const uint32_t qs = ldg_u32(bp + 16 + 4 * lane);
+        const float d = h2f(dd), dmin = h2f(dd >> 16);
+        int sc0, m0, sc1, m1;
+        q4k_scale_min(s0, s1, s2, 2 * c, sc0, m0);
+        q4k_scale_min(s0, s1, s2, 2 * c + 1, sc1, m1);
+        const float dl0 = d * (float)sc0, ml0 = dmin * (float)m0;
+        const float dl1 = d * (float)sc1, ml1 = dmin * (float)m1;
+        float wv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t byte = (qs >> (8 * i)) & 0xff;
+            wv[i] = dl0 * (float)(byte & 15) - ml0;
+            wv[4 + i] = dl1 * (float)(byte >> 4) - ml1;
+        }
+        fma8<NB>(acc, wv, x, k, (int64_t)blk * 256 + 64 * c + p0, true);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = v;
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_q6_k(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                      float *__restrict__ y, int64_t ldy) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const int nb = k / 256;
+    const uint8_t *wr = w + (int64_t)row * nb * 210;
+    const int h = lane >> 4, t = (lane & 15) >> 2, l0 = 8 * (lane & 3);
+    const int ql_off = 64 * h + l0 + 32 * (t & 1), qh_off = 128 + 32 * h + l0;
+    const int nib = (t >= 2) ? 4 : 0, hsh = 2 * t;
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+#pragma unroll 2
+    for (int blk = 0; blk < nb; ++blk) {
+        const uint8_t *bp = wr + (int64_t)blk * 210;
+        const float d = h2f(ldg_u16(bp + 208));
+        const float ds = d * (float)(int)(int8_t)__ldg(bp + 192 + (lane >> 1));
+        float wv[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const uint32_t ql = ldg_u16(bp + ql_off + i), qh = ldg_u16(bp + qh_off + i);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int lo4 = (ql >> (8 * e + nib)) & 15;
+                const int hi2 = (qh >> (8 * e + hsh)) & 3;
+                wv[i + e] = ds * (float)((lo4 | (hi2 << 4)) - 32);
+            }
+        }
+        fma8<NB>(acc, wv, x, k, (int64_t)blk * 256 + 8 * lane, false);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = v;
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_q8_0(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                      float *__restrict__ y, int64_t ldy) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const int nb = k / 32;
+    const uint8_t *wr = w + (int64_t)row * nb * 34;
+    const int part = lane & 3;
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    for (int g = 0; g < nb; g += 8) {
+        const int blk = g + (lane >> 2);
+        if (blk < nb) {
+            const uint8_t *bp = wr + (int64_t)blk * 34;
+            const float d = h2f(ldg_u16(bp));
+            float wv[8];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const uint32_t q2 = ldg_u16(bp + 2 + 8 * part + i);
+                wv[i] = d * (float)(int8_t)(q2 & 0xff);
+                wv[i + 1] = d * (float)(int8_t)(q2 >> 8);
+            }
+            fma8<NB>(acc, wv, x, k, (int64_t)blk * 32 + 8 * part, false);
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = v;
+    }
+}
+
+// Per-row int8: lanes stride the row 4 codes at a time when k % 4 == 0
+// (row starts are then 4-byte aligned), else one code at a time.
+template <int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_i8_row(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                        float *__restrict__ y, int64_t ldy, int64_t soff) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const uint8_t *wr = w + (int64_t)row * k;
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    if ((k & 3) == 0) {
+        for (int i = 4 * lane; i < k; i += 128) {
+            const uint32_t q = ldg_u32(wr + i);
+            const float q0 = (float)(int8_t)(q & 0xff), q1 = (float)(int8_t)((q >> 8) & 0xff);
+            const float q2 = (float)(int8_t)((q >> 16) & 0xff), q3 = (float)(int8_t)(q >> 24);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float4 a = ldg_f4(x + (int64_t)b * k + i);
+                acc[b] = fmaf(q0, a.x, acc[b]);
+                acc[b] = fmaf(q1, a.y, acc[b]);
+                acc[b] = fmaf(q2, a.z, acc[b]);
+                acc[b] = fmaf(q3, a.w, acc[b]);
+            }
+        }
+    } else {
+        for (int i = lane; i < k; i += 32) {
+            const float q = (float)(int8_t)__ldg(wr + i);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) acc[b] = fmaf(q, __ldg(x + (int64_t)b * k + i), acc[b]);
+        }
+    }
+    const float s = __ldg(reinterpret_cast<const float *>(w + soff) + row);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = s * v;
+    }
+}
+
+template <int NB>
+cudaError_t launch_nb(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x,
+                      float *y, int64_t ldy, cudaStream_t s) {
+    const int grid = (int)((n_out + kWarps - 1) / kWarps);
+    const int n = (int)n_out, kk = (int)k;
+    switch (fmt) {
+    case PQ_Q4_K: gemv_generic_q4_k<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_Q6_K: gemv_generic_q6_k<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_Q8_0: gemv_generic_q8_0<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_I8_ROW:
+        gemv_generic_i8_row<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy,
+                                                          i8row_scale_offset(n_out, k));
+        break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// x is [batch][k], y is [batch][ldy]; columns are processed 4 at a time.
+cudaError_t launch_gemv_generic(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
+                                const float *x, int batch, float *y, int64_t ldy,
+                                cudaStream_t s) {
+    for (int b0 = 0; b0 < batch; b0 += 4) {
+        const int nb = batch - b0 < 4 ? batch - b0 : 4;
+        const float *xb = x + (int64_t)b0 * k;
+        float *yb = y + (int64_t)b0 * ldy;
+        cudaError_t e;
+        switch (nb) {
+        case 1: e = launch_nb<1>(fmt, w, n_out, k, xb, yb, ldy, s); break;
+        case 2: e = launch_nb<2>(fmt, w, n_out, k, xb, yb, ldy, s); break;
+        case 3: e = launch_nb<3>(fmt, w, n_out, k, xb, yb, ldy, s); break;
+        default: e = launch_nb<4>(fmt, w, n_out, k, xb, yb, ldy, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace pqk

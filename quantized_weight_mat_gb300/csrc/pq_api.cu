@@ -1,0 +1,217 @@
+// C ABI of the library: argument checks, kernel choice, launches.
+//
+// Every check runs on the host before any launch, so a rejected call never
+// touches the GPU.  Nothing is allocated here; the only state is a
+// per-device record of properties, filled once per device.
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "pq_internal.h"
+
+namespace pqk {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+bool g_ok[kMaxDevices];
+
+void fill_info(int dev) {
+    DeviceInfo &d = g_info[dev];
+    int v = 0;
+    g_ok[dev] = false;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return;
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return;
+    if (cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return;
+    d.smem_optin = (size_t)v;
+    if (cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return;
+    g_ok[dev] = true;
+}
+}  // namespace
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(g_once[dev], fill_info, dev);
+    return g_ok[dev] ? &g_info[dev] : nullptr;
+}
+
+}  // namespace pqk
+
+using namespace pqk;
+
+namespace {
+
+bool valid_fmt(int fmt) { return fmt >= PQ_Q8_0 && fmt <= PQ_I8_ROW; }
+
+// Bytes of W, or -1 when the shape is invalid / overflows.
+int64_t weight_bytes64(int fmt, int64_t n_out, int64_t k) {
+    if (!valid_fmt(fmt) || n_out <= 0 || k <= 0) return -1;
+    if (k % kQK[fmt]) return -1;
+    if (n_out > (INT64_C(1) << 40) / k) return -1;   // n_out*k <= 2^40 weights
+    if (fmt == PQ_I8_ROW) return i8row_scale_offset(n_out, k) + 4 * n_out;
+    return n_out * (k / kQK[fmt]) * kBlockBytes[fmt];
+}
+
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+int check_common(int fmt, const void *w, int n_out, int k) {
+    if (!valid_fmt(fmt)) return PQ_ERR_FMT;
+    if (!w || n_out <= 0 || k <= 0) return PQ_ERR_ARG;
+    if (k % kQK[fmt]) return PQ_ERR_K;
+    if (weight_bytes64(fmt, n_out, k) < 0) return PQ_ERR_SIZE;
+    if ((uintptr_t)w % 16) return PQ_ERR_ALIGN;
+    return PQ_OK;
+}
+
+int check_device(const DeviceInfo **out) {
+    const DeviceInfo *dev = device_info();
+    if (!dev || dev->major != 10 || dev->minor != 3) return PQ_ERR_DEVICE;
+    *out = dev;
+    return PQ_OK;
+}
+
+int check_gemv(int fmt, const void *w, int n_out, int k, const float *x, int batch,
+               const float *y) {
+    int st = check_common(fmt, w, n_out, k);
+    if (st) return st;
+    if (!x || !y || batch <= 0) return PQ_ERR_ARG;
+    if ((int64_t)batch * n_out > (INT64_C(1) << 40) || (int64_t)batch * k > (INT64_C(1) << 40))
+        return PQ_ERR_SIZE;
+    if ((uintptr_t)x % 16 || (uintptr_t)y % 4) return PQ_ERR_ALIGN;
+    const int64_t ybytes = 4 * (int64_t)batch * n_out;
+    if (overlaps(y, ybytes, w, weight_bytes64(fmt, n_out, k)) ||
+        overlaps(y, ybytes, x, 4 * (int64_t)batch * k))
+        return PQ_ERR_ARG;
+    return PQ_OK;
+}
+
+// Kernel for one chunk of `nb` batch columns.
+int choose(int fmt, int64_t n_out, int64_t k, int nb) {
+    if (nb >= 5 && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
+    if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
+    return PQ_KERNEL_GENERIC;
+}
+
+// Chunking of the batch: chunks of up to 16 columns; a chunk that no
+// tensor-core kernel takes is split further into chunks of up to 4.
+template <class F>
+int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &&f) {
+    for (int b0 = 0; b0 < batch;) {
+        int nb = batch - b0 < 16 ? batch - b0 : 16;
+        int kern = forced >= 0 ? forced : choose(fmt, n_out, k, nb);
+        if (kern != PQ_KERNEL_TC && nb > 4) nb = 4;
+        if (kern == PQ_KERNEL_STREAM && !stream_supported(fmt, n_out, k, nb)) return PQ_ERR_KERNEL;
+        if (kern == PQ_KERNEL_TC && !tc_supported(fmt, n_out, k, nb)) return PQ_ERR_KERNEL;
+        int st = f(kern, b0, nb);
+        if (st) return st;
+        b0 += nb;
+    }
+    return PQ_OK;
+}
+
+int gemv_impl(int fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
+              float *y, cudaStream_t stream, int kernel) {
+    int st = check_gemv(fmt, w_blocks, n_out, k, x, batch, y);
+    if (st) return st;
+    if (kernel < PQ_KERNEL_AUTO || kernel > PQ_KERNEL_TC) return PQ_ERR_KERNEL;
+    const DeviceInfo *dev = nullptr;
+    if ((st = check_device(&dev))) return st;
+    const uint8_t *w = static_cast<const uint8_t *>(w_blocks);
+    // validate every chunk before the first launch
+    st = for_each_chunk(fmt, n_out, k, batch, kernel, [](int, int, int) { return PQ_OK; });
+    if (st) return st;
+    return for_each_chunk(fmt, n_out, k, batch, kernel, [&](int kern, int b0, int nb) {
+        const float *xb = x + (int64_t)b0 * k;
+        float *yb = y + (int64_t)b0 * n_out;
+        cudaError_t e;
+        if (kern == PQ_KERNEL_TC)
+            e = launch_gemv_tc(fmt, w, n_out, k, xb, nb, yb, n_out, stream, *dev);
+        else if (kern == PQ_KERNEL_STREAM)
+            e = launch_gemv_stream(fmt, w, n_out, k, xb, nb, yb, n_out, stream, *dev);
+        else
+            e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, yb, n_out, stream);
+        return e == cudaSuccess ? PQ_OK : PQ_ERR_LAUNCH;
+    });
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pq_weight_bytes(pq_fmt fmt, int n_out, int k) {
+    const int64_t n = weight_bytes64((int)fmt, n_out, k);
+    return n < 0 ? 0 : (size_t)n;
+}
+
+const char *pq_strerror(int status) {
+    switch (status) {
+    case PQ_OK: return "ok";
+    case PQ_ERR_ARG: return "invalid argument (null pointer, non-positive size, or overlapping output)";
+    case PQ_ERR_FMT: return "unknown quantization format";
+    case PQ_ERR_K: return "k is not a multiple of the format's block size";
+    case PQ_ERR_ALIGN: return "misaligned pointer (w and x need 16 bytes, y and out need 4 or 16)";
+    case PQ_ERR_SIZE: return "sizes overflow";
+    case PQ_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
+    case PQ_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case PQ_ERR_KERNEL: return "the requested kernel does not support this case";
+    }
+    return "unknown status";
+}
+
+int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
+            float *y, struct CUstream_st *stream) {
+    return gemv_impl((int)fmt, w_blocks, n_out, k, x, batch, y, stream, PQ_KERNEL_AUTO);
+}
+
+int pq_gemv_kernel(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x,
+                   int batch, float *y, struct CUstream_st *stream, int kernel) {
+    return gemv_impl((int)fmt, w_blocks, n_out, k, x, batch, y, stream, kernel);
+}
+
+int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch) {
+    int st = check_common((int)fmt, (const void *)16, n_out, k);
+    if (st) return st;
+    if (batch <= 0) return PQ_ERR_ARG;
+    return choose((int)fmt, n_out, k, batch < 16 ? batch : 16);
+}
+
+int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch) {
+    int st = check_common((int)fmt, (const void *)16, n_out, k);
+    if (st) return st;
+    if (batch <= 0) return PQ_ERR_ARG;
+    int launches = 0;
+    st = for_each_chunk((int)fmt, n_out, k, batch, PQ_KERNEL_AUTO, [&](int, int, int) {
+        ++launches;
+        return PQ_OK;
+    });
+    return st ? st : launches;
+}
+
+int pq_dequant(pq_fmt fmt, const void *w_blocks, int n_out, int k, float *out,
+               struct CUstream_st *stream) {
+    int st = check_common((int)fmt, w_blocks, n_out, k);
+    if (st) return st;
+    if (!out) return PQ_ERR_ARG;
+    if ((uintptr_t)out % 16) return PQ_ERR_ALIGN;
+    if (overlaps(out, 4 * (int64_t)n_out * k, w_blocks, weight_bytes64((int)fmt, n_out, k)))
+        return PQ_ERR_ARG;
+    const DeviceInfo *dev = nullptr;
+    if ((st = check_device(&dev))) return st;
+    cudaError_t e = launch_dequant((int)fmt, static_cast<const uint8_t *>(w_blocks), n_out, k, out,
+                                   stream);
+    return e == cudaSuccess ? PQ_OK : PQ_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Device-side helpers shared by the kernels of this library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace pqk {
+
+// IEEE binary16 bits -> f32 (exact hardware conversion).
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+    return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xffffu)));
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const unsigned int *>(p));
+}
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const unsigned short *>(p));
+}
+__device__ __forceinline__ uint4 ldg_u128(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ float4 ldg_f4(const float *p) {
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// The 6-bit (scale, min) pair of sub-block j (0..7) of a Q4_K super-block.
+// s0, s1, s2 are the 12 packed bytes as three little-endian words:
+//   j < 4 : sc = bits 0-5 of byte j,          m = bits 0-5 of byte j+4
+//   j >= 4: sc = low nibble of byte j+4 | (bits 6-7 of byte j-4) << 4
+//           m  = high nibble of byte j+4 | (bits 6-7 of byte j) << 4
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j,
+                                              int &sc, int &m) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        m = (s1 >> (8 * j)) & 63;
+    } else {
+        const int b = 8 * (j - 4);
+        sc = ((s2 >> b) & 15) | (((s0 >> (b + 6)) & 3) << 4);
+        m = ((s2 >> (b + 4)) & 15) | (((s1 >> (b + 6)) & 3) << 4);
+    }
+}
+
+}  // namespace pqk

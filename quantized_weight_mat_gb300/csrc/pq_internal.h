@@ -1,0 +1,48 @@
+// Internal interface between the C ABI (pq_api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pq.h"
+
+namespace pqk {
+
+constexpr int kQK[4] = {32, 256, 256, 1};        // weights per block
+constexpr int kBlockBytes[4] = {34, 144, 210, 1}; // bytes per block
+
+// Byte offset of the f32 scales of a per-row int8 matrix.
+inline int64_t i8row_scale_offset(int64_t n_out, int64_t k) { return (n_out * k + 15) / 16 * 16; }
+
+struct DeviceInfo {
+    int sm_count;
+    int major, minor;
+    size_t smem_optin;   // max dynamic shared memory per block (opt-in)
+    int l2_bytes;
+};
+
+// Cached per-device properties of the current device; nullptr on failure.
+const DeviceInfo *device_info();
+
+// Launchers: arguments already validated; return cudaError_t of the launch.
+cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, float *out,
+                           cudaStream_t s);
+
+cudaError_t launch_gemv_generic(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
+                                const float *x, int batch, float *y, int64_t ldy,
+                                cudaStream_t s);
+
+// Streaming kernel (bulk-copy ring).  `supported` reports whether it can run
+// this case; the launcher handles batch <= 4.
+bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch);
+cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
+                               const float *x, int batch, float *y, int64_t ldy,
+                               cudaStream_t s, const DeviceInfo &dev);
+
+// Tensor-core kernel (tcgen05): Q4_K, batch chunks of 8 or 16.
+bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch);
+cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
+                           const float *x, int batch, float *y, int64_t ldy,
+                           cudaStream_t s, const DeviceInfo &dev);
+
+}  // namespace pqk

@@ -81,7 +81,7 @@ def random_records(fmt: str, n_out: int, k: int, seed: int,
     if fmt == "i8_row":
         total = weight_bytes(fmt, n_out, k)
         buf = np.zeros(total, dtype=np.uint8)
-        buf[: n_out * k] = g.integers(0, 256, size=n_out * k, dtype=np.int64).astype(np.uint8)
+        buf[: n_out * k] = np.frombuffer(g.bytes(n_out * k), dtype=np.uint8)
         soff = (n_out * k + 15) // 16 * 16
         s = g.uniform(1e-4, 4e-4, size=n_out).astype(np.float32)
         buf[soff: soff + 4 * n_out] = s.astype("<f4").view(np.uint8)
@@ -89,7 +89,7 @@ def random_records(fmt: str, n_out: int, k: int, seed: int,
     qk, bb = BLOCK[fmt]
     assert k % qk == 0
     nblk = n_out * (k // qk)
-    rec = g.integers(0, 256, size=(nblk, bb), dtype=np.int64).astype(np.uint8)
+    rec = np.frombuffer(g.bytes(nblk * bb), dtype=np.uint8).reshape(nblk, bb).copy()
     if fmt == "q8_0":
         rec[:, 0:2] = _f16_field(g, nblk, *d_range)
     elif fmt == "q4_k":

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching a GPU."""
+import os
+import re
+
+import pytest
+
+import oracle
+import quantized_weight_mat_gb300 as pq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from quantized_weight_mat_gb300 import build
+    build.build()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"pq_gemv", "pq_dequant", "pq_weight_bytes", "pq_strerror"} <= set(names)
+    lib = pq.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(pq.EXPORTS)
+
+
+def test_weight_bytes_agree_with_oracle():
+    for fmt in ("q8_0", "q4_k", "q6_k", "i8_row"):
+        for n_out, k in [(1, 256), (7, 512), (896, 896 if fmt in ("q8_0", "i8_row") else 1024),
+                         (128256, 4096)]:
+            assert pq.pq_weight_bytes(fmt, n_out, k) == oracle.weight_bytes(fmt, n_out, k)
+    assert pq.pq_weight_bytes("q4_k", 4, 100) == 0
+    assert pq.pq_weight_bytes(7, 4, 256) == 0
+    assert pq.pq_weight_bytes("q4_k", 0, 256) == 0
+    assert pq.pq_weight_bytes("q4_k", 1 << 30, 1 << 30) == 0     # overflow guard
+
+
+def test_strerror_covers_every_code():
+    for st in range(0, -9, -1):
+        s = pq.pq_strerror(st)
+        assert s and s != "unknown status"
+    assert pq.pq_strerror(-99) == "unknown status"
+
+
+A16 = 1 << 20        # a 16-byte aligned fake address (never dereferenced)
+
+
+@pytest.mark.parametrize("args,status", [
+    (("q4_k", A16, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_OK),
+    ((9, A16, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_ERR_FMT),
+    (("q4_k", 0, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 4, 256, 0, 1, A16 * 3), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 4, 256, A16 * 2, 1, 0), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 0, 256, A16 * 2, 1, A16 * 3), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 4, 0, A16 * 2, 1, A16 * 3), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 4, 256, A16 * 2, 0, A16 * 3), pq.PQ_ERR_ARG),
+    (("q4_k", A16, 4, 100, A16 * 2, 1, A16 * 3), pq.PQ_ERR_K),
+    (("q8_0", A16, 4, 48, A16 * 2, 1, A16 * 3), pq.PQ_ERR_K),
+    (("q4_k", A16 + 8, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_ERR_ALIGN),
+    (("q4_k", A16, 4, 256, A16 * 2 + 4, 1, A16 * 3), pq.PQ_ERR_ALIGN),
+    (("q4_k", A16, 4, 256, A16 * 2, 1, A16 * 3 + 2), pq.PQ_ERR_ALIGN),
+    (("q4_k", A16, 4, 256, A16 * 2, 1, A16 + 16), pq.PQ_ERR_ARG),       # y overlaps w
+    (("q4_k", A16, 4, 256, A16 * 2, 1, A16 * 2 + 512), pq.PQ_ERR_ARG),  # y overlaps x
+    (("q4_k", A16, 1 << 30, 1 << 20, A16 * 2, 1, A16 * 3), pq.PQ_ERR_SIZE),
+])
+def test_gemv_argument_checks(args, status):
+    import torch
+    st = pq.lib().pq_gemv(pq._fmt(args[0]), *args[1:], 0)
+    if status == pq.PQ_OK:
+        # valid arguments reach the device check; without a GPU that fails
+        if torch.cuda.is_available():
+            pytest.skip("would launch on a real GPU with fake pointers")
+        assert st == pq.PQ_ERR_DEVICE
+    else:
+        assert st == status
+
+
+def test_dequant_argument_checks():
+    L = pq.lib()
+    assert L.pq_dequant(1, A16, 4, 256, 0, 0) == pq.PQ_ERR_ARG
+    assert L.pq_dequant(1, A16, 4, 256, A16 * 2 + 4, 0) == pq.PQ_ERR_ALIGN
+    assert L.pq_dequant(1, A16, 4, 255, A16 * 2, 0) == pq.PQ_ERR_K
+    assert L.pq_dequant(5, A16, 4, 256, A16 * 2, 0) == pq.PQ_ERR_FMT
+    assert L.pq_dequant(1, A16, 4, 256, A16 + 32, 0) == pq.PQ_ERR_ARG   # out overlaps w
+
+
+def test_kernel_choice_table():
+    # pure host logic: which kernel and how many launches a call makes
+    assert pq.pq_gemv_choice("q4_k", 4096, 4096, 0) == pq.PQ_ERR_ARG
+    assert pq.pq_gemv_choice("q4_k", 4096, 100, 1) == pq.PQ_ERR_K
+    for fmt, k in (("q4_k", 4096), ("q6_k", 4096), ("q8_0", 896), ("i8_row", 100)):
+        for b in (1, 2, 3, 4, 8, 16, 17, 40):
+            c = pq.pq_gemv_choice(fmt, 4096, k, b)
+            assert c in (pq.KERNEL_GENERIC, pq.KERNEL_STREAM, pq.KERNEL_TC)
+            n = pq.pq_gemv_launches(fmt, 4096, k, b)
+            assert (b + 15) // 16 <= n <= (b + 3) // 4
+
+
+def test_bad_kernel_id_rejected():
+    assert pq.lib().pq_gemv_kernel(1, A16, 4, 256, A16 * 2, 1, A16 * 3, 0, 7) == pq.PQ_ERR_KERNEL

@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Dequant must be bit-exact; the mat-vec must satisfy
+max|y_gpu - y_ref| <= 2e-3 * RMS(y_ref) + 1e-6 (RMS over all outputs of the call).
+Every output buffer carries a guard band that must stay untouched.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import quantized_weight_mat_gb300 as pq
+from pqcases import tolerance_ok, weights, x_for
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 64
+SENTINEL = np.float32(np.frombuffer(np.uint32(0x7fc0beef).tobytes(), dtype=np.float32)[0])
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup(cuda_ok):
+    from quantized_weight_mat_gb300 import build
+    build.build()
+    import torch
+    torch.cuda.init()
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def out_buf(n):
+    import torch
+    t = torch.empty(n + GUARD, dtype=torch.float32, device="cuda")
+    t.fill_(float(SENTINEL))
+    return t
+
+
+def guard_intact(t, n):
+    g = t[n:].cpu().numpy().view(np.uint32)
+    return bool(np.all(g == np.uint32(0x7fc0beef)))
+
+
+def run_gemv(fmt, w, n_out, k, x, kernel="auto"):
+    import torch
+    batch = x.shape[0]
+    wd, xd = dev(w), dev(x)
+    y = out_buf(batch * n_out)
+    st = pq.pq_gemv_kernel(fmt, wd, n_out, k, xd, batch, y, kernel=kernel, check=False)
+    torch.cuda.synchronize()
+    if st == pq.PQ_ERR_KERNEL:
+        return None
+    assert st == 0, pq.pq_strerror(st)
+    assert guard_intact(y, batch * n_out)
+    return y[: batch * n_out].cpu().numpy().reshape(batch, n_out)
+
+
+# ------------------------------------------------------------------ dequant
+
+DQ_CASES = [
+    ("q8_0", 1, 32), ("q8_0", 7, 96), ("q8_0", 129, 896), ("q8_0", 300, 4096),
+    ("q4_k", 1, 256), ("q4_k", 7, 768), ("q4_k", 129, 4096), ("q4_k", 37, 14336),
+    ("q6_k", 1, 256), ("q6_k", 7, 768), ("q6_k", 129, 4096), ("q6_k", 9, 14336),
+    ("i8_row", 1, 1), ("i8_row", 7, 13), ("i8_row", 129, 100), ("i8_row", 33, 4096),
+]
+
+
+@pytest.mark.parametrize("kind", ["quantized", "random"])
+@pytest.mark.parametrize("fmt,n_out,k", DQ_CASES)
+def test_dequant_bit_exact(fmt, n_out, k, kind):
+    import torch
+    w = weights(fmt, n_out, k, kind, 100 + n_out)
+    ref = oracle.dequant(fmt, w, n_out, k)
+    out = out_buf(n_out * k)
+    pq.pq_dequant(fmt, dev(w), n_out, k, out)
+    torch.cuda.synchronize()
+    got = out[: n_out * k].cpu().numpy().reshape(n_out, k)
+    assert guard_intact(out, n_out * k)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ mat-vec, small shapes
+
+GEMV_SHAPES = {
+    "q8_0": [(1, 32), (7, 96), (129, 896), (300, 4096)],
+    "q4_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (37, 14336)],
+    "q6_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (9, 14336)],
+    "i8_row": [(1, 1), (7, 13), (129, 100), (300, 4096), (33, 2048)],
+}
+CASES = [(f, n, k) for f, shapes in GEMV_SHAPES.items() for (n, k) in shapes]
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16, 17])
+@pytest.mark.parametrize("kernel", ["auto", "generic", "stream", "tc"])
+@pytest.mark.parametrize("fmt,n_out,k", CASES)
+def test_gemv_parity(fmt, n_out, k, kernel, batch):
+    w = weights(fmt, n_out, k, "random" if n_out % 2 else "quantized", 200 + n_out)
+    x = x_for(batch, k, 300 + batch)
+    y = run_gemv(fmt, w, n_out, k, x, kernel)
+    if y is None:
+        assert kernel in ("stream", "tc"), "generic and auto take every case"
+        pytest.skip(f"{kernel} kernel does not take this case")
+    ref = oracle.gemv(fmt, w, n_out, k, x)
+    ok, err, bound = tolerance_ok(y, ref)
+    assert ok, f"max err {err:.3g} > {bound:.3g}"
+
+
+@pytest.mark.parametrize("fmt,n_out,k,batch", [("q4_k", 4096, 4096, 1), ("q6_k", 1000, 4096, 2),
+                                               ("q4_k", 4096, 4096, 16), ("q8_0", 896, 896, 1)])
+def test_gemv_deterministic(fmt, n_out, k, batch):
+    import torch
+    w = weights(fmt, n_out, k, "random", 7)
+    x = x_for(batch, k, 8)
+    wd, xd = dev(w), dev(x)
+    ys = []
+    for _ in range(3):
+        y = torch.empty(batch * n_out, dtype=torch.float32, device="cuda")
+        pq.pq_gemv(fmt, wd, n_out, k, xd, batch, y)
+        ys.append(y.cpu().numpy())
+    torch.cuda.synchronize()
+    assert all(np.array_equal(ys[0].view(np.uint32), v.view(np.uint32)) for v in ys[1:])
+
+
+def test_gemv_one_hot_x_gives_the_column():
+    # one-hot x: the exact result is one decoded column; the dot product has a
+    # single nonzero term, so every kernel must return it exactly
+    fmt, n_out, k = "q4_k", 513, 4096
+    w = weights(fmt, n_out, k, "quantized", 11)
+    W = oracle.dequant(fmt, w, n_out, k)
+    x = np.zeros((4, k), dtype=np.float32)
+    for b, col in enumerate((0, 255, 2049, 4095)):
+        x[b, col] = 1.0
+    for kernel in ("generic", "stream", "auto"):
+        y = run_gemv(fmt, w, n_out, k, x, kernel)
+        if y is None:
+            continue
+        for b, col in enumerate((0, 255, 2049, 4095)):
+            np.testing.assert_allclose(y[b], W[:, col], rtol=0, atol=1e-7 * np.abs(W).max())
+
+
+def test_errors_on_device_launch_nothing():
+    import torch
+    w = dev(weights("q4_k", 8, 256, "random", 1))
+    x = torch.zeros(256 + 4, dtype=torch.float32, device="cuda")
+    y = out_buf(8)
+    assert pq.pq_gemv("q4_k", w, 8, 256, x[1:].data_ptr(), 1, y, check=False) == pq.PQ_ERR_ALIGN
+    assert pq.pq_gemv("q4_k", w, 8, 255, x, 1, y, check=False) == pq.PQ_ERR_K
+    assert pq.pq_gemv("q4_k", w, 8, 256, x, 1, w.data_ptr() + 16, check=False) == pq.PQ_ERR_ARG
+    torch.cuda.synchronize()
+    assert guard_intact(y, 0)     # nothing written anywhere in y
+
+
+# ------------------------------------------------------------------ workload-sized cases
+
+def full_case(fmt, n_out, k, batch, wseed, xseed, kind="quantized"):
+    w = weights(fmt, n_out, k, kind, wseed)
+    x = x_for(batch, k, xseed)
+    y = run_gemv(fmt, w, n_out, k, x, "auto")
+    ref = oracle.gemv(fmt, w, n_out, k, x)
+    ok, err, bound = tolerance_ok(y, ref)
+    assert ok, f"{fmt} {n_out}x{k} b{batch}: max err {err:.3g} > {bound:.3g}"
+    return err / bound
+
+
+def test_workload_q8_0_896():
+    full_case("q8_0", 896, 896, 1, 0, 1)
+
+
+def test_workload_q4_k_4096():
+    full_case("q4_k", 4096, 4096, 1, 20, 21)
+
+
+@pytest.mark.parametrize("j,n_out,k", [(0, 6144, 4096), (1, 4096, 4096), (2, 28672, 4096),
+                                       (3, 4096, 14336)])
+def test_workload_decode_layer_set(j, n_out, k):
+    full_case("q4_k", n_out, k, 1, 30 + 2 * j, 31 + 2 * j)
+
+
+def test_workload_q6_k_output_head():
+    full_case("q6_k", 128256, 4096, 1, 40, 41)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("n_out,k,j", [(14336, 4096, 0), (4096, 14336, 1)])
+def test_workload_small_batch(n_out, k, j, batch):
+    full_case("q4_k", n_out, k, batch, 50 + 2 * j, 51 + 2 * j)
+
+
+def test_workload_dequant_output_head_sampled():
+    # the 2.1 GB f32 output of the 128256 x 4096 head, compared bit for bit on
+    # a sample of rows (first, last, tails of every power-of-two tile size)
+    import torch
+    fmt, n_out, k = "q6_k", 128256, 4096
+    w = weights(fmt, n_out, k, "quantized", 40)
+    out = out_buf(n_out * k)
+    pq.pq_dequant(fmt, dev(w), n_out, k, out)
+    torch.cuda.synchronize()
+    assert guard_intact(out, n_out * k)
+    rows = sorted({0, 1, 127, 128, n_out - 257, n_out - 256, n_out - 2, n_out - 1,
+                   *np.random.default_rng(0).integers(0, n_out, 64).tolist()})
+    bb = 210 * (k // 256)
+    o = out[: n_out * k].view(n_out, k)
+    for r in rows:
+        ref = oracle.dequant(fmt, w[r * bb:(r + 1) * bb], 1, k)[0]
+        assert np.array_equal(o[r].cpu().numpy().view(np.uint32), ref.view(np.uint32)), r
