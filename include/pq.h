@@ -57,7 +57,7 @@ typedef enum {
 #define PQ_ERR_ARG (-1)      /* null pointer, or n_out / k / batch <= 0, or y aliases x or w */
 #define PQ_ERR_FMT (-2)      /* unknown format */
 #define PQ_ERR_K (-3)        /* k not a multiple of the format's block size QK */
-#define PQ_ERR_ALIGN (-4)    /* w_blocks or x not 16-byte aligned, y/out not 4-byte aligned */
+#define PQ_ERR_ALIGN (-4)    /* w_blocks, x or out not 16-byte aligned, or y not 4-byte aligned */
 #define PQ_ERR_SIZE (-5)     /* byte or element counts overflow 64-bit arithmetic */
 #define PQ_ERR_DEVICE (-6)   /* current device is not compute capability 10.3 (sm_103) */
 #define PQ_ERR_LAUNCH (-7)   /* the CUDA launch itself failed (cudaGetLastError after launch) */
@@ -86,7 +86,7 @@ int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k,
  * out[r][i] = w(r, i) as f32, row-major [n_out][k], bit-identical to the
  * layout rules above (one f32 rounding for Q4_K's final subtraction and for
  * PQ_I8_ROW's product; every other step is exact).
- *   out  device, 4 * n_out * k bytes, 4-byte aligned, must not overlap w_blocks.
+ *   out  device, 4 * n_out * k bytes, 16-byte aligned, must not overlap w_blocks.
  */
 int pq_dequant(pq_fmt fmt, const void *w_blocks, int n_out, int k,
                float *out, struct CUstream_st *stream);
@@ -123,6 +123,29 @@ int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch);
 
 /* Number of kernel launches one pq_gemv call with these arguments makes. */
 int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch);
+
+/*
+ * Weight prefetch across kernel boundaries (process-wide, default off).
+ * pq_gemv's batch-1 kernel is launched with programmatic dependent launch: it
+ * may be scheduled while the preceding kernel on the stream is still
+ * finishing, and it always waits for that kernel before reading x or writing
+ * y.  With prefetch enabled it also starts streaming w_blocks before that
+ * wait.  Enable it only when no kernel that runs immediately before a
+ * pq_gemv on its stream writes that call's w_blocks (the usual case: weights
+ * loaded once, then only read).  Copies (cudaMemcpy*) are always waited for.
+ * Returns the previous setting.
+ */
+int pq_set_weight_prefetch(int enable);
+
+/*
+ * Number of bounded waits that ran out in this library's kernels on the
+ * current device since the last reset (reset != 0 clears the count).  Every
+ * barrier wait inside a kernel gives up after 1 s, records the event here
+ * and lets the kernel finish instead of hanging; a nonzero count means the
+ * affected outputs are invalid.  Synchronous (reads device memory).
+ * Returns PQ_ERR_DEVICE if the current device is not sm_103.
+ */
+int pq_wait_timeouts(int reset);
 
 #ifdef __cplusplus
 }

@@ -21,9 +21,11 @@ PQ_OK = 0
 PQ_ERR_ARG, PQ_ERR_FMT, PQ_ERR_K, PQ_ERR_ALIGN = -1, -2, -3, -4
 PQ_ERR_SIZE, PQ_ERR_DEVICE, PQ_ERR_LAUNCH, PQ_ERR_KERNEL = -5, -6, -7, -8
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpq.so")
+LIB_PATH = os.environ.get("PQ_LIB_PATH") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libpq.so")
 EXPORTS = ("pq_gemv", "pq_dequant", "pq_weight_bytes", "pq_strerror",
-           "pq_gemv_kernel", "pq_gemv_choice", "pq_gemv_launches")
+           "pq_gemv_kernel", "pq_gemv_choice", "pq_gemv_launches", "pq_wait_timeouts",
+           "pq_set_weight_prefetch")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +61,10 @@ def lib() -> ctypes.CDLL:
             L.pq_gemv_choice.restype = i32
             L.pq_gemv_launches.argtypes = [i32, i32, i32, i32]
             L.pq_gemv_launches.restype = i32
+            L.pq_wait_timeouts.argtypes = [i32]
+            L.pq_wait_timeouts.restype = i32
+            L.pq_set_weight_prefetch.argtypes = [i32]
+            L.pq_set_weight_prefetch.restype = i32
             _lib = L
     return _lib
 
@@ -125,3 +131,11 @@ def pq_gemv_choice(fmt, n_out: int, k: int, batch: int) -> int:
 
 def pq_gemv_launches(fmt, n_out: int, k: int, batch: int) -> int:
     return int(lib().pq_gemv_launches(_fmt(fmt), int(n_out), int(k), int(batch)))
+
+
+def pq_wait_timeouts(reset: bool = False) -> int:
+    return int(lib().pq_wait_timeouts(1 if reset else 0))
+
+
+def pq_set_weight_prefetch(enable: bool) -> int:
+    return int(lib().pq_set_weight_prefetch(1 if enable else 0))

@@ -1,10 +1,759 @@
-// Streaming kernel placeholder (filled in below by the bulk-copy ring kernel).
+// Weight-streaming fused dequant + mat-vec for batch 1..4 on CUDA cores.
+//
+// The operation is the ember pull request's fused "dequantize+mat-vec that
+// never expands weights back to f32" (quant.rs description) for GGUF-style
+// Q4_K super-blocks (the K-family the PESTI README dequantizes, "What This
+// Is").  At batch 1 it moves 0.5625 B per weight and does 2 flops per
+// weight: it is bound by HBM bandwidth, and the design goal is to keep HBM
+// busy while spending as few issue slots per weight as possible.
+//
+// Common structure (one persistent CTA per SM, each owning a contiguous,
+// balanced range of rows):
+//   * a producer warp streams the CTA's rows through a ring of shared-memory
+//     stages with bulk asynchronous copies (cp.async.bulk; completion counted
+//     in bytes on an mbarrier per stage, slots handed back on a second one);
+//   * x is converted once per CTA into two int8 limbs per element with one
+//     scale per 256 values: x ~= u * (254*xh + xl), |error| <= max|x|/64516,
+//     so each 32-weight sub-block's dot product sum_i q_i*x_i becomes dp4a
+//     integer dot products (exact);
+//   * per super-block the 6-bit scales and mins are applied in 32-bit
+//     integers (H = sum_j sc_j*dot_j over both limbs, M = sum_j m_j*sum X_i),
+//     then a few f32 operations: y += u*(d*(254*H + L) - dmin*M);
+//   * partial sums are reduced with warp shuffles (and, for long rows split
+//     over several warps, in shared memory in a fixed order).
+// No atomics, fixed summation order: results are deterministic.
+//
+// Two kernels share that structure:
+//   gemv_rows_q4_k     batch 1: a stage is a run of whole rows fetched with
+//                      ONE contiguous bulk copy; each lane owns 128 weights
+//                      (half a super-block) of a fixed k range and keeps that
+//                      range of x in registers for the whole kernel;
+//   gemv_stream_q4_k   batch 1..4, any k: a stage is 32 rows x 8 super-blocks
+//                      (one copy per row segment), x read from the shared
+//                      image per stage and reused across a warp's rows.
+//
+// Every mbarrier wait is bounded in time (pq_ptx.cuh); on timeout the
+// kernel records it and the warp stops.
+
+#include "pq_device.cuh"
 #include "pq_internal.h"
+#include "pq_ptx.cuh"
 
 namespace pqk {
-bool stream_supported(int, int64_t, int64_t, int) { return false; }
-cudaError_t launch_gemv_stream(int, const uint8_t *, int64_t, int64_t, const float *, int, float *,
-                               int64_t, cudaStream_t, const DeviceInfo &) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+#ifndef PQ_STREAM_CW
+#define PQ_STREAM_CW 8
+#endif
+#ifndef PQ_STREAM_RPW
+#define PQ_STREAM_RPW 4
+#endif
+constexpr int CW = PQ_STREAM_CW;             // consumer warps
+constexpr int RPW = PQ_STREAM_RPW;           // rows per consumer warp per stage
+constexpr int TR = CW * RPW;                 // rows per tile (<= 32: one copy per producer lane)
+constexpr int KB = 8;                        // super-blocks per row segment
+constexpr int SEG = KB * 144;                // bytes per row segment
+constexpr int STAGE = TR * SEG;              // bytes per stage
+constexpr int MAX_STAGES = 8;
+constexpr int THREADS = (CW + 1) * 32;
+constexpr int kSmemBudget = 227 * 1024;      // sm_103 opt-in shared memory per block
+constexpr int kStaticSmem = 2 * MAX_STAGES * 8;
+
+static_assert(TR <= 32, "one producer lane per row of a tile");
+static_assert(SEG % 16 == 0 && STAGE % 128 == 0, "bulk-copy alignment");
+
+struct Params {
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    long long ldy;
+    int n_out;
+    int k;
+    int nstages;
+};
+
+// Bytes of the per-CTA x image for `nb_cols` columns: two int8 limbs per
+// element plus 16 B of metadata per 64-weight slice.
+inline int x_image_bytes(int64_t k, int nb_cols) { return (int)(nb_cols * (2 * k + (k / 64) * 16)); }
+
+int plan_stages(int64_t k, int nb_cols) {
+    const int64_t avail = kSmemBudget - kStaticSmem - x_image_bytes(k, nb_cols);
+    int64_t s = avail / STAGE;
+    return (int)(s > MAX_STAGES ? MAX_STAGES : s);
 }
+
+// x -> limbs.  Warp per 256-value block q; lane l holds values 8l..8l+7, which
+// lie in sub-block j = l/4.  Layout of one column's image (S = k/64 slices,
+// slice s = 4q + c covers sub-blocks 2c and 2c+1 of block q):
+//   group g (0..7) of slice s at byte (g*S + s)*16:
+//     g0,g1: xh of sub-block 2c (values 0-15, 16-31)   g2,g3: xh of sub-block 2c+1
+//     g4..g7: the same for xl
+//   meta of slice s at byte s*16: {XS_2c, XS_2c+1, u, 0}, XS_j = sum of 254*xh+xl.
+// Consecutive lanes read consecutive 16-byte groups: no bank conflicts.
+__device__ __forceinline__ void prep_x_vals(const float (&v)[8], uint8_t *img, uint8_t *meta,
+                                            int q, int S, int lane) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax * (1.0f / 127.0f);
+    const float inv = amax > 0.f ? 127.0f / amax : 0.f;
+    const float inv2 = amax > 0.f ? (254.0f * 127.0f) / amax : 0.f;
+    uint32_t h[2] = {0, 0}, l[2] = {0, 0};
+    int xs = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int hi = __float2int_rn(v[i] * inv);
+        hi = max(-127, min(127, hi));
+        const float r = fmaf(-s, (float)hi, v[i]);
+        int lo = __float2int_rn(r * inv2);
+        lo = max(-127, min(127, lo));
+        xs += 254 * hi + lo;
+        h[i >> 2] |= (uint32_t)(hi & 0xff) << (8 * (i & 3));
+        l[i >> 2] |= (uint32_t)(lo & 0xff) << (8 * (i & 3));
+    }
+    xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+    xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+    const int j = lane >> 2, c = j >> 1, half = j & 1;
+    const int slice = 4 * q + c;
+    const int g = 2 * half + ((lane & 3) >> 1);
+    const int off8 = 8 * (lane & 1);
+    *reinterpret_cast<uint2 *>(img + (g * S + slice) * 16 + off8) = make_uint2(h[0], h[1]);
+    *reinterpret_cast<uint2 *>(img + ((g + 4) * S + slice) * 16 + off8) = make_uint2(l[0], l[1]);
+    if ((lane & 3) == 0) *reinterpret_cast<int *>(meta + slice * 16 + 4 * half) = xs;
+    if ((lane & 7) == 0) *reinterpret_cast<float *>(meta + slice * 16 + 8) = s * (1.0f / 254.0f);
+}
+
+__device__ __forceinline__ void prep_x_block(const float *xb, uint8_t *img, uint8_t *meta, int q,
+                                             int S, int lane) {
+    const float4 a = ldg_f4(xb + q * 256 + 8 * lane);
+    const float4 b = ldg_f4(xb + q * 256 + 8 * lane + 4);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    prep_x_vals(v, img, meta, q, S, lane);
+}
+
+// The x image of one column, blocks q = first, first+step, ...: the loads of
+// up to four blocks are issued before any of them is converted.
+__device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_t *meta, int nb,
+                                           int S, int first, int step, int lane) {
+    for (int q0 = first; q0 < nb; q0 += 4 * step) {
+        float v[4][8];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int q = q0 + r * step;
+            if (q < nb) {
+                const float4 a = ldg_f4(xb + q * 256 + 8 * lane);
+                const float4 b = ldg_f4(xb + q * 256 + 8 * lane + 4);
+                v[r][0] = a.x; v[r][1] = a.y; v[r][2] = a.z; v[r][3] = a.w;
+                v[r][4] = b.x; v[r][5] = b.y; v[r][6] = b.z; v[r][7] = b.w;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int q = q0 + r * step;
+            if (q < nb) prep_x_vals(v[r], img, meta, q, S, lane);
+        }
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(THREADS, 1) gemv_stream_q4_k(Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.k / 256;
+    const int nchunks = (nb + KB - 1) / KB;
+    const int S = p.k / 64;
+    const int64_t rowbytes = (int64_t)nb * 144;
+    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
+    const int64_t r1 = (int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x;
+    const int ntiles = (int)((r1 - r0 + TR - 1) / TR);
+    const int units = ntiles * nchunks;
+    const int NS = p.nstages;
+    uint8_t *ring = smem;
+    uint8_t *ximg = smem + NS * STAGE;
+    uint8_t *xmeta = ximg + NB * 2 * p.k;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], CW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer ----------------
+        const uint64_t pol = make_evict_first_policy();
+        int slot = 0, tile = 0, ch = 0;
+        uint32_t ph = 0;
+        for (int u = 0; u < units; ++u) {
+            const int64_t row0 = r0 + (int64_t)tile * TR;
+            const int rows = (int)(r1 - row0 < TR ? r1 - row0 : TR);
+            const int kbc = nb - ch * KB < KB ? nb - ch * KB : KB;
+            const uint32_t bytes = (uint32_t)kbc * 144u;
+            int ok = 1;
+            if (lane == 0) {
+                ok = mbar_wait(&empty_bar[slot], ph ^ 1u);
+                if (ok) mbar_arrive_expect_tx(&full_bar[slot], bytes * (uint32_t)rows);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane < rows) {
+                const uint8_t *src = p.w + (row0 + lane) * rowbytes + (int64_t)ch * SEG;
+                bulk_g2s_hint(ring + slot * STAGE + lane * SEG, src, bytes, &full_bar[slot], pol);
+            }
+            if (++slot == NS) { slot = 0; ph ^= 1u; }
+            if (++ch == nchunks) { ch = 0; ++tile; }
+        }
+        return;
+    }
+
+    // ---------------- consumers: x image ----------------
+    for (int b = 0; b < NB; ++b) {
+        const float *xb = p.x + (int64_t)b * p.k;
+        for (int q = warp; q < nb; q += CW)
+            prep_x_block(xb, ximg + b * 2 * p.k, xmeta + b * S * 16, q, S, lane);
+    }
+    named_sync(1, CW * 32);
+
+    // ---------------- consumers: main loop ----------------
+    const int bl = lane >> 2, c = lane & 3;
+    // byte selectors: bytes 2c', 2c'+1 (c' = c & 1) of scale words 0 and 1, and of word 2
+    const uint32_t c2 = 2u * (uint32_t)(c & 1);
+    const uint32_t selP = c2 | ((c2 + 1) << 4) | ((c2 + 4) << 8) | ((c2 + 5) << 12);
+    const uint32_t selQ = c2 | ((c2 + 1) << 4) | (c2 << 8) | ((c2 + 1) << 12);
+    float acc[RPW][NB];
+#pragma unroll
+    for (int t = 0; t < RPW; ++t)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[t][b] = 0.f;
+
+    int slot = 0, tile = 0, ch = 0;
+    uint32_t ph = 0;
+    for (int u = 0; u < units; ++u) {
+        const int64_t row0 = r0 + (int64_t)tile * TR;
+        const int rows = (int)(r1 - row0 < TR ? r1 - row0 : TR);
+        const int kbc = nb - ch * KB < KB ? nb - ch * KB : KB;
+        if (!mbar_wait(&full_bar[slot], ph)) break;
+        const bool active = bl < kbc;
+        const uint8_t *stage = ring + slot * STAGE;
+
+        uint32_t lo[RPW][8], hi[RPW][8];
+        int sc0x16[RPW], sc1[RPW], m0[RPW], m1[RPW];
+        float d16[RPW], dmin[RPW];
+        bool live[RPW];
+#pragma unroll
+        for (int t = 0; t < RPW; ++t) {
+            const int trow = warp * RPW + t;
+            live[t] = active && trow < rows;
+            uint4 hd = make_uint4(0, 0, 0, 0), qa = hd, qb = hd;
+            if (live[t]) {
+                const uint8_t *blk = stage + trow * SEG + bl * 144;
+                hd = *reinterpret_cast<const uint4 *>(blk);
+                qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+                qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+            }
+            const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lo[t][i] = qw[i] & 0x0F0F0F0Fu;
+                hi[t][i] = qw[i] & 0xF0F0F0F0u;   // 16*q: rescaled by d/16 below
+            }
+            // (sc, m) of sub-blocks 2c and 2c+1 as bytes {sc0, sc1, m0, m1}
+            const uint32_t P = __byte_perm(hd.y, hd.z, selP);
+            uint32_t r4;
+            if (c < 2) {
+                r4 = P & 0x3F3F3F3Fu;
+            } else {
+                const uint32_t Q = __byte_perm(hd.w, 0u, selQ);
+                r4 = ((P >> 2) & 0x30303030u) | (Q & 0x00000F0Fu) | ((Q >> 4) & 0x0F0F0000u);
+            }
+            sc0x16[t] = (int)((r4 << 4) & 0xFF0u);
+            sc1[t] = (int)((r4 >> 8) & 0xFFu);
+            m0[t] = (int)((r4 >> 16) & 0xFFu);
+            m1[t] = (int)(r4 >> 24);
+            d16[t] = h2f(hd.x) * 0.0625f;
+            dmin[t] = h2f(hd.x >> 16);
+        }
+
+        if (active) {
+            const int slice = ch * (4 * KB) + lane;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const uint8_t *img = ximg + b * 2 * p.k;
+                uint4 g[8];
+#pragma unroll
+                for (int gi = 0; gi < 8; ++gi)
+                    g[gi] = *reinterpret_cast<const uint4 *>(img + (gi * S + slice) * 16);
+                const int4 mt = *reinterpret_cast<const int4 *>(xmeta + b * S * 16 + slice * 16);
+                const float ub = __int_as_float(mt.z);
+                const uint32_t xh0[8] = {g[0].x, g[0].y, g[0].z, g[0].w, g[1].x, g[1].y, g[1].z, g[1].w};
+                const uint32_t xh1[8] = {g[2].x, g[2].y, g[2].z, g[2].w, g[3].x, g[3].y, g[3].z, g[3].w};
+                const uint32_t xl0[8] = {g[4].x, g[4].y, g[4].z, g[4].w, g[5].x, g[5].y, g[5].z, g[5].w};
+                const uint32_t xl1[8] = {g[6].x, g[6].y, g[6].z, g[6].w, g[7].x, g[7].y, g[7].z, g[7].w};
+#pragma unroll
+                for (int t = 0; t < RPW; ++t) {
+                    if (!live[t]) continue;
+                    int dh0 = 0, dh1 = 0, dl0 = 0, dl1 = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        dh0 = dp4a_ss(lo[t][i], xh0[i], dh0);
+                        dl0 = dp4a_ss(lo[t][i], xl0[i], dl0);
+                        dh1 = dp4a_us(hi[t][i], xh1[i], dh1);
+                        dl1 = dp4a_us(hi[t][i], xl1[i], dl1);
+                    }
+                    const int H = sc0x16[t] * dh0 + sc1[t] * dh1;
+                    const int L = sc0x16[t] * dl0 + sc1[t] * dl1;
+                    const int M = m0[t] * mt.x + m1[t] * mt.y;
+                    const float val = d16[t] * fmaf(254.0f, (float)H, (float)L) - dmin[t] * (float)M;
+                    acc[t][b] = fmaf(ub, val, acc[t][b]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+
+        if (ch == nchunks - 1) {
+#pragma unroll
+            for (int t = 0; t < RPW; ++t) {
+                const int trow = warp * RPW + t;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float v = warp_sum(acc[t][b]);
+                    if (lane == 0 && trow < rows) p.y[b * p.ldy + row0 + trow] = v;
+                    acc[t][b] = 0.f;
+                }
+            }
+        }
+        if (++slot == NS) { slot = 0; ph ^= 1u; }
+        if (++ch == nchunks) { ch = 0; ++tile; }
+    }
+}
+
+template <int NB>
+cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
+    Params p = p0;
+    p.nstages = plan_stages(p.k, NB);
+    const int smem = p.nstages * STAGE + x_image_bytes(p.k, NB);
+    static bool configured = false;   // attribute is per function; setting it twice is harmless
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_stream_q4_k<NB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBudget - kStaticSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    gemv_stream_q4_k<NB><<<grid, THREADS, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Batch-1 kernel with whole-row stages.
+//
+// A row of nb super-blocks is split into G = ceil(nb/16) segments of 16
+// super-blocks (4096 weights); a "row group" of G warps handles a row, warp
+// seg of the group owning segment seg for every row of the kernel.  Lane l of
+// a warp owns super-block seg*16 + l/2 and its half l%2 (chunks 2h, 2h+1 =
+// sub-blocks 4h..4h+3, 128 weights): its x limbs (64 registers) and sub-block
+// sums are loaded once.  NG = CW/G row groups share a stage of RS = 2*NG
+// consecutive rows, fetched with a single bulk copy; group gi takes rows gi
+// and gi+NG of a stage, two stages per loop iteration, and reduces those four
+// rows with one transposed shuffle tree.  With G > 1 the per-warp partials
+// of a row are kept in shared memory and summed in segment order at the end.
+//
+// Launched with programmatic dependent launch: the CTA lets the next kernel
+// on the stream start as soon as it is resident, and waits for the previous
+// kernel (griddepcontrol.wait) before reading x -- and before reading the
+// weights too, unless the caller has declared weights static
+// (pq_set_weight_prefetch), in which case the producer starts streaming them
+// while the previous kernel finishes.
+#ifndef PQ_ROWS_CW
+#define PQ_ROWS_CW 8
+#endif
+namespace rowk {
+constexpr int CW = PQ_ROWS_CW;               // consumer warps
+constexpr int KW = 16;                       // super-blocks per warp segment
+constexpr int RPG = 2;                       // rows per row group per stage
+constexpr int THREADS = (CW + 1) * 32;
+constexpr int MAX_STAGES = 8;
+constexpr int kStatic = 2 * MAX_STAGES * 8;
+
+struct Params {
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    int n_out;
+    int k;
+    int G;          // warps per row
+    int NG;         // row groups
+    int RS;         // rows per stage
+    int nstages;
+    int rows_cap;   // max rows of one CTA (partials buffer, G > 1)
+    int early_w;    // stream weights before waiting on the previous kernel
+};
+
+inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
+
+inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
+
+// Stage plan for (k, n_out, grid): false when this kernel cannot take it.
+inline bool plan(int64_t k, int64_t n_out, int grid, Params &p) {
+    if (k % 256 || grid < 1) return false;
+    const int G = segments(k);
+    if (G < 1 || G > CW) return false;
+    p.G = G;
+    p.NG = CW / G;
+    p.RS = RPG * p.NG;
+    p.rows_cap = (int)((n_out + grid - 1) / grid);
+    const int64_t stage = (int64_t)p.RS * (k / 256) * 144;
+    const int64_t avail = kSmemBudget - kStatic - x_image_bytes(k, 1) - red_bytes(p);
+    int64_t ns = avail / stage;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    p.nstages = (int)ns;
+    return ns >= 2;
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ uint4 lds(uint32_t a) { return lds128(a); }
+__device__ __forceinline__ int byte_of(uint32_t v, int i) {
+    return (int)__byte_perm(v, 0u, 0x4440u | (uint32_t)i);
+}
+
+#ifndef PQ_ROWS_DP2A
+#define PQ_ROWS_DP2A 0
+#endif
+
+// This lane's x for its 128 weights (sub-blocks 4hf..4hf+3 of one
+// super-block), loaded once: X = 254*xh + xl as signed 16-bit pairs (dp2a
+// form) or as the two int8 limbs (dp4a form), plus the sub-block sums of X.
+struct XRegs {
+#if PQ_ROWS_DP2A
+    uint32_t xp[2][2][16];        // [chunk][lo/hi sub-block][pair of positions 2m, 2m+1]
+#else
+    uint32_t hl[2][8], hh[2][8], ll[2][8], lh[2][8];
+#endif
+    int xs[4];                    // sum of X over sub-blocks 4hf+0..3
+    float u;                      // x ~= u * X
+    uint32_t mA, mB, qoff;
+};
+
+// Partial dot product of this lane's 128 weights of one row (super-block at
+// shared address `blk`).
+__device__ __forceinline__ float row_dot(uint32_t blk, const XRegs &X, int hf) {
+    const uint4 hd = lds(blk);
+    const uint4 qa = lds(blk + X.qoff), qb = lds(blk + X.qoff + 16);
+    const uint4 qc = lds(blk + X.qoff + 32), qd = lds(blk + X.qoff + 48);
+    const uint32_t w0[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t w1[8] = {qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
+    // packed 6-bit scales / mins of sub-blocks 4hf..4hf+3, one per byte
+    const uint32_t sc4 = ((hf ? hd.w : hd.y) & X.mA) | ((hd.y >> 2) & X.mB);
+    const uint32_t m4 = ((hf ? (hd.w >> 4) : hd.z) & X.mA) | ((hd.z >> 2) & X.mB);
+    const int M = byte_of(m4, 0) * X.xs[0] + byte_of(m4, 1) * X.xs[1] +
+                  byte_of(m4, 2) * X.xs[2] + byte_of(m4, 3) * X.xs[3];        // |M| < 2^28
+#if PQ_ROWS_DP2A
+    // D_j = sum_i q_i*X_i per sub-block; high nibbles enter as 16*q
+    int e0 = 0, o0 = 0, e1 = 0, o1 = 0, e2 = 0, o2 = 0, e3 = 0, o3 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int ii = i + h;
+            const uint32_t lo0 = w0[ii] & 0x0F0F0F0Fu, hi0 = w0[ii] & 0xF0F0F0F0u;
+            const uint32_t lo1 = w1[ii] & 0x0F0F0F0Fu, hi1 = w1[ii] & 0xF0F0F0F0u;
+            int &a0 = h ? o0 : e0, &a1 = h ? o1 : e1, &a2 = h ? o2 : e2, &a3 = h ? o3 : e3;
+            a0 = dp2a_hi(X.xp[0][0][2 * ii + 1], lo0, dp2a_lo(X.xp[0][0][2 * ii], lo0, a0));
+            a1 = dp2a_hi(X.xp[0][1][2 * ii + 1], hi0, dp2a_lo(X.xp[0][1][2 * ii], hi0, a1));
+            a2 = dp2a_hi(X.xp[1][0][2 * ii + 1], lo1, dp2a_lo(X.xp[1][0][2 * ii], lo1, a2));
+            a3 = dp2a_hi(X.xp[1][1][2 * ii + 1], hi1, dp2a_lo(X.xp[1][1][2 * ii], hi1, a3));
+        }
+    }
+    // |D| <= 32*15*32385 < 2^24; sc*D < 2^30; two of them < 2^31
+    const int Ha = byte_of(sc4, 0) * (e0 + o0) + byte_of(sc4, 1) * ((e1 + o1) >> 4);
+    const int Hb = byte_of(sc4, 2) * (e2 + o2) + byte_of(sc4, 3) * ((e3 + o3) >> 4);
+    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+    return X.u * (d * ((float)Ha + (float)Hb) - dmin * (float)M);
+#else
+    int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0, dh2 = 0, dl2 = 0, dh3 = 0, dl3 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo0 = w0[i] & 0x0F0F0F0Fu, hi0 = w0[i] & 0xF0F0F0F0u;
+        const uint32_t lo1 = w1[i] & 0x0F0F0F0Fu, hi1 = w1[i] & 0xF0F0F0F0u;
+        dh0 = dp4a_ss(lo0, X.hl[0][i], dh0);
+        dl0 = dp4a_ss(lo0, X.ll[0][i], dl0);
+        dh1 = dp4a_us(hi0, X.hh[0][i], dh1);
+        dl1 = dp4a_us(hi0, X.lh[0][i], dl1);
+        dh2 = dp4a_ss(lo1, X.hl[1][i], dh2);
+        dl2 = dp4a_ss(lo1, X.ll[1][i], dl2);
+        dh3 = dp4a_us(hi1, X.hh[1][i], dh3);
+        dl3 = dp4a_us(hi1, X.lh[1][i], dl3);
+    }
+    // even sub-blocks pair with low nibbles (x1), odd ones with high nibbles (x16)
+    const int s0 = byte_of(sc4, 0) << 4, s1 = byte_of(sc4, 1);
+    const int s2 = byte_of(sc4, 2) << 4, s3 = byte_of(sc4, 3);
+    const int H = s0 * dh0 + s1 * dh1 + s2 * dh2 + s3 * dh3;        // |H| < 2^28
+    const int L = s0 * dl0 + s1 * dl1 + s2 * dl2 + s3 * dl3;
+    const float d = h2f(hd.x) * 0.0625f, dmin = h2f(hd.x >> 16);
+    return X.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+#endif
+}
+
+// One loop step: two stages (A, B), rows gi and gi+NG of each; CHECK handles
+// partial stages (and a missing B) at the end of the CTA's rows.
+template <bool CHECK>
+__device__ __forceinline__ void four_rows(float (&pr)[4], uint32_t sA, uint32_t sB, uint32_t rA0,
+                                          uint32_t rA1, int gi, int NG, int nA, int nB,
+                                          const XRegs &X, int hf) {
+    if (!CHECK) {
+        pr[0] = row_dot(sA + rA0, X, hf);
+        pr[1] = row_dot(sA + rA1, X, hf);
+        pr[2] = row_dot(sB + rA0, X, hf);
+        pr[3] = row_dot(sB + rA1, X, hf);
+    } else {
+        pr[0] = gi < nA ? row_dot(sA + rA0, X, hf) : 0.f;
+        pr[1] = gi + NG < nA ? row_dot(sA + rA1, X, hf) : 0.f;
+        pr[2] = gi < nB ? row_dot(sB + rA0, X, hf) : 0.f;
+        pr[3] = gi + NG < nB ? row_dot(sB + rA1, X, hf) : 0.f;
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.k / 256;
+    const int S = p.k / 64;
+    const uint32_t rowbytes = (uint32_t)nb * 144u;
+    const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
+    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
+    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
+    const int units = (nrows + RS - 1) / RS;
+    const int NS = p.nstages;
+    const uint32_t stage_bytes = (uint32_t)RS * rowbytes;
+    uint8_t *ximg = smem + (size_t)NS * stage_bytes;
+    uint8_t *xmeta = ximg + 2 * p.k;
+    float *red = reinterpret_cast<float *>(xmeta + S * 16);
+    const uint32_t ring_s = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], CA);
+        }
+        fence_mbar_init();
+    }
+    grid_dep_launch();   // the next kernel on the stream may start when resident
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer: one contiguous copy per stage ----------------
+        if (lane == 0) {
+            if (!p.early_w) grid_dep_wait();
+            const uint64_t pol = make_evict_first_policy();
+            const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
+            int slot = 0;
+            uint32_t ph = 0;
+            for (int u = 0; u < units; ++u) {
+                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
+                const uint32_t bytes = (uint32_t)rows * rowbytes;
+                if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_g2s_hint(smem + (size_t)slot * stage_bytes, src, bytes, &full_bar[slot], pol);
+                src += (size_t)RS * rowbytes;
+                if (++slot == NS) { slot = 0; ph ^= 1u; }
+            }
+        }
+        return;
+    }
+
+    // ---------------- x image (all consumer warps) ----------------
+    grid_dep_wait();
+    prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
+    named_sync(1, CW * 32);
+    if (warp >= CA) return;
+
+    const int gi = warp / G, seg = warp - gi * G;
+    const int hf = lane & 1;
+    const int kb = seg * KW + (lane >> 1);
+    const bool valid = kb < nb;
+    const int kbc = valid ? kb : nb - 1;       // idle lanes read a real block, weight 0
+
+    XRegs X;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int slice = 4 * kbc + 2 * hf + cc;
+        uint4 g[8];
+#pragma unroll
+        for (int gi2 = 0; gi2 < 8; ++gi2)
+            g[gi2] = *reinterpret_cast<const uint4 *>(ximg + (gi2 * S + slice) * 16);
+        const uint32_t *gw = reinterpret_cast<const uint32_t *>(g);
+#if PQ_ROWS_DP2A
+        // words 0-7: xh of the low sub-block, 8-15: xh of the high one, 16-31: xl
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t h = gw[8 * hs + i], l = gw[16 + 8 * hs + i];
+                int Xv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    Xv[e] = 254 * (int)(int8_t)(h >> (8 * e)) + (int)(int8_t)(l >> (8 * e));
+                X.xp[cc][hs][2 * i] = ((uint32_t)Xv[0] & 0xFFFFu) | ((uint32_t)Xv[1] << 16);
+                X.xp[cc][hs][2 * i + 1] = ((uint32_t)Xv[2] & 0xFFFFu) | ((uint32_t)Xv[3] << 16);
+            }
+#else
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            X.hl[cc][i] = gw[i];
+            X.hh[cc][i] = gw[8 + i];
+            X.ll[cc][i] = gw[16 + i];
+            X.lh[cc][i] = gw[24 + i];
+        }
+#endif
+        const int4 mt = *reinterpret_cast<const int4 *>(xmeta + slice * 16);
+        X.xs[2 * cc] = mt.x;
+        X.xs[2 * cc + 1] = mt.y;
+        X.u = __int_as_float(mt.z);
+    }
+    if (!valid) X.u = 0.f;
+    X.mA = hf ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+    X.mB = hf ? 0x30303030u : 0u;
+    X.qoff = 16u + 64u * (uint32_t)hf;
+    const uint32_t lane_base = ring_s + (uint32_t)kbc * 144u;
+    const uint32_t rA0 = (uint32_t)gi * rowbytes, rA1 = (uint32_t)(gi + NG) * rowbytes;
+    const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+    // the row this lane's reduced value belongs to: 0,1 of stage A, 2,3 of stage B
+    const int my_t = gi + (b3 ? NG : 0);
+    const int full_pairs = nrows / (2 * RS);    // iterations whose two stages are full
+
+    int slot = 0;
+    uint32_t ph = 0;
+    bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
+    for (int u = 0; u < units; u += 2) {
+        const bool hasB = u + 1 < units;
+        const int slotA = slot;
+        const uint32_t phA = ph;
+        if (++slot == NS) { slot = 0; ph ^= 1u; }
+        const int slotB = slot;
+        const uint32_t phB = ph;
+        if (hasB) {
+            if (++slot == NS) { slot = 0; ph ^= 1u; }
+        }
+        if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
+        if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
+        const uint32_t sA = lane_base + (uint32_t)slotA * stage_bytes;
+        const uint32_t sB = lane_base + (uint32_t)slotB * stage_bytes;
+        const int nA = nrows - u * RS < RS ? nrows - u * RS : RS;
+        const int nB = hasB ? (nrows - (u + 1) * RS < RS ? nrows - (u + 1) * RS : RS) : 0;
+        float pr[4];
+        if (u / 2 < full_pairs)
+            four_rows<false>(pr, sA, sB, rA0, rA1, gi, NG, nA, nB, X, hf);
+        else
+            four_rows<true>(pr, sA, sB, rA0, rA1, gi, NG, nA, nB, X, hf);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&empty_bar[slotA]);
+            if (hasB) mbar_arrive(&empty_bar[slotB]);
+        }
+        // transposed reduction of the four rows: lanes 0-7 end with row 0,
+        // 8-15 row 1, 16-23 row 2, 24-31 row 3
+        float a0 = b4 ? pr[2] : pr[0], a1 = b4 ? pr[3] : pr[1];
+        a0 += __shfl_xor_sync(0xffffffffu, b4 ? pr[0] : pr[2], 16);
+        a1 += __shfl_xor_sync(0xffffffffu, b4 ? pr[1] : pr[3], 16);
+        float v = (b3 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, b3 ? a0 : a1, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if ((lane & 7) == 0) {
+            const int n_here = b4 ? nB : nA;
+            if (my_t < n_here) {
+                const int row = (u + (b4 ? 1 : 0)) * RS + my_t;     // relative to r0
+                if (G == 1)
+                    p.y[r0 + row] = v;
+                else
+                    red[row * G + seg] = v;
+            }
+        }
+    }
+    if (G > 1) {
+        named_sync(2, CA * 32);
+        for (int i = warp * 32 + lane; i < nrows; i += CA * 32) {
+            float sum = red[i * G];
+            for (int g2 = 1; g2 < G; ++g2) sum += red[i * G + g2];
+            p.y[r0 + i] = sum;
+        }
+    }
+}
+
+cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
+                   int grid, cudaStream_t s, int early_w) {
+    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w};
+    if (!plan(k, n_out, grid, p)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * 144 + x_image_bytes(k, 1) + red_bytes(p);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_rows_q4_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBudget - kStatic);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_q4_k, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+}  // namespace rowk
+
+}  // namespace
+
+unsigned stream_wait_timeouts(bool reset) {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    if (reset) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_wait_timeouts, &z, sizeof(z));
+    }
+    return v;
+}
+
+bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch) {
+    if (fmt != PQ_Q4_K || batch < 1 || batch > 4 || n_out < 1) return false;
+    if (k % 256 || k > (INT64_C(1) << 20)) return false;
+    return plan_stages(k, batch) >= 2;
+}
+
+cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
+                               const float *x, int batch, float *y, int64_t ldy,
+                               cudaStream_t s, const DeviceInfo &dev) {
+    if (!stream_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
+    Params p{w, x, y, (long long)ldy, (int)n_out, (int)k, 0};
+    const int grid = (int)(n_out < dev.sm_count ? n_out : dev.sm_count);
+    rowk::Params rp{};
+    if (batch == 1 && rowk::plan(k, n_out, grid, rp))
+        return rowk::launch(w, n_out, k, x, y, grid, s, weight_prefetch());
+    switch (batch) {
+    case 1: return launch_nb<1>(p, grid, s);
+    case 2: return launch_nb<2>(p, grid, s);
+    case 3: return launch_nb<3>(p, grid, s);
+    default: return launch_nb<4>(p, grid, s);
+    }
+}
+
 }  // namespace pqk

@@ -37,6 +37,12 @@ void fill_info(int dev) {
 }
 }  // namespace
 
+namespace {
+std::atomic<int> g_weight_prefetch{0};
+}
+
+int weight_prefetch() { return g_weight_prefetch.load(std::memory_order_relaxed); }
+
 const DeviceInfo *device_info() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -197,6 +203,17 @@ int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch) {
         return PQ_OK;
     });
     return st ? st : launches;
+}
+
+int pq_set_weight_prefetch(int enable) {
+    return g_weight_prefetch.exchange(enable ? 1 : 0);
+}
+
+int pq_wait_timeouts(int reset) {
+    const DeviceInfo *dev = nullptr;
+    if (check_device(&dev)) return PQ_ERR_DEVICE;
+    const unsigned n = stream_wait_timeouts(reset != 0) + tc_wait_timeouts(reset != 0);
+    return n > 0x7fffffffu ? 0x7fffffff : (int)n;
 }
 
 int pq_dequant(pq_fmt fmt, const void *w_blocks, int n_out, int k, float *out,

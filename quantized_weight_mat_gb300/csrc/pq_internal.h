@@ -45,4 +45,12 @@ cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                            const float *x, int batch, float *y, int64_t ldy,
                            cudaStream_t s, const DeviceInfo &dev);
 
+// Process-wide: may kernels read weights before the preceding kernel on the
+// stream has finished (set by pq_set_weight_prefetch)?
+int weight_prefetch();
+
+// Bounded waits that ran out in each kernel file since the last reset.
+unsigned stream_wait_timeouts(bool reset);
+unsigned tc_wait_timeouts(bool reset);
+
 }  // namespace pqk
