@@ -135,13 +135,13 @@ __device__ __forceinline__ void prep_x_block(const float *xb, uint8_t *img, uint
 }
 
 // The x image of one column, blocks q = first, first+step, ...: the loads of
-// up to four blocks are issued before any of them is converted.
+// up to eight blocks are in flight before any of them is converted.
 __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_t *meta, int nb,
                                            int S, int first, int step, int lane) {
-    for (int q0 = first; q0 < nb; q0 += 4 * step) {
-        float v[4][8];
+    for (int q0 = first; q0 < nb; q0 += 8 * step) {
+        float v[8][8];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 8; ++r) {
             const int q = q0 + r * step;
             if (q < nb) {
                 const float4 a = ldg_f4(xb + q * 256 + 8 * lane);
@@ -151,7 +151,7 @@ __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_
             }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 8; ++r) {
             const int q = q0 + r * step;
             if (q < nb) prep_x_vals(v[r], img, meta, q, S, lane);
         }
@@ -505,22 +505,17 @@ __device__ __forceinline__ float row_dot(uint32_t blk, const XRegs &X, int hf) {
 #endif
 }
 
-// One loop step: two stages (A, B), rows gi and gi+NG of each; CHECK handles
-// partial stages (and a missing B) at the end of the CTA's rows.
+// Rows gi and gi+NG of one stage (lane base address s); CHECK handles a
+// partial last stage.
 template <bool CHECK>
-__device__ __forceinline__ void four_rows(float (&pr)[4], uint32_t sA, uint32_t sB, uint32_t rA0,
-                                          uint32_t rA1, int gi, int NG, int nA, int nB,
-                                          const XRegs &X, int hf) {
+__device__ __forceinline__ void two_rows(float &p0, float &p1, uint32_t s, uint32_t rA0, uint32_t rA1,
+                                         int gi, int NG, int n, const XRegs &X, int hf) {
     if (!CHECK) {
-        pr[0] = row_dot(sA + rA0, X, hf);
-        pr[1] = row_dot(sA + rA1, X, hf);
-        pr[2] = row_dot(sB + rA0, X, hf);
-        pr[3] = row_dot(sB + rA1, X, hf);
+        p0 = row_dot(s + rA0, X, hf);
+        p1 = row_dot(s + rA1, X, hf);
     } else {
-        pr[0] = gi < nA ? row_dot(sA + rA0, X, hf) : 0.f;
-        pr[1] = gi + NG < nA ? row_dot(sA + rA1, X, hf) : 0.f;
-        pr[2] = gi < nB ? row_dot(sB + rA0, X, hf) : 0.f;
-        pr[3] = gi + NG < nB ? row_dot(sB + rA1, X, hf) : 0.f;
+        p0 = gi < n ? row_dot(s + rA0, X, hf) : 0.f;
+        p1 = gi + NG < n ? row_dot(s + rA1, X, hf) : 0.f;
     }
 }
 
@@ -633,7 +628,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
     const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
     // the row this lane's reduced value belongs to: 0,1 of stage A, 2,3 of stage B
     const int my_t = gi + (b3 ? NG : 0);
-    const int full_pairs = nrows / (2 * RS);    // iterations whose two stages are full
 
     int slot = 0;
     uint32_t ph = 0;
@@ -648,22 +642,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
         if (hasB) {
             if (++slot == NS) { slot = 0; ph ^= 1u; }
         }
-        if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
-        if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
         const uint32_t sA = lane_base + (uint32_t)slotA * stage_bytes;
         const uint32_t sB = lane_base + (uint32_t)slotB * stage_bytes;
         const int nA = nrows - u * RS < RS ? nrows - u * RS : RS;
         const int nB = hasB ? (nrows - (u + 1) * RS < RS ? nrows - (u + 1) * RS : RS) : 0;
         float pr[4];
-        if (u / 2 < full_pairs)
-            four_rows<false>(pr, sA, sB, rA0, rA1, gi, NG, nA, nB, X, hf);
+        // stage A: wait, compute its two rows, hand the slot back; then stage B
+        if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
+        if (nA == RS)
+            two_rows<false>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
         else
-            four_rows<true>(pr, sA, sB, rA0, rA1, gi, NG, nA, nB, X, hf);
+            two_rows<true>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&empty_bar[slotA]);
-            if (hasB) mbar_arrive(&empty_bar[slotB]);
-        }
+        if (lane == 0) mbar_arrive(&empty_bar[slotA]);
+        if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
+        if (nB == RS)
+            two_rows<false>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+        else
+            two_rows<true>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+        __syncwarp();
+        if (lane == 0 && hasB) mbar_arrive(&empty_bar[slotB]);
         // transposed reduction of the four rows: lanes 0-7 end with row 0,
         // 8-15 row 1, 16-23 row 2, 24-31 row 3
         float a0 = b4 ? pr[2] : pr[0], a1 = b4 ? pr[3] : pr[1];
