@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from one ncu capture, keyed by the sha256 of the kernel source it was
 # taken on; any edit of that source makes the figure stale (reported as null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"29941bd02c932b34": 66_145_280}
 
 
 def set_bytes():
@@ -402,6 +402,31 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_shape(args):
+    """One shape launched back to back (for profiler captures and sweeps):
+    --shape fmt:NxK[:batch], weights rotating over copies larger than L2."""
+    import torch
+    from quantized_weight_mat_gb300 import build
+    import quantized_weight_mat_gb300 as pq
+    build.build()
+    parts = args.shape.split(":")
+    fmt = parts[0]
+    n, k = (int(v) for v in parts[1].split("x"))
+    batch = int(parts[2]) if len(parts) > 2 else 1
+    nbytes = synth.weight_bytes(fmt, n, k)
+    copies = max(2, -(-400_000_000 // nbytes))
+    base = torch.from_numpy(synth.random_records(fmt, n, k, seed=5)).cuda()
+    W = [base] + [base.clone() for _ in range(copies - 1)]
+    x = torch.from_numpy(synth.normal_x(batch, k, seed=6)).cuda()
+    y = torch.empty(batch * n, device="cuda")
+    torch.cuda.synchronize()
+    for i in range(args.launches):
+        pq.pq_gemv_kernel(fmt, W[i % copies], n, k, x, batch, y, kernel=args.kernel)
+    torch.cuda.synchronize()
+    print(json.dumps({"shape": args.shape, "launches": args.launches, "kernel": args.kernel,
+                      "checksum": float(y.double().abs().sum())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -414,7 +439,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None, help="fmt:NxK[:batch]: launch one shape only")
+    ap.add_argument("--launches", type=int, default=6)
+    ap.add_argument("--kernel", default="auto")
     args = ap.parse_args()
+    if args.shape:
+        run_shape(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
