@@ -402,16 +402,18 @@ inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
 
 inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
 
-// Stage plan for (k, n_out, grid): false when this kernel cannot take it.
-inline bool plan(int64_t k, int64_t n_out, int grid, Params &p) {
-    if (k % 256 || grid < 1) return false;
+// Stage plan for (k, n_out, grid) with super-blocks of `block_bytes`; false
+// when this kernel cannot take the shape (rows must be whole multiples of
+// 16 bytes for the bulk copy).
+inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p) {
+    if (k % 256 || grid < 1 || ((k / 256) * block_bytes) % 16) return false;
     const int G = segments(k);
     if (G < 1 || G > CW) return false;
     p.G = G;
     p.NG = CW / G;
     p.RS = RPG * p.NG;
     p.rows_cap = (int)((n_out + grid - 1) / grid);
-    const int64_t stage = (int64_t)p.RS * (k / 256) * 144;
+    const int64_t stage = (int64_t)p.RS * (k / 256) * block_bytes;
     const int64_t avail = kSmemBudget - kStatic - x_image_bytes(k, 1) - red_bytes(p);
     int64_t ns = avail / stage;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
@@ -423,103 +425,210 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 __device__ __forceinline__ uint4 lds(uint32_t a) { return lds128(a); }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
 __device__ __forceinline__ int byte_of(uint32_t v, int i) {
     return (int)__byte_perm(v, 0u, 0x4440u | (uint32_t)i);
 }
+// byte i of v as a signed value
+__device__ __forceinline__ int sbyte_of(uint32_t v, int i) { return (int)(int8_t)(v >> (8 * i)); }
 
-#ifndef PQ_ROWS_DP2A
-#define PQ_ROWS_DP2A 0
-#endif
+// The lane's 64 x limb words from the x image: chunks 2h, 2h+1 of super-block
+// kbc (slices 4kbc+2h, 4kbc+2h+1).  part[0..3] = the four runs of 32
+// positions, in order; meta gives the 32-position sums and the scale u.
+__device__ __forceinline__ void load_x_parts(uint32_t (&xh)[4][8], uint32_t (&xl)[4][8], int (&xs32)[4],
+                                             float &u, const uint8_t *ximg, const uint8_t *xmeta,
+                                             int S, int kbc, int hf) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int slice = 4 * kbc + 2 * hf + cc;
+        uint4 g[8];
+#pragma unroll
+        for (int gi2 = 0; gi2 < 8; ++gi2)
+            g[gi2] = *reinterpret_cast<const uint4 *>(ximg + (gi2 * S + slice) * 16);
+        const uint32_t *gw = reinterpret_cast<const uint32_t *>(g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            xh[2 * cc][i] = gw[i];
+            xh[2 * cc + 1][i] = gw[8 + i];
+            xl[2 * cc][i] = gw[16 + i];
+            xl[2 * cc + 1][i] = gw[24 + i];
+        }
+        const int4 mt = *reinterpret_cast<const int4 *>(xmeta + slice * 16);
+        xs32[2 * cc] = mt.x;
+        xs32[2 * cc + 1] = mt.y;
+        u = __int_as_float(mt.z);
+    }
+}
 
-// This lane's x for its 128 weights (sub-blocks 4hf..4hf+3 of one
-// super-block), loaded once: X = 254*xh + xl as signed 16-bit pairs (dp2a
-// form) or as the two int8 limbs (dp4a form), plus the sub-block sums of X.
-struct XRegs {
-#if PQ_ROWS_DP2A
-    uint32_t xp[2][2][16];        // [chunk][lo/hi sub-block][pair of positions 2m, 2m+1]
-#else
-    uint32_t hl[2][8], hh[2][8], ll[2][8], lh[2][8];
-#endif
-    int xs[4];                    // sum of X over sub-blocks 4hf+0..3
-    float u;                      // x ~= u * X
-    uint32_t mA, mB, qoff;
+// ---------------------------------------------------------------------------
+// Q4_K: lane owns sub-blocks 4h..4h+3 (chunks 2h, 2h+1) of its super-block.
+struct Q4K {
+    static constexpr int kBlockBytes = 144;
+    struct X {
+        uint32_t xh[4][8], xl[4][8];   // limbs of the 4 sub-blocks (32 positions each)
+        int xs[4];                     // sum of X = 254*xh + xl per sub-block
+        float u;                       // x ~= u * X
+        uint32_t mA, mB, qoff;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        load_x_parts(R.xh, R.xl, R.xs, R.u, ximg, xmeta, S, kbc, hf);
+        if (!valid) R.u = 0.f;
+        R.mA = hf ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+        R.mB = hf ? 0x30303030u : 0u;
+        R.qoff = 16u + 64u * (uint32_t)hf;
+    }
+    // Partial dot product of this lane's 128 weights of the row whose
+    // super-block starts at shared address blk.
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint4 hd = lds(blk);
+        const uint4 qa = lds(blk + R.qoff), qb = lds(blk + R.qoff + 16);
+        const uint4 qc = lds(blk + R.qoff + 32), qd = lds(blk + R.qoff + 48);
+        const uint32_t w0[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const uint32_t w1[8] = {qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
+        // packed 6-bit scales / mins of sub-blocks 4h..4h+3, one per byte
+        const uint32_t sc4 = ((hf ? hd.w : hd.y) & R.mA) | ((hd.y >> 2) & R.mB);
+        const uint32_t m4 = ((hf ? (hd.w >> 4) : hd.z) & R.mA) | ((hd.z >> 2) & R.mB);
+        int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0, dh2 = 0, dl2 = 0, dh3 = 0, dl3 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo0 = w0[i] & 0x0F0F0F0Fu, hi0 = w0[i] & 0xF0F0F0F0u;
+            const uint32_t lo1 = w1[i] & 0x0F0F0F0Fu, hi1 = w1[i] & 0xF0F0F0F0u;
+            dh0 = dp4a_ss(lo0, R.xh[0][i], dh0);
+            dl0 = dp4a_ss(lo0, R.xl[0][i], dl0);
+            dh1 = dp4a_us(hi0, R.xh[1][i], dh1);
+            dl1 = dp4a_us(hi0, R.xl[1][i], dl1);
+            dh2 = dp4a_ss(lo1, R.xh[2][i], dh2);
+            dl2 = dp4a_ss(lo1, R.xl[2][i], dl2);
+            dh3 = dp4a_us(hi1, R.xh[3][i], dh3);
+            dl3 = dp4a_us(hi1, R.xl[3][i], dl3);
+        }
+        // even sub-blocks pair with low nibbles (x1), odd ones with high nibbles (x16)
+        const int s0 = byte_of(sc4, 0) << 4, s1 = byte_of(sc4, 1);
+        const int s2 = byte_of(sc4, 2) << 4, s3 = byte_of(sc4, 3);
+        const int H = s0 * dh0 + s1 * dh1 + s2 * dh2 + s3 * dh3;        // |H| < 2^28
+        const int L = s0 * dl0 + s1 * dl1 + s2 * dl2 + s3 * dl3;
+        const int M = byte_of(m4, 0) * R.xs[0] + byte_of(m4, 1) * R.xs[1] +
+                      byte_of(m4, 2) * R.xs[2] + byte_of(m4, 3) * R.xs[3];    // |M| < 2^28
+        const float d = h2f(hd.x) * 0.0625f, dmin = h2f(hd.x >> 16);
+        return R.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+    }
 };
 
-// Partial dot product of this lane's 128 weights of one row (super-block at
-// shared address `blk`).
-__device__ __forceinline__ float row_dot(uint32_t blk, const XRegs &X, int hf) {
-    const uint4 hd = lds(blk);
-    const uint4 qa = lds(blk + X.qoff), qb = lds(blk + X.qoff + 16);
-    const uint4 qc = lds(blk + X.qoff + 32), qd = lds(blk + X.qoff + 48);
-    const uint32_t w0[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    const uint32_t w1[8] = {qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
-    // packed 6-bit scales / mins of sub-blocks 4hf..4hf+3, one per byte
-    const uint32_t sc4 = ((hf ? hd.w : hd.y) & X.mA) | ((hd.y >> 2) & X.mB);
-    const uint32_t m4 = ((hf ? (hd.w >> 4) : hd.z) & X.mA) | ((hd.z >> 2) & X.mB);
-    const int M = byte_of(m4, 0) * X.xs[0] + byte_of(m4, 1) * X.xs[1] +
-                  byte_of(m4, 2) * X.xs[2] + byte_of(m4, 3) * X.xs[3];        // |M| < 2^28
-#if PQ_ROWS_DP2A
-    // D_j = sum_i q_i*X_i per sub-block; high nibbles enter as 16*q
-    int e0 = 0, o0 = 0, e1 = 0, o1 = 0, e2 = 0, o2 = 0, e3 = 0, o3 = 0;
+// ---------------------------------------------------------------------------
+// Q6_K: lane owns half h of its super-block (weights 128h..128h+127): ql bytes
+// 64h..64h+63, qh bytes 32h..32h+31, scales 8h..8h+7.  Blocks are 210 bytes,
+// so a block may start 2 bytes past a 4-byte boundary: the lane loads aligned
+// words and realigns them with one byte permute each (selector fixed per lane,
+// since row and stage sizes are multiples of 16 bytes).
+struct Q6K {
+    static constexpr int kBlockBytes = 210;
+    struct X {
+        uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-position parts t = 0..3
+        int xs[8];                     // sum of X over the 8 sub-blocks of 16
+        float u;
+        uint32_t delta, sel, dsh;      // misalignment (0/2), realign selector, d shift
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t lane_base) {
+        int xs32[4];
+        load_x_parts(R.xh, R.xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
+        for (int sb = 0; sb < 8; ++sb) {
+            int sh = 0, sl = 0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int ii = i + h;
-            const uint32_t lo0 = w0[ii] & 0x0F0F0F0Fu, hi0 = w0[ii] & 0xF0F0F0F0u;
-            const uint32_t lo1 = w1[ii] & 0x0F0F0F0Fu, hi1 = w1[ii] & 0xF0F0F0F0u;
-            int &a0 = h ? o0 : e0, &a1 = h ? o1 : e1, &a2 = h ? o2 : e2, &a3 = h ? o3 : e3;
-            a0 = dp2a_hi(X.xp[0][0][2 * ii + 1], lo0, dp2a_lo(X.xp[0][0][2 * ii], lo0, a0));
-            a1 = dp2a_hi(X.xp[0][1][2 * ii + 1], hi0, dp2a_lo(X.xp[0][1][2 * ii], hi0, a1));
-            a2 = dp2a_hi(X.xp[1][0][2 * ii + 1], lo1, dp2a_lo(X.xp[1][0][2 * ii], lo1, a2));
-            a3 = dp2a_hi(X.xp[1][1][2 * ii + 1], hi1, dp2a_lo(X.xp[1][1][2 * ii], hi1, a3));
+            for (int i = 0; i < 4; ++i) {
+                sh = dp4a_ss(R.xh[sb >> 1][4 * (sb & 1) + i], 0x01010101u, sh);
+                sl = dp4a_ss(R.xl[sb >> 1][4 * (sb & 1) + i], 0x01010101u, sl);
+            }
+            R.xs[sb] = 254 * sh + sl;
         }
+        if (!valid) R.u = 0.f;
+        R.delta = lane_base & 2u;
+        R.sel = R.delta ? 0x5432u : 0x3210u;
+        R.dsh = R.delta ? 16u : 0u;
     }
-    // |D| <= 32*15*32385 < 2^24; sc*D < 2^30; two of them < 2^31
-    const int Ha = byte_of(sc4, 0) * (e0 + o0) + byte_of(sc4, 1) * ((e1 + o1) >> 4);
-    const int Hb = byte_of(sc4, 2) * (e2 + o2) + byte_of(sc4, 3) * ((e3 + o3) >> 4);
-    const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-    return X.u * (d * ((float)Ha + (float)Hb) - dmin * (float)M);
-#else
-    int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0, dh2 = 0, dl2 = 0, dh3 = 0, dl3 = 0;
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint32_t a = blk - R.delta;
+        uint32_t ql[16], qh[8], scw[2];
+        {
+            uint32_t w[17];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t lo0 = w0[i] & 0x0F0F0F0Fu, hi0 = w0[i] & 0xF0F0F0F0u;
-        const uint32_t lo1 = w1[i] & 0x0F0F0F0Fu, hi1 = w1[i] & 0xF0F0F0F0u;
-        dh0 = dp4a_ss(lo0, X.hl[0][i], dh0);
-        dl0 = dp4a_ss(lo0, X.ll[0][i], dl0);
-        dh1 = dp4a_us(hi0, X.hh[0][i], dh1);
-        dl1 = dp4a_us(hi0, X.lh[0][i], dl1);
-        dh2 = dp4a_ss(lo1, X.hl[1][i], dh2);
-        dl2 = dp4a_ss(lo1, X.ll[1][i], dl2);
-        dh3 = dp4a_us(hi1, X.hh[1][i], dh3);
-        dl3 = dp4a_us(hi1, X.lh[1][i], dl3);
+            for (int j = 0; j < 17; ++j) w[j] = lds32(a + 64u * (uint32_t)hf + 4u * (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ql[j] = __byte_perm(w[j], w[j + 1], R.sel);
+        }
+        {
+            uint32_t w[9];
+#pragma unroll
+            for (int j = 0; j < 9; ++j) w[j] = lds32(a + 128u + 32u * (uint32_t)hf + 4u * (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) qh[j] = __byte_perm(w[j], w[j + 1], R.sel);
+        }
+        {
+            uint32_t w[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) w[j] = lds32(a + 192u + 8u * (uint32_t)hf + 4u * (uint32_t)j);
+            scw[0] = __byte_perm(w[0], w[1], R.sel);
+            scw[1] = __byte_perm(w[1], w[2], R.sel);
+        }
+        const uint32_t dw = lds32(a + 208u) >> R.dsh;
+        // 6-bit codes (0..63) of the four parts, four positions per word;
+        // sub-block of part t, word i: 2t + i/4
+        int dh[8], dl[8];
+#pragma unroll
+        for (int sb = 0; sb < 8; ++sb) dh[sb] = dl[sb] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t la = ql[i], lb = ql[8 + i], h = qh[i];
+            const uint32_t q0 = (la & 0x0F0F0F0Fu) | ((h << 4) & 0x30303030u);
+            const uint32_t q1 = (lb & 0x0F0F0F0Fu) | ((h << 2) & 0x30303030u);
+            const uint32_t q2 = ((la >> 4) & 0x0F0F0F0Fu) | (h & 0x30303030u);
+            const uint32_t q3 = ((lb >> 4) & 0x0F0F0F0Fu) | ((h >> 2) & 0x30303030u);
+            const int s = i >> 2;
+            dh[0 + s] = dp4a_us(q0, R.xh[0][i], dh[0 + s]);
+            dl[0 + s] = dp4a_us(q0, R.xl[0][i], dl[0 + s]);
+            dh[2 + s] = dp4a_us(q1, R.xh[1][i], dh[2 + s]);
+            dl[2 + s] = dp4a_us(q1, R.xl[1][i], dl[2 + s]);
+            dh[4 + s] = dp4a_us(q2, R.xh[2][i], dh[4 + s]);
+            dl[4 + s] = dp4a_us(q2, R.xl[2][i], dl[4 + s]);
+            dh[6 + s] = dp4a_us(q3, R.xh[3][i], dh[6 + s]);
+            dl[6 + s] = dp4a_us(q3, R.xl[3][i], dl[6 + s]);
+        }
+        // signed sub-block scales; |H|, |L| < 2^28, |M| < 2^30
+        int H = 0, L = 0, M = 0;
+#pragma unroll
+        for (int sb = 0; sb < 8; ++sb) {
+            const int sc = sbyte_of(scw[sb >> 2], sb & 3);
+            H += sc * dh[sb];
+            L += sc * dl[sb];
+            M += sc * R.xs[sb];
+        }
+        const float d = h2f(dw);
+        return R.u * d * (fmaf(254.0f, (float)H, (float)L) - 32.0f * (float)M);
     }
-    // even sub-blocks pair with low nibbles (x1), odd ones with high nibbles (x16)
-    const int s0 = byte_of(sc4, 0) << 4, s1 = byte_of(sc4, 1);
-    const int s2 = byte_of(sc4, 2) << 4, s3 = byte_of(sc4, 3);
-    const int H = s0 * dh0 + s1 * dh1 + s2 * dh2 + s3 * dh3;        // |H| < 2^28
-    const int L = s0 * dl0 + s1 * dl1 + s2 * dl2 + s3 * dl3;
-    const float d = h2f(hd.x) * 0.0625f, dmin = h2f(hd.x >> 16);
-    return X.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
-#endif
-}
+};
 
 // Rows gi and gi+NG of one stage (lane base address s); CHECK handles a
 // partial last stage.
-template <bool CHECK>
+template <class F, bool CHECK>
 __device__ __forceinline__ void two_rows(float &p0, float &p1, uint32_t s, uint32_t rA0, uint32_t rA1,
-                                         int gi, int NG, int n, const XRegs &X, int hf) {
+                                         int gi, int NG, int n, const typename F::X &X, int hf) {
     if (!CHECK) {
-        p0 = row_dot(s + rA0, X, hf);
-        p1 = row_dot(s + rA1, X, hf);
+        p0 = F::dot(s + rA0, X, hf);
+        p1 = F::dot(s + rA1, X, hf);
     } else {
-        p0 = gi < n ? row_dot(s + rA0, X, hf) : 0.f;
-        p1 = gi + NG < n ? row_dot(s + rA1, X, hf) : 0.f;
+        p0 = gi < n ? F::dot(s + rA0, X, hf) : 0.f;
+        p1 = gi + NG < n ? F::dot(s + rA1, X, hf) : 0.f;
     }
 }
 
-__global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
+template <class F>
+__global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
@@ -527,7 +636,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = p.k / 256;
     const int S = p.k / 64;
-    const uint32_t rowbytes = (uint32_t)nb * 144u;
+    const uint32_t rowbytes = (uint32_t)nb * (uint32_t)F::kBlockBytes;
     const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
     const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
     const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
@@ -581,49 +690,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
     const int kb = seg * KW + (lane >> 1);
     const bool valid = kb < nb;
     const int kbc = valid ? kb : nb - 1;       // idle lanes read a real block, weight 0
+    const uint32_t lane_base = ring_s + (uint32_t)kbc * (uint32_t)F::kBlockBytes;
 
-    XRegs X;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const int slice = 4 * kbc + 2 * hf + cc;
-        uint4 g[8];
-#pragma unroll
-        for (int gi2 = 0; gi2 < 8; ++gi2)
-            g[gi2] = *reinterpret_cast<const uint4 *>(ximg + (gi2 * S + slice) * 16);
-        const uint32_t *gw = reinterpret_cast<const uint32_t *>(g);
-#if PQ_ROWS_DP2A
-        // words 0-7: xh of the low sub-block, 8-15: xh of the high one, 16-31: xl
-#pragma unroll
-        for (int hs = 0; hs < 2; ++hs)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t h = gw[8 * hs + i], l = gw[16 + 8 * hs + i];
-                int Xv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    Xv[e] = 254 * (int)(int8_t)(h >> (8 * e)) + (int)(int8_t)(l >> (8 * e));
-                X.xp[cc][hs][2 * i] = ((uint32_t)Xv[0] & 0xFFFFu) | ((uint32_t)Xv[1] << 16);
-                X.xp[cc][hs][2 * i + 1] = ((uint32_t)Xv[2] & 0xFFFFu) | ((uint32_t)Xv[3] << 16);
-            }
-#else
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            X.hl[cc][i] = gw[i];
-            X.hh[cc][i] = gw[8 + i];
-            X.ll[cc][i] = gw[16 + i];
-            X.lh[cc][i] = gw[24 + i];
-        }
-#endif
-        const int4 mt = *reinterpret_cast<const int4 *>(xmeta + slice * 16);
-        X.xs[2 * cc] = mt.x;
-        X.xs[2 * cc + 1] = mt.y;
-        X.u = __int_as_float(mt.z);
-    }
-    if (!valid) X.u = 0.f;
-    X.mA = hf ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
-    X.mB = hf ? 0x30303030u : 0u;
-    X.qoff = 16u + 64u * (uint32_t)hf;
-    const uint32_t lane_base = ring_s + (uint32_t)kbc * 144u;
+    typename F::X X;
+    F::load(X, ximg, xmeta, S, kbc, hf, valid, lane_base);
     const uint32_t rA0 = (uint32_t)gi * rowbytes, rA1 = (uint32_t)(gi + NG) * rowbytes;
     const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
     // the row this lane's reduced value belongs to: 0,1 of stage A, 2,3 of stage B
@@ -650,16 +720,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
         // stage A: wait, compute its two rows, hand the slot back; then stage B
         if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
         if (nA == RS)
-            two_rows<false>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
+            two_rows<F, false>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
         else
-            two_rows<true>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
+            two_rows<F, true>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slotA]);
         if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
         if (nB == RS)
-            two_rows<false>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+            two_rows<F, false>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
         else
-            two_rows<true>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+            two_rows<F, true>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
         __syncwarp();
         if (lane == 0 && hasB) mbar_arrive(&empty_bar[slotB]);
         // transposed reduction of the four rows: lanes 0-7 end with row 0,
@@ -692,14 +762,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_q4_k(Params p) {
     }
 }
 
+template <class F>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
                    int grid, cudaStream_t s, int early_w) {
     Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w};
-    if (!plan(k, n_out, grid, p)) return cudaErrorInvalidValue;
-    const int smem = p.nstages * p.RS * (int)(k / 256) * 144 + x_image_bytes(k, 1) + red_bytes(p);
+    if (!plan(k, n_out, grid, F::kBlockBytes, p)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_rows_q4_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemBudget - kStatic);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -714,8 +785,18 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_q4_k, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows<F>, p);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Whether the whole-row kernel takes (fmt, k, n_out) at batch 1.
+inline bool takes(int fmt, int64_t k, int64_t n_out) {
+    Params p{};
+    const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
+    const int grid = (int)(n_out < grid_est ? n_out : grid_est);
+    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, p);
+    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p);
+    return false;
 }
 }  // namespace rowk
 
@@ -732,6 +813,7 @@ unsigned stream_wait_timeouts(bool reset) {
 }
 
 bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch) {
+    if (batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out)) return true;
     if (fmt != PQ_Q4_K || batch < 1 || batch > 4 || n_out < 1) return false;
     if (k % 256 || k > (INT64_C(1) << 20)) return false;
     return plan_stages(k, batch) >= 2;
@@ -743,9 +825,10 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
     if (!stream_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
     Params p{w, x, y, (long long)ldy, (int)n_out, (int)k, 0};
     const int grid = (int)(n_out < dev.sm_count ? n_out : dev.sm_count);
-    rowk::Params rp{};
-    if (batch == 1 && rowk::plan(k, n_out, grid, rp))
-        return rowk::launch(w, n_out, k, x, y, grid, s, weight_prefetch());
+    if (batch == 1 && fmt == PQ_Q4_K && rowk::takes(fmt, k, n_out))
+        return rowk::launch<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch());
+    if (batch == 1 && fmt == PQ_Q6_K && rowk::takes(fmt, k, n_out))
+        return rowk::launch<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch());
     switch (batch) {
     case 1: return launch_nb<1>(p, grid, s);
     case 2: return launch_nb<2>(p, grid, s);
