@@ -20,11 +20,13 @@
 //           1-D bulk copy brings that super-block's fp16 x tile;
 //   warps 0-7 decoders: thread (r, h) turns the 128 weights of row r, half h
 //           of the super-block into fp16 sc*q (one LOP3 + one HFMA2 per two
-//           weights) in the K-major no-swizzle layout, 64 weights per slot,
-//           into a ring of eight slots (two super-blocks);
-//   warp 13 MMA issuer (one thread): per super-block the K=16 mins product,
-//           then four tcgen05.mma (M=128, N=2*NBP, K=16) per slot into a TMEM
-//           accumulator;
+//           weights), 64 weights per slot, and write them straight into
+//           tensor memory (tcgen05.st; TMEM lane = row, two K values per
+//           column), a ring of eight slots (two super-blocks);
+//   warp 13 MMA issuer (one thread): per super-block the K=16 mins product
+//           (A from shared memory), then four tcgen05.mma (M=128, N=2*NBP,
+//           K=16, A from tensor memory, x from shared memory) per slot into a
+//           TMEM accumulator;
 //   warps 8-11 epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
 //           lanes 32(w%4).. = its rows), d and dmin from a small ring the
 //           decoders fill, f32 scaling.
@@ -48,18 +50,19 @@ namespace {
 
 constexpr int TM = 128;                       // rows per tile = MMA M
 constexpr int RAW_BYTES = TM * 144;           // one super-block column of a tile
-constexpr int A_SLOT_BYTES = TM * 64 * 2;     // 64 weights per row, fp16
-constexpr int A_SLOTS = 8;                    // two super-blocks
+constexpr int A_SLOTS = 8;                    // two super-blocks of 64-weight slots, in TMEM
+constexpr int A_COL = 256;                    // TMEM column of A slot 0 (32 columns per slot)
+constexpr int TMEM_COLS = 512;
 constexpr int AMIN_BYTES = TM * 16 * 2;
 constexpr int THREADS = 14 * 32;              // 8 decoder, 4 epilogue, producer, MMA warps
 
 // x image of one super-block for N' = 2*NBP columns: main part N' x 256 fp16
 // (K-major, 8x8 core matrices), then the mins part N' x 16.
 template <int NP> __host__ __device__ constexpr int btile_bytes() { return NP * 256 * 2 + NP * 16 * 2; }
-template <int NP> __host__ __device__ constexpr int raw_stages() { return NP == 32 ? 2 : 3; }
+template <int NP> __host__ __device__ constexpr int raw_stages() { return NP == 32 ? 5 : 7; }
 template <int NP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NP>(); }
 template <int NP> __host__ __device__ constexpr int smem_bytes() {
-    return raw_stages<NP>() * stage_bytes<NP>() + A_SLOTS * A_SLOT_BYTES + 2 * AMIN_BYTES + 1024;
+    return raw_stages<NP>() * stage_bytes<NP>() + 2 * AMIN_BYTES + 1024;
 }
 
 // K order inside a super-block: chunk e of A-column a (8 fp16 per 16 bytes)
@@ -78,33 +81,43 @@ __host__ __device__ constexpr int kmaj_off(int n, int K, int sbo) {
 }
 
 // ---------------------------------------------------------------- x image
+// One block per super-block.  Lets the main kernel launch at once
+// (programmatic dependent launch): it sets up and streams weights while this
+// runs, and waits for it only before its first x tile.
 template <int NBP>
 __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, int k, int nb_cols,
                                                  uint8_t *__restrict__ img) {
     constexpr int NP = 2 * NBP;
+    asm volatile("griddepcontrol.launch_dependents;");
     const int sb = blockIdx.x;
     __half *out = reinterpret_cast<__half *>(img + (size_t)sb * btile_bytes<NP>());
     __shared__ float xs[NBP][8];
     const int t = threadIdx.x;
-    // sub-block sums (fixed order)
+    // sub-block sums, fixed order (thread per (column, sub-block), 8 vector loads)
     if (t < NBP * 8) {
         const int b = t / 8, j = t % 8;
         float s = 0.f;
         if (b < nb_cols) {
-            const float *xb = x + (size_t)b * k + sb * 256 + 32 * j;
-            for (int i = 0; i < 32; ++i) s += xb[i];
+            const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)b * k + sb * 256 + 32 * j);
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldg(xb + i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s = s + v[i].x + v[i].y + v[i].z + v[i].w;
         }
         xs[b][j] = s;
     }
-    // main part: thread t = K index
+    // main part: thread t = K index; all column loads in flight together
     {
         const int K = t;
         const int pos = kpos(K / 8, K % 8);
+        float v[NBP];
+#pragma unroll
+        for (int b = 0; b < NBP; ++b) v[b] = b < nb_cols ? __ldg(x + (size_t)b * k + sb * 256 + pos) : 0.f;
 #pragma unroll
         for (int b = 0; b < NBP; ++b) {
-            const float v = b < nb_cols ? x[(size_t)b * k + sb * 256 + pos] : 0.f;
-            const __half hi = __float2half_rn(v);
-            const __half lo = __float2half_rn(v - __half2float(hi));
+            const __half hi = __float2half_rn(v[b]);
+            const __half lo = __float2half_rn(v[b] - __half2float(hi));
             out[kmaj_off(b, K, 4096) / 2] = hi;
             out[kmaj_off(NBP + b, K, 4096) / 2] = lo;
         }
@@ -146,6 +159,28 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+
+// Same with the A operand in tensor memory (column address a_tmem).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// Each thread writes 32 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -195,6 +230,7 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<const uint32_t *>(&v); }
 
 struct TcParams {
+    const uint8_t *w;          // for L2 prefetch of whole tiles (rows are contiguous)
     const uint8_t *x_img;
     float *y;
     long long ldy;
@@ -210,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int NSR = raw_stages<NP>();
     constexpr int STAGE = stage_bytes<NP>();
     constexpr uint32_t IDESC = instr_desc(TM, NP);
-    constexpr uint32_t TCOLS = 4 * NP;   // 2 buffers x (main + mins)
+    static_assert(4 * NP <= A_COL, "accumulators below the A slots");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
@@ -223,8 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // 1024-aligned working area
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *ring = smem;
-    uint8_t *aring = ring + NSR * STAGE;
-    uint8_t *amin = aring + A_SLOTS * A_SLOT_BYTES;
+    uint8_t *amin = ring + NSR * STAGE;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = p.k / 256;
@@ -256,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 13) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_base_sh)),
-                     "r"(TCOLS));
+                     "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -278,6 +313,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t *st = ring + slot * STAGE;
                 mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)STAGE);
                 tma_load_2d(st, &wmap, sb * 144, tile * TM, &raw_full[slot]);
+                // the weights were complete before the x-prep kernel started; the x
+                // image is that kernel's output: wait for it once, before its first use
+                if (g == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NP>(), (uint32_t)btile_bytes<NP>(),
                               &raw_full[slot], pol);
             }
@@ -309,12 +347,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int c = 0; c < 4; ++c) {
                     if ((c & 1) && !dead && !mbar_wait(&a_full[a0 + c], aph)) dead = true;
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(aring + (a0 + c) * A_SLOT_BYTES);
+                    const uint32_t acol = tmem + (uint32_t)(A_COL + 32 * (a0 + c));
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = smem_desc(abase + 256u * ks, 128u, 1024u);
                         const uint64_t bd = smem_desc(bbase + 256u * (4 * c + ks), 128u, 4096u);
-                        if (!dead) mma_f16(d_main, ad, bd, IDESC, (c | ks) ? 1u : 0u);
+                        if (!dead) mma_f16_ta(d_main, acol + 8u * ks, bd, IDESC, (c | ks) ? 1u : 0u);
                     }
                     mma_commit(&a_empty[a0 + c]);
                 }
@@ -330,6 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int b = 0; b < NBP; ++b) yacc[b] = 0.f;
         bool dead = false;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // before any store of y
         for (int g = 0; g < total; ++g) {
             const int buf = g & 1;
             if (!dead && !mbar_wait(&acc_full[buf], (uint32_t)(g >> 1) & 1u)) dead = true;
@@ -379,6 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int h = threadIdx.x >> 7;         // half of the super-block: sub-blocks 4h..4h+3
         const uint32_t mA = h ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
         const uint32_t mB = h ? 0x30303030u : 0u;
+        const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's TMEM lanes
         bool dead = false;
         for (int g = 0; g < total; ++g) {
             const int slot = g % NSR;
@@ -429,24 +468,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t Chi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(-64.0f)));
                 const uint32_t w[8] = {qw[2 * cc].x, qw[2 * cc].y, qw[2 * cc].z, qw[2 * cc].w,
                                        qw[2 * cc + 1].x, qw[2 * cc + 1].y, qw[2 * cc + 1].z, qw[2 * cc + 1].w};
-                uint8_t *aslot = aring + as * A_SLOT_BYTES;
+                // the slot's 64 K values of row r: TMEM column j holds K = 2j, 2j+1
+                uint32_t R[32];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) {
                     const uint32_t w0 = w[2 * a], w1 = w[2 * a + 1];
                     const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-                    uint4 lo, hi;
-                    lo.x = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    lo.y = hfma2_u((s0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    lo.z = hfma2_u((w1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    lo.w = hfma2_u((s1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    hi.x = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    hi.y = hfma2_u((s0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    hi.z = hfma2_u((w1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    hi.w = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    *reinterpret_cast<uint4 *>(aslot + kmaj_off(r, 8 * a, 1024)) = lo;
-                    *reinterpret_cast<uint4 *>(aslot + kmaj_off(r, 8 * (a + 4), 1024)) = hi;
+                    R[4 * a + 0] = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                    R[4 * a + 1] = hfma2_u((s0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                    R[4 * a + 2] = hfma2_u((w1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                    R[4 * a + 3] = hfma2_u((s1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                    R[16 + 4 * a + 0] = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                    R[16 + 4 * a + 1] = hfma2_u((s0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                    R[16 + 4 * a + 2] = hfma2_u((w1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                    R[16 + 4 * a + 3] = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tmem_st32(a_lane + (uint32_t)(A_COL + 32 * as), R);
+                tmem_st_wait();
+                if (cc == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // mins row
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[as]);
             }
@@ -457,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (warp == 13) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
     }
 }
 
@@ -531,9 +571,19 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     }
     const int ntiles = (int)((n_out + TM - 1) / TM);
     const int grid = ntiles < dev.sm_count ? ntiles : dev.sm_count;
-    TcParams p{img, y, (long long)ldy, (int)n_out, (int)k, batch};
-    gemv_tc_q4_k<NBP><<<grid, THREADS, smem_bytes<NP>(), s>>>(map, p);
-    return cudaGetLastError();
+    TcParams p{w, img, y, (long long)ldy, (int)n_out, (int)k, batch};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes<NP>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
