@@ -147,6 +147,34 @@ int pq_set_weight_prefetch(int enable);
  */
 int pq_wait_timeouts(int reset);
 
+/*
+ * Mat-vec that allocates no memory at all (no counterpart on the pages: an
+ * addition of this library for callers that cannot allocate).
+ *
+ * Who needs it: code that may not call cudaMalloc, cudaFree or an
+ * allocating pool once it runs -- a serving process whose device memory was
+ * carved up ahead of time by another allocator, a runtime with a fixed
+ * memory plan checked at start-up, or code recorded into a legacy-stream
+ * capture, where allocation calls are not permitted.  pq_gemv's tensor-core
+ * path (batch >= 5) takes a small per-call buffer from a stream-ordered pool;
+ * this entry runs that same kernel with the buffer in a fixed device array
+ * instead (1,114,112 bytes, part of the library image: every GPU that loads
+ * the library holds it until the process exits).
+ *
+ * Same arguments, layouts and accuracy as pq_gemv; limits: fmt must be PQ_Q4_K
+ * (PQ_ERR_KERNEL otherwise) and k <= 16384 (PQ_ERR_SIZE otherwise); any
+ * batch >= 1 (chunks of 16, run one after another on `stream`).
+ * Shared state: all calls in the process use the one array per GPU, which
+ * keeps the last call's contents; each call writes every byte of it that it
+ * later reads, so nothing needs clearing, but calls that overlap on the GPU
+ * (different streams, or different threads) race on it and must be ordered
+ * by the caller.  The first call on a device looks up the array's device
+ * address (a one-time set-up with that device current); make that first call
+ * before any stream capture.
+ */
+int pq_gemv_noalloc(pq_fmt fmt, const void *w_blocks, int n_out, int k,
+                    const float *x, int batch, float *y, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

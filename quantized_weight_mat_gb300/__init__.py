@@ -25,7 +25,7 @@ LIB_PATH = os.environ.get("PQ_LIB_PATH") or os.path.join(
     os.path.dirname(os.path.abspath(__file__)), "libpq.so")
 EXPORTS = ("pq_gemv", "pq_dequant", "pq_weight_bytes", "pq_strerror",
            "pq_gemv_kernel", "pq_gemv_choice", "pq_gemv_launches", "pq_wait_timeouts",
-           "pq_set_weight_prefetch")
+           "pq_set_weight_prefetch", "pq_gemv_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.pq_gemv_launches.restype = i32
             L.pq_wait_timeouts.argtypes = [i32]
             L.pq_wait_timeouts.restype = i32
+            L.pq_gemv_noalloc.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
+            L.pq_gemv_noalloc.restype = i32
             L.pq_set_weight_prefetch.argtypes = [i32]
             L.pq_set_weight_prefetch.restype = i32
             _lib = L
@@ -139,3 +141,13 @@ def pq_wait_timeouts(reset: bool = False) -> int:
 
 def pq_set_weight_prefetch(enable: bool) -> int:
     return int(lib().pq_set_weight_prefetch(1 if enable else 0))
+
+
+def pq_gemv_noalloc(fmt, w_blocks, n_out: int, k: int, x, batch: int, y, stream=None,
+                    check: bool = True) -> int:
+    """Allocation-free mat-vec (fixed device scratch; see include/pq.h)."""
+    st = lib().pq_gemv_noalloc(_fmt(fmt), _addr(w_blocks), int(n_out), int(k), _addr(x),
+                               int(batch), _addr(y), _stream(stream))
+    if check and st:
+        raise PQError(st, "pq_gemv_noalloc")
+    return st

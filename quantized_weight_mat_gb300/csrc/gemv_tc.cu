@@ -586,7 +586,39 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Fixed scratch for the allocation-free entry point (pq_gemv_noalloc): the
+// fp16 x image for k up to kNoAllocMaxK at up to 16 columns, 1,114,112 bytes.
+// Every GPU that loads this library keeps it until the process exits.  In
+// host code the name is only a stand-in for the device array; its device
+// address comes from cudaGetSymbolAddress, once per device.
+constexpr int kNoAllocMaxK = 16384;
+constexpr size_t kNoAllocScratchBytes = (size_t)(kNoAllocMaxK / 256) * (size_t)btile_bytes<32>();
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+uint8_t *noalloc_scratch_ptr() {
+    static uint8_t *ptrs[64] = {};
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::call_once(once[dev], [dev] {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess) ptrs[dev] = static_cast<uint8_t *>(ptr);
+    });
+    return ptrs[dev];
+}
+
 }  // namespace
+
+int noalloc_max_k() { return kNoAllocMaxK; }
+
+cudaError_t launch_gemv_tc_noalloc(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
+                                   float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev) {
+    if (!tc_supported(PQ_Q4_K, n_out, k, batch) || k > kNoAllocMaxK) return cudaErrorInvalidValue;
+    uint8_t *img = noalloc_scratch_ptr();
+    if (!img) return cudaErrorInvalidSymbol;
+    return batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, dev, img)
+                      : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, dev, img);
+}
 
 unsigned tc_wait_timeouts(bool reset) {
     unsigned v = 0;

@@ -216,6 +216,28 @@ int pq_wait_timeouts(int reset) {
     return n > 0x7fffffffu ? 0x7fffffff : (int)n;
 }
 
+// Allocation-free mat-vec (tensor-core kernel with fixed scratch).  Checks as
+// pq_gemv, then: Q4_K only (PQ_ERR_KERNEL otherwise), k <= noalloc_max_k()
+// (PQ_ERR_SIZE otherwise).  Batches above 16 run in chunks of 16, one after
+// another on `stream`, each reusing the scratch.
+int pq_gemv_noalloc(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
+                    float *y, struct CUstream_st *stream) {
+    int st = check_gemv((int)fmt, w_blocks, n_out, k, x, batch, y);
+    if (st) return st;
+    if (fmt != PQ_Q4_K) return PQ_ERR_KERNEL;
+    if (k > noalloc_max_k()) return PQ_ERR_SIZE;
+    const DeviceInfo *dev = nullptr;
+    if ((st = check_device(&dev))) return st;
+    for (int b0 = 0; b0 < batch; b0 += 16) {
+        const int nb = batch - b0 < 16 ? batch - b0 : 16;
+        cudaError_t e = launch_gemv_tc_noalloc(static_cast<const uint8_t *>(w_blocks), n_out, k,
+                                               x + (int64_t)b0 * k, nb, y + (int64_t)b0 * n_out, n_out,
+                                               stream, *dev);
+        if (e != cudaSuccess) return PQ_ERR_LAUNCH;
+    }
+    return PQ_OK;
+}
+
 int pq_dequant(pq_fmt fmt, const void *w_blocks, int n_out, int k, float *out,
                struct CUstream_st *stream) {
     int st = check_common((int)fmt, w_blocks, n_out, k);

@@ -45,6 +45,12 @@ cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                            const float *x, int batch, float *y, int64_t ldy,
                            cudaStream_t s, const DeviceInfo &dev);
 
+// Allocation-free variant of the tensor-core kernel: the x image lives in a
+// fixed device array instead of pool memory (k <= noalloc_max_k(), batch <= 16).
+int noalloc_max_k();
+cudaError_t launch_gemv_tc_noalloc(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
+                                   float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev);
+
 // Process-wide: may kernels read weights before the preceding kernel on the
 // stream has finished (set by pq_set_weight_prefetch)?
 int weight_prefetch();

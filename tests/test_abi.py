@@ -106,3 +106,15 @@ def test_kernel_choice_table():
 
 def test_bad_kernel_id_rejected():
     assert pq.lib().pq_gemv_kernel(1, A16, 4, 256, A16 * 2, 1, A16 * 3, 0, 7) == pq.PQ_ERR_KERNEL
+
+
+def test_noalloc_argument_checks():
+    # the allocation-free entry checks as pq_gemv does, then its own limits
+    L = pq.lib()
+    assert L.pq_gemv_noalloc(1, 0, 4, 256, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_ARG
+    assert L.pq_gemv_noalloc(1, A16 + 8, 4, 256, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_ALIGN
+    assert L.pq_gemv_noalloc(0, A16, 4, 256, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_KERNEL   # Q8_0
+    assert L.pq_gemv_noalloc(1, A16, 4, 16640, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_SIZE
+    import torch
+    if not torch.cuda.is_available():
+        assert L.pq_gemv_noalloc(1, A16, 4, 16384, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_DEVICE

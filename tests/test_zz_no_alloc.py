@@ -1,0 +1,70 @@
+"""The allocation-free mat-vec (pq_gemv_noalloc) against pq_gemv, through the C ABI.
+
+Collected last on purpose: it must pass after every other test of the suite
+(the shared device scratch then holds whatever earlier calls left) as well as
+alone in a fresh process (the first call does the per-device set-up).
+Bar: max|y_noalloc - y_gemv| <= 2e-3 * RMS(y_gemv) + 1e-6, the mat-vec bar of
+the parity tests, on two calls in a row with different inputs.
+"""
+import numpy as np
+import pytest
+
+import quantized_weight_mat_gb300 as pq
+import synth
+from pqcases import tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup(cuda_ok):
+    from quantized_weight_mat_gb300 import build
+    build.build()
+    import torch
+    torch.cuda.init()
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def both(w, n_out, k, x):
+    """(y from pq_gemv_noalloc, y from pq_gemv) for the same inputs."""
+    import torch
+    batch = x.shape[0]
+    wd, xd = dev(w), dev(x)
+    y_na = torch.full((batch * n_out,), float("nan"), dtype=torch.float32, device="cuda")
+    y_ref = torch.empty(batch * n_out, dtype=torch.float32, device="cuda")
+    pq.pq_gemv_noalloc("q4_k", wd, n_out, k, xd, batch, y_na)
+    pq.pq_gemv("q4_k", wd, n_out, k, xd, batch, y_ref)
+    torch.cuda.synchronize()
+    return y_na.cpu().numpy(), y_ref.cpu().numpy()
+
+
+@pytest.mark.parametrize("n_out,k,batches", [
+    (1000, 4096, (8, 13)),      # ragged last tile; 8 then 13 columns (two image widths)
+    (4096, 14336, (16, 5)),     # down projection shape, near the scratch limit
+    (384, 16384, (20, 3)),      # k at the limit; 20 columns run as chunks of 16 + 4
+])
+def test_two_calls_in_a_row_match_pq_gemv(n_out, k, batches):
+    w = synth.random_records("q4_k", n_out, k, seed=70 + n_out % 7)
+    for i, batch in enumerate(batches):
+        x = synth.normal_x(batch, k, seed=80 + i)
+        y_na, y_ref = both(w, n_out, k, x)
+        assert np.all(np.isfinite(y_na))
+        ok, err, bound = tolerance_ok(y_na, y_ref)
+        assert ok, f"call {i}: batch {batch}: max err {err} > {bound}"
+
+
+def test_limits_are_reported_before_any_launch():
+    import torch
+    k_big = 16640
+    w = torch.zeros(synth.weight_bytes("q4_k", 8, k_big), dtype=torch.uint8, device="cuda")
+    x = torch.zeros(k_big, dtype=torch.float32, device="cuda")
+    y = torch.zeros(8, dtype=torch.float32, device="cuda")
+    assert pq.pq_gemv_noalloc("q4_k", w, 8, k_big, x, 1, y, check=False) == pq.PQ_ERR_SIZE
+    w8 = torch.zeros(synth.weight_bytes("q8_0", 8, 256), dtype=torch.uint8, device="cuda")
+    assert pq.pq_gemv_noalloc("q8_0", w8, 8, 256, x, 1, y, check=False) == pq.PQ_ERR_KERNEL
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y).item() == 0
