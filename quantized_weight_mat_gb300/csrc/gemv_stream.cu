@@ -135,7 +135,9 @@ __device__ __forceinline__ void prep_x_block(const float *xb, uint8_t *img, uint
 }
 
 // The x image of one column, blocks q = first, first+step, ...: the loads of
-// up to eight blocks are in flight before any of them is converted.
+// up to eight blocks are in flight before any of them is converted.  x is
+// read from global memory, or (FROM_SMEM) from a shared-memory copy.
+template <bool FROM_SMEM = false>
 __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_t *meta, int nb,
                                            int S, int first, int step, int lane) {
     for (int q0 = first; q0 < nb; q0 += 8 * step) {
@@ -144,8 +146,9 @@ __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_
         for (int r = 0; r < 8; ++r) {
             const int q = q0 + r * step;
             if (q < nb) {
-                const float4 a = ldg_f4(xb + q * 256 + 8 * lane);
-                const float4 b = ldg_f4(xb + q * 256 + 8 * lane + 4);
+                const float *xq = xb + q * 256 + 8 * lane;
+                const float4 a = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq) : ldg_f4(xq);
+                const float4 b = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq + 4) : ldg_f4(xq + 4);
                 v[r][0] = a.x; v[r][1] = a.y; v[r][2] = a.z; v[r][3] = a.w;
                 v[r][4] = b.x; v[r][5] = b.y; v[r][6] = b.z; v[r][7] = b.w;
             }
@@ -376,13 +379,18 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 #ifndef PQ_ROWS_CW
 #define PQ_ROWS_CW 8
 #endif
+#ifndef PQ_ROWS_MINB
+#define PQ_ROWS_MINB 1
+#endif
 namespace rowk {
 constexpr int CW = PQ_ROWS_CW;               // consumer warps
+constexpr int MINB = PQ_ROWS_MINB;           // CTAs per SM the kernel is sized for
+constexpr int kRowsSmem = MINB == 1 ? kSmemBudget : (228 * 1024) / MINB - 1024;
 constexpr int KW = 16;                       // super-blocks per warp segment
 constexpr int RPG = 2;                       // rows per row group per stage
 constexpr int THREADS = (CW + 1) * 32;
 constexpr int MAX_STAGES = 8;
-constexpr int kStatic = 2 * MAX_STAGES * 8;
+constexpr int kStatic = 512;                 // reserve for the kernel's static shared memory (barriers)
 
 struct Params {
     const uint8_t *w;
@@ -396,16 +404,23 @@ struct Params {
     int nstages;
     int rows_cap;   // max rows of one CTA (partials buffer, G > 1)
     int early_w;    // stream weights before waiting on the previous kernel
+    int xstage;     // x through a shared-memory copy (see x_stage_bytes)
 };
 
 inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
+
+// With p.xstage, x arrives as an f32 copy in shared memory, fetched with one
+// bulk copy issued ahead of the weight stream (so that it does not queue
+// behind the CTA's weight copies), and is converted to the limb image from
+// there.  Without it the consumer warps read x from global memory.
+__host__ __device__ inline int x_stage_bytes(int64_t k, bool staged) { return staged ? (int)(4 * k) : 0; }
 
 inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
 
 // Stage plan for (k, n_out, grid) with super-blocks of `block_bytes`; false
 // when this kernel cannot take the shape (rows must be whole multiples of
 // 16 bytes for the bulk copy).
-inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p) {
+inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, bool staged, Params &p) {
     if (k % 256 || grid < 1 || ((k / 256) * block_bytes) % 16) return false;
     const int G = segments(k);
     if (G < 1 || G > CW) return false;
@@ -414,7 +429,8 @@ inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p)
     p.RS = RPG * p.NG;
     p.rows_cap = (int)((n_out + grid - 1) / grid);
     const int64_t stage = (int64_t)p.RS * (k / 256) * block_bytes;
-    const int64_t avail = kSmemBudget - kStatic - x_image_bytes(k, 1) - red_bytes(p);
+    p.xstage = staged ? 1 : 0;
+    const int64_t avail = kRowsSmem - kStatic - x_stage_bytes(k, staged) - x_image_bytes(k, 1) - red_bytes(p);
     int64_t ns = avail / stage;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
     p.nstages = (int)ns;
@@ -628,10 +644,11 @@ __device__ __forceinline__ void two_rows(float &p0, float &p1, uint32_t s, uint3
 }
 
 template <class F>
-__global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
+__global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t x_bar;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = p.k / 256;
@@ -643,7 +660,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
     const int units = (nrows + RS - 1) / RS;
     const int NS = p.nstages;
     const uint32_t stage_bytes = (uint32_t)RS * rowbytes;
-    uint8_t *ximg = smem + (size_t)NS * stage_bytes;
+    float *xstage = reinterpret_cast<float *>(smem + (size_t)NS * stage_bytes);
+    uint8_t *ximg = smem + (size_t)NS * stage_bytes + x_stage_bytes(p.k, p.xstage);
     uint8_t *xmeta = ximg + 2 * p.k;
     float *red = reinterpret_cast<float *>(xmeta + S * 16);
     const uint32_t ring_s = smem_u32(smem);
@@ -653,6 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], CA);
         }
+        mbar_init(&x_bar, 1);
         fence_mbar_init();
     }
     grid_dep_launch();   // the next kernel on the stream may start when resident
@@ -661,12 +680,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
     if (warp == CW) {
         // ---------------- producer: one contiguous copy per stage ----------------
         if (lane == 0) {
-            if (!p.early_w) grid_dep_wait();
+            // weights that may be read before the previous kernel ends: the
+            // first ring's worth when they are declared static, else none
+            const int early = p.early_w ? (units < NS ? units : NS) : 0;
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
             int slot = 0;
             uint32_t ph = 0;
-            for (int u = 0; u < units; ++u) {
+            for (int u = 0; u <= units; ++u) {
+                if (u == early) {
+                    // x (the previous kernel's output, if any) goes ahead of
+                    // the rest of the weight stream
+                    grid_dep_wait();
+                    if (p.xstage) {
+                        mbar_arrive_expect_tx(&x_bar, (uint32_t)(4 * p.k));
+                        bulk_g2s(xstage, p.x, (uint32_t)(4 * p.k), &x_bar);
+                    }
+                }
+                if (u == units) break;
                 const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
                 const uint32_t bytes = (uint32_t)rows * rowbytes;
                 if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
@@ -680,8 +711,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
     }
 
     // ---------------- x image (all consumer warps) ----------------
-    grid_dep_wait();
-    prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
+    bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
+    if (p.xstage) {
+        if (!mbar_wait(&x_bar, 0)) dead = true;
+        prep_x_all<true>(xstage, ximg, xmeta, nb, S, warp, CW, lane);
+    } else {
+        grid_dep_wait();
+        prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
+    }
     named_sync(1, CW * 32);
     if (warp >= CA) return;
 
@@ -701,7 +738,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
 
     int slot = 0;
     uint32_t ph = 0;
-    bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
     for (int u = 0; u < units; u += 2) {
         const bool hasB = u + 1 < units;
         const int slotA = slot;
@@ -765,13 +801,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows(Params p) {
 template <class F>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
                    int grid, cudaStream_t s, int early_w) {
-    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w};
-    if (!plan(k, n_out, grid, F::kBlockBytes, p)) return cudaErrorInvalidValue;
-    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p);
+    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, 0};
+    // x through shared memory unless the weights are prefetched and rows are
+    // short (then the ring depth matters more than where x queues)
+    const bool staged = !early_w || segments(k) > 1;
+    if (!plan(k, n_out, grid, F::kBlockBytes, staged, p)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_stage_bytes(k, staged) +
+                     x_image_bytes(k, 1) + red_bytes(p);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBudget - kStatic);
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows<F>);
+        if (e != cudaSuccess) return e;
+        if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -794,8 +837,8 @@ inline bool takes(int fmt, int64_t k, int64_t n_out) {
     Params p{};
     const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
     const int grid = (int)(n_out < grid_est ? n_out : grid_est);
-    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, p);
-    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p);
+    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, true, p);
+    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, true, p);
     return false;
 }
 }  // namespace rowk
