@@ -9,32 +9,37 @@
 // Exactness: a tile entry is the integer sc_j*q (q in 0..15, sc_j in 0..63,
 // so <= 945), exactly representable in fp16; x enters as two fp16 columns
 // (x_hi = fp16(x), x_lo = fp16(x - x_hi)), so every product is exact in the
-// f32 accumulator and only accumulation rounds.  The sub-block mins enter
-// through a second, K=16 product of the 6-bit mins with the fp16 hi/lo sums
-// of x over each 32-element sub-block.  Per super-block and row the epilogue
-// forms y += d*(A.x) - dmin*(m.XS) in f32.
+// f32 accumulator and only accumulation rounds.  Per super-block and row the
+// epilogue forms y += d*(A.x) - dmin*sum_j m_j*XS_j in f32, where XS_j is the
+// f32 sum of x over sub-block j (the mins term runs on CUDA cores).
 //
-// Pipeline (one CTA per SM, persistent over 128-row tiles):
+// Work split: the (128-row tile, super-block) items of the matrix, in
+// tile-major order, are cut into one contiguous, equal-sized range per CTA
+// (one CTA per SM).  A tile whose items are spread over several CTAs is
+// split-K: each writes its partial sums to scratch, and a small kernel that
+// runs after the main one adds the parts in CTA order and writes y, so the
+// result does not depend on timing.
+//
+// Pipeline inside a CTA:
 //   warp 12 producer: a 2-D TMA load (tensor map over W as [n_out][row bytes])
 //           brings one 128-row x 144-byte super-block column per stage, and a
-//           1-D bulk copy brings that super-block's fp16 x tile;
+//           1-D bulk copy brings that super-block's x tile;
 //   warps 0-7 decoders: thread (r, h) turns the 128 weights of row r, half h
 //           of the super-block into fp16 sc*q (one LOP3 + one HFMA2 per two
-//           weights), 64 weights per slot, and write them straight into
+//           weights), 64 weights per slot, and writes them straight into
 //           tensor memory (tcgen05.st; TMEM lane = row, two K values per
 //           column), a ring of eight slots (two super-blocks);
-//   warp 13 MMA issuer (one thread): per super-block the K=16 mins product
-//           (A from shared memory), then four tcgen05.mma (M=128, N=2*NBP,
-//           K=16, A from tensor memory, x from shared memory) per slot into a
-//           TMEM accumulator;
-//   warps 8-11 epilogue: tcgen05.ld of the accumulators (warp w reads TMEM
-//           lanes 32(w%4).. = its rows), d and dmin from a small ring the
-//           decoders fill, f32 scaling.
+//   warp 13 MMA issuer (one thread): four tcgen05.mma (M=128, N=2*NBP, K=16,
+//           A from tensor memory, x from shared memory) per slot into the
+//           super-block's TMEM accumulator, then one commit per super-block;
+//   warps 8-11 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//           lanes 32(w%4).. = its rows), the row's d, dmin and mins from the
+//           raw block, f32 scaling; frees the stage and the accumulator.
 // Accumulators are double-buffered in TMEM; every mbarrier wait is bounded.
 //
-// x is converted once per call by a small kernel into a per-super-block fp16
-// image (the operand layout the MMA reads), in a stream-ordered scratch
-// buffer.
+// x is converted once per call by a small kernel into a per-super-block image
+// (the operand layout the MMA reads, plus the sub-block sums), in scratch
+// memory that also holds the split-K partial sums.
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -50,19 +55,35 @@ namespace {
 
 constexpr int TM = 128;                       // rows per tile = MMA M
 constexpr int RAW_BYTES = TM * 144;           // one super-block column of a tile
-constexpr int A_SLOTS = 8;                    // two super-blocks of 64-weight slots, in TMEM
-constexpr int A_COL = 256;                    // TMEM column of A slot 0 (32 columns per slot)
+#ifndef PQ_TC_ABUFS
+#define PQ_TC_ABUFS 2
+#endif
+constexpr int A_BUFS = PQ_TC_ABUFS;           // super-blocks in flight between decoders, MMA and epilogue
+constexpr int A_SLOTS = 4 * A_BUFS;           // 64-weight slots
 constexpr int TMEM_COLS = 512;
-constexpr int AMIN_BYTES = TM * 16 * 2;
-constexpr int THREADS = 14 * 32;              // 8 decoder, 4 epilogue, producer, MMA warps
+constexpr int A_COL = TMEM_COLS - 32 * A_SLOTS;   // TMEM column of A slot 0 (32 columns per slot)
+constexpr int DEC_WARPS = 8, EPI_WARPS = 4;
+constexpr int PRODUCER_WARP = DEC_WARPS + EPI_WARPS;
+constexpr int MMA_WARP = PRODUCER_WARP + 1;   // MMA_WARP + j issues the super-blocks with g % A_BUFS == j
+constexpr int THREADS = (MMA_WARP + A_BUFS) * 32;
+constexpr int kMaxGrid = 160;                 // CTAs at most (partial-sum slots are sized for it)
 
-// x image of one super-block for N' = 2*NBP columns: main part N' x 256 fp16
-// (K-major, 8x8 core matrices), then the mins part N' x 16.
-template <int NP> __host__ __device__ constexpr int btile_bytes() { return NP * 256 * 2 + NP * 16 * 2; }
-template <int NP> __host__ __device__ constexpr int raw_stages() { return NP == 32 ? 5 : 7; }
-template <int NP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NP>(); }
-template <int NP> __host__ __device__ constexpr int smem_bytes() {
-    return raw_stages<NP>() * stage_bytes<NP>() + 2 * AMIN_BYTES + 1024;
+// x image of one super-block for NBP columns (N' = 2*NBP MMA columns, the hi
+// parts then the lo parts): N' x 256 fp16, K-major 8x8 core matrices, 8-row
+// groups 4096 bytes apart; then f32 XS[8][NBP], the sums over each sub-block.
+template <int NBP> __host__ __device__ constexpr int xmain_bytes() { return 2 * NBP * 256 * 2; }
+template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xmain_bytes<NBP>() + 8 * NBP * 4; }
+template <int NBP> __host__ __device__ constexpr int raw_stages() { return NBP == 16 ? 6 : 8; }
+template <int NBP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NBP>(); }
+template <int NBP> __host__ __device__ constexpr int smem_bytes() { return raw_stages<NBP>() * stage_bytes<NBP>() + 1024; }
+static_assert(stage_bytes<8>() % 128 == 0 && stage_bytes<16>() % 128 == 0, "stage alignment");
+
+// Scratch of one call: x image, then partial sums [grid][2][NBP][TM] (slot
+// 2c: CTA c's first tile, 2c+1: its last tile, when split).
+template <int NBP> size_t scratch_img_bytes(int64_t k) { return (size_t)(k / 256) * btile_bytes<NBP>(); }
+template <int NBP> size_t scratch_part_bytes(int grid) { return (size_t)grid * 2 * NBP * TM * 4; }
+template <int NBP> size_t scratch_bytes(int64_t k, int grid) {
+    return scratch_img_bytes<NBP>(k) + scratch_part_bytes<NBP>(grid);
 }
 
 // K order inside a super-block: chunk e of A-column a (8 fp16 per 16 bytes)
@@ -81,17 +102,17 @@ __host__ __device__ constexpr int kmaj_off(int n, int K, int sbo) {
 }
 
 // ---------------------------------------------------------------- x image
-// One block per super-block.  Lets the main kernel launch at once
-// (programmatic dependent launch): it sets up and streams weights while this
-// runs, and waits for it only before its first x tile.
+// One block per super-block.  Lets the main kernel launch at once (programmatic dependent launch): it sets
+// up and streams weights while this runs, and waits for it only before its
+// first x tile.
 template <int NBP>
 __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, int k, int nb_cols,
                                                  uint8_t *__restrict__ img) {
-    constexpr int NP = 2 * NBP;
     asm volatile("griddepcontrol.launch_dependents;");
     const int sb = blockIdx.x;
-    __half *out = reinterpret_cast<__half *>(img + (size_t)sb * btile_bytes<NP>());
-    __shared__ float xs[NBP][8];
+    uint8_t *tile = img + (size_t)sb * btile_bytes<NBP>();
+    __half *out = reinterpret_cast<__half *>(tile);
+    float *xs_out = reinterpret_cast<float *>(tile + xmain_bytes<NBP>());
     const int t = threadIdx.x;
     // sub-block sums, fixed order (thread per (column, sub-block), 8 vector loads)
     if (t < NBP * 8) {
@@ -105,36 +126,20 @@ __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, in
 #pragma unroll
             for (int i = 0; i < 8; ++i) s = s + v[i].x + v[i].y + v[i].z + v[i].w;
         }
-        xs[b][j] = s;
+        xs_out[j * NBP + b] = s;
     }
     // main part: thread t = K index; all column loads in flight together
-    {
-        const int K = t;
-        const int pos = kpos(K / 8, K % 8);
-        float v[NBP];
+    const int K = t;
+    const int pos = kpos(K / 8, K % 8);
+    float v[NBP];
 #pragma unroll
-        for (int b = 0; b < NBP; ++b) v[b] = b < nb_cols ? __ldg(x + (size_t)b * k + sb * 256 + pos) : 0.f;
+    for (int b = 0; b < NBP; ++b) v[b] = b < nb_cols ? __ldg(x + (size_t)b * k + sb * 256 + pos) : 0.f;
 #pragma unroll
-        for (int b = 0; b < NBP; ++b) {
-            const __half hi = __float2half_rn(v[b]);
-            const __half lo = __float2half_rn(v[b] - __half2float(hi));
-            out[kmaj_off(b, K, 4096) / 2] = hi;
-            out[kmaj_off(NBP + b, K, 4096) / 2] = lo;
-        }
-    }
-    __syncthreads();
-    // mins part: K = j < 8 holds the sums, K = 8..15 zero
-    __half *om = out + NP * 256;
-    for (int i = t; i < NP * 16; i += 256) {
-        const int n = i / 16, K = i % 16;
-        const int b = n % NBP;
-        float v = 0.f;
-        if (K < 8) {
-            const float s = xs[b][K];
-            const __half hi = __float2half_rn(s);
-            v = n < NBP ? __half2float(hi) : __half2float(__float2half_rn(s - __half2float(hi)));
-        }
-        om[kmaj_off(n, K, 256) / 2] = __float2half_rn(v);
+    for (int b = 0; b < NBP; ++b) {
+        const __half hi = __float2half_rn(v[b]);
+        const __half lo = __float2half_rn(v[b] - __half2float(hi));
+        out[kmaj_off(b, K, 4096) / 2] = hi;
+        out[kmaj_off(NBP + b, K, 4096) / 2] = lo;
     }
 }
 
@@ -229,187 +234,226 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
 }
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<const uint32_t *>(&v); }
 
+// Each thread reads 16 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+          "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+        :
+        : "memory");
+}
+
 struct TcParams {
-    const uint8_t *w;          // for L2 prefetch of whole tiles (rows are contiguous)
-    const uint8_t *x_img;
+    const uint8_t *x_img;      // x image, one tile per super-block
     float *y;
+    float *partials;           // [grid][2][NBP][TM] split-K partial sums
     long long ldy;
+    long long total;           // work items: tiles x super-blocks per row
     int n_out;
     int k;
     int nb_cols;
 };
 
+// First work item of CTA c when `total` items are split over `grid` CTAs, and
+// the CTA that owns item i (the largest c with item_begin(c) <= i).
+__device__ __forceinline__ long long item_begin(long long c, long long total, int grid) { return c * total / grid; }
+__device__ __forceinline__ int item_owner(long long i, long long total, int grid) {
+    return (int)(((i + 1) * grid - 1) / total);
+}
+
 template <int NBP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemv_tc_q4_k(const __grid_constant__ CUtensorMap wmap, TcParams p) {
     constexpr int NP = 2 * NBP;
-    constexpr int NSR = raw_stages<NP>();
-    constexpr int STAGE = stage_bytes<NP>();
+    constexpr int NSR = raw_stages<NBP>();
+    constexpr int STAGE = stage_bytes<NBP>();
     constexpr uint32_t IDESC = instr_desc(TM, NP);
-    static_assert(4 * NP <= A_COL, "accumulators below the A slots");
+    static_assert(A_BUFS * NP <= A_COL, "accumulators below the A slots");
+    static_assert(A_COL + 32 * A_SLOTS <= TMEM_COLS, "A slots fit in the allocation");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
-    __shared__ __align__(8) uint64_t a_full[A_SLOTS], a_empty[A_SLOTS];
-    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
-    __shared__ __align__(8) uint64_t dmeta_full[4];
-    __shared__ float2 dmeta[4][TM];      // (d, dmin) of each row, per super-block
+    __shared__ __align__(8) uint64_t a_full[A_BUFS];
+    __shared__ __align__(8) uint64_t item_done[A_BUFS], acc_empty[A_BUFS];
     __shared__ uint32_t tmem_base_sh;
 
     // 1024-aligned working area
-    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t *ring = smem;
-    uint8_t *amin = ring + NSR * STAGE;
+    uint8_t *ring = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = p.k / 256;
-    const int ntiles = (p.n_out + TM - 1) / TM;
-    const int my_tiles = ntiles > (int)blockIdx.x ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total = my_tiles * nb;    // super-block steps of this CTA
+    const int grid = (int)gridDim.x;
+    const long long i0 = item_begin(blockIdx.x, p.total, grid);
+    const int count = (int)(item_begin(blockIdx.x + 1, p.total, grid) - i0);   // items of this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSR; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], 1);
+            mbar_init(&raw_empty[s], EPI_WARPS);
         }
-        for (int s = 0; s < 4; ++s) mbar_init(&dmeta_full[s], 4);
-        for (int s = 0; s < A_SLOTS; ++s) {
-            mbar_init(&a_full[s], 4);
-            mbar_init(&a_empty[s], 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], 4);
+        for (int s = 0; s < A_BUFS; ++s) mbar_init(&a_full[s], DEC_WARPS);
+        for (int s = 0; s < A_BUFS; ++s) {
+            mbar_init(&item_done[s], 1);
+            mbar_init(&acc_empty[s], EPI_WARPS);
         }
         fence_mbar_init();
     }
-    // zero the unused K = 8..15 half of both mins tiles (never rewritten)
-    for (int i = threadIdx.x; i < 2 * TM; i += THREADS) {
-        const int buf = i / TM, r = i % TM;
-        *reinterpret_cast<uint4 *>(amin + buf * AMIN_BYTES + kmaj_off(r, 8, 256)) = make_uint4(0, 0, 0, 0);
-    }
-    if (warp == 13) {
+    if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_base_sh)),
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    // the split-K finishing kernel may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
 
-    if (warp == 12) {
+    if (warp == PRODUCER_WARP) {
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint64_t pol = make_evict_first_policy();
-            bool dead = false;
-            for (int g = 0; g < total && !dead; ++g) {
+            int tile = (int)(i0 / nb), sb = (int)(i0 % nb);
+            for (int g = 0; g < count; ++g) {
                 const int slot = g % NSR;
                 const uint32_t ph = (uint32_t)(g / NSR) & 1u;
-                const int tile = (int)blockIdx.x + (g / nb) * (int)gridDim.x, sb = g % nb;
-                if (!mbar_wait(&raw_empty[slot], ph ^ 1u)) { dead = true; break; }
+                if (!mbar_wait(&raw_empty[slot], ph ^ 1u)) break;
                 uint8_t *st = ring + slot * STAGE;
                 mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)STAGE);
                 tma_load_2d(st, &wmap, sb * 144, tile * TM, &raw_full[slot]);
                 // the weights were complete before the x-prep kernel started; the x
                 // image is that kernel's output: wait for it once, before its first use
                 if (g == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-                bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NP>(), (uint32_t)btile_bytes<NP>(),
+                bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NBP>(), (uint32_t)btile_bytes<NBP>(),
                               &raw_full[slot], pol);
+                if (++sb == nb) { sb = 0; ++tile; }
             }
         }
-    } else if (warp == 13) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp >= MMA_WARP) {
+        // ---------------- MMA issuers (one thread per A buffer) ----------------
+        // Several issuing threads keep the tensor core busy: one thread's
+        // tcgen05 instructions and waits are issued one after another.
+        const int buf = warp - MMA_WARP;
         if (lane == 0) {
             bool dead = false;
-            for (int g = 0; g < total; ++g) {
+            for (int g = buf; g < count; g += A_BUFS) {
                 const int slot = g % NSR;
-                const uint32_t ph = (uint32_t)(g / NSR) & 1u;
-                const int buf = g & 1;
-                const int a0 = 4 * buf;                       // A slots of this super-block
-                const uint32_t aph = (uint32_t)(g >> 1) & 1u;
-                if (!dead && !mbar_wait(&acc_empty[buf], ((uint32_t)(g >> 1) & 1u) ^ 1u)) dead = true;
-                if (!dead && !mbar_wait(&raw_full[slot], ph)) dead = true;
-                // the mins rows are complete once both halves' first slots are
-                if (!dead && !mbar_wait(&a_full[a0], aph)) dead = true;
-                if (!dead && !mbar_wait(&a_full[a0 + 2], aph)) dead = true;
+                const uint32_t par = (uint32_t)(g / A_BUFS) & 1u;
+                // accumulator free (epilogue done with super-block g - A_BUFS), then
+                // the A tile decoded; the decoders saw the stage (weights and x tile)
+                // complete before they arrived
+                if (!dead && !mbar_wait(&acc_empty[buf], par ^ 1u)) dead = true;
+                if (!dead && !mbar_wait(&a_full[buf], par)) dead = true;
                 tc_fence_after();
-                const uint32_t d_main = tmem + (uint32_t)(buf * 2 * NP);
-                const uint32_t d_min = d_main + NP;
-                const uint32_t bbase = smem_u32(ring + slot * STAGE + RAW_BYTES);
-                {
-                    const uint64_t ad = smem_desc(smem_u32(amin + buf * AMIN_BYTES), 128u, 256u);
-                    const uint64_t bd = smem_desc(bbase + NP * 256 * 2, 128u, 256u);
-                    if (!dead) mma_f16(d_min, ad, bd, IDESC, 0u);
-                }
-                for (int c = 0; c < 4; ++c) {
-                    if ((c & 1) && !dead && !mbar_wait(&a_full[a0 + c], aph)) dead = true;
-                    tc_fence_after();
-                    const uint32_t acol = tmem + (uint32_t)(A_COL + 32 * (a0 + c));
+                if (!dead) {
+                    // the super-block's 16 products back to back, no branch between them
+                    const uint32_t d_acc = tmem + (uint32_t)(buf * NP);
+                    const uint32_t a0 = tmem + (uint32_t)(A_COL + 32 * 4 * buf);
+                    const uint64_t b0 = smem_desc(smem_u32(ring + slot * STAGE + RAW_BYTES), 128u, 4096u);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = smem_desc(bbase + 256u * (4 * c + ks), 128u, 4096u);
-                        if (!dead) mma_f16_ta(d_main, acol + 8u * ks, bd, IDESC, (c | ks) ? 1u : 0u);
-                    }
-                    mma_commit(&a_empty[a0 + c]);
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16_ta(d_acc, a0 + (uint32_t)(32 * c + 8 * ks), b0 + (uint64_t)(16 * (4 * c + ks)),
+                                       IDESC, (c | ks) ? 1u : 0u);
                 }
-                mma_commit(&acc_full[buf]);
-                mma_commit(&raw_empty[slot]);
+                mma_commit(&item_done[buf]);
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= DEC_WARPS) {
         // ---------------- epilogue (warps 8-11) ----------------
-        const int r = 32 * (warp - 8) + lane;           // row within the tile = TMEM lane
-        const uint32_t row_taddr = tmem + ((uint32_t)(32 * (warp - 8)) << 16);
+        const int r = 32 * (warp - DEC_WARPS) + lane;                       // row within the tile = TMEM lane
+        const uint32_t row_taddr = tmem + ((uint32_t)(32 * (warp - DEC_WARPS)) << 16);
+        const int first_tile = (int)(i0 / nb);
         float yacc[NBP];
 #pragma unroll
         for (int b = 0; b < NBP; ++b) yacc[b] = 0.f;
         bool dead = false;
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // before any store of y
-        for (int g = 0; g < total; ++g) {
-            const int buf = g & 1;
-            if (!dead && !mbar_wait(&acc_full[buf], (uint32_t)(g >> 1) & 1u)) dead = true;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // before any store of y or partials
+        int tile = first_tile, sb = (int)(i0 % nb);
+        for (int g = 0; g < count; ++g) {
+            const int slot = g % NSR;
+            const int buf = g % A_BUFS;
+            const uint32_t par = (uint32_t)(g / A_BUFS) & 1u;
+            if (!dead && !mbar_wait(&item_done[buf], par)) dead = true;
             tc_fence_after();
-            uint32_t v[2 * NP];
-            {
+            float dot[NBP];
+            if constexpr (NP == 32) {
                 uint32_t t0[32];
-                tmem_ld32(row_taddr + (uint32_t)(buf * 2 * NP), t0);
-                if constexpr (NP == 32) {
-                    uint32_t t1[32];
-                    tmem_ld32(row_taddr + (uint32_t)(buf * 2 * NP + 32), t1);
-                    tmem_ld_wait(t1);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[32 + i] = t1[i];
-                }
+                tmem_ld32(row_taddr + (uint32_t)(buf * NP), t0);
                 tmem_ld_wait(t0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = t0[i];
+                for (int b = 0; b < NBP; ++b) dot[b] = __uint_as_float(t0[b]) + __uint_as_float(t0[NBP + b]);
+            } else {
+                uint32_t t0[16];
+                tmem_ld16(row_taddr + (uint32_t)(buf * NP), t0);
+                tmem_ld_wait(t0);
+#pragma unroll
+                for (int b = 0; b < NBP; ++b) dot[b] = __uint_as_float(t0[b]) + __uint_as_float(t0[NBP + b]);
             }
             tc_fence_before();
-            if (!dead && !mbar_wait(&dmeta_full[g & 3], (uint32_t)(g >> 2) & 1u)) dead = true;
-            const float2 dm = dmeta[g & 3][r];
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            const float d = dm.x, dmin = dm.y;
+            // d, dmin and the eight 6-bit mins of row r; sub-block sums of x
+            const uint8_t *st = ring + slot * STAGE;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(st + r * 144);
+            const uint32_t mlo = hd.z & 0x3F3F3F3Fu;
+            const uint32_t mhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+            const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+            const float4 *xs = reinterpret_cast<const float4 *>(st + RAW_BYTES + xmain_bytes<NBP>());
+            float mn[NBP];
 #pragma unroll
-            for (int b = 0; b < NBP; ++b) {
-                const float dot = __uint_as_float(v[b]) + __uint_as_float(v[NBP + b]);
-                const float mn = __uint_as_float(v[NP + b]) + __uint_as_float(v[NP + NBP + b]);
-                yacc[b] = fmaf(d, dot, fmaf(-dmin, mn, yacc[b]));
+            for (int b = 0; b < NBP; ++b) mn[b] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float m = (float)((j < 4 ? (mlo >> (8 * j)) : (mhi >> (8 * (j - 4)))) & 0xFFu);
+#pragma unroll
+                for (int b4 = 0; b4 < NBP / 4; ++b4) {
+                    const float4 v = xs[j * (NBP / 4) + b4];
+                    mn[4 * b4 + 0] = fmaf(m, v.x, mn[4 * b4 + 0]);
+                    mn[4 * b4 + 1] = fmaf(m, v.y, mn[4 * b4 + 1]);
+                    mn[4 * b4 + 2] = fmaf(m, v.z, mn[4 * b4 + 2]);
+                    mn[4 * b4 + 3] = fmaf(m, v.w, mn[4 * b4 + 3]);
+                }
             }
-            if (g % nb == nb - 1) {
-                const int tile = (int)blockIdx.x + (g / nb) * (int)gridDim.x;
-                const int row = tile * TM + r;
-                if (row < p.n_out) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[slot]);
 #pragma unroll
-                    for (int b = 0; b < NBP; ++b)
-                        if (b < p.nb_cols) p.y[(size_t)b * p.ldy + row] = yacc[b];
+            for (int b = 0; b < NBP; ++b) yacc[b] = fmaf(d, dot[b], fmaf(-dmin, mn[b], yacc[b]));
+
+            if (sb == nb - 1 || g == count - 1) {
+                // the CTA's part of this tile is complete
+                const long long t0i = (long long)tile * nb;
+                const int cf = item_owner(t0i, p.total, grid), cl = item_owner(t0i + nb - 1, p.total, grid);
+                const int row = tile * TM + r;
+                if (cf == cl) {
+                    if (row < p.n_out) {
+#pragma unroll
+                        for (int b = 0; b < NBP; ++b)
+                            if (b < p.nb_cols) p.y[(size_t)b * p.ldy + row] = yacc[b];
+                    }
+                } else {
+                    // split tile: this CTA's part, added up by the finishing kernel
+                    const int side = tile == first_tile ? 0 : 1;
+                    float *mine = p.partials + ((size_t)(blockIdx.x * 2 + side) * NBP) * TM;
+#pragma unroll
+                    for (int b = 0; b < NBP; ++b) mine[b * TM + r] = yacc[b];
                 }
 #pragma unroll
                 for (int b = 0; b < NBP; ++b) yacc[b] = 0.f;
             }
+            if (++sb == nb) { sb = 0; ++tile; }
         }
     } else {
         // ---------------- decoders (warps 0-7) ----------------
@@ -419,46 +463,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t mB = h ? 0x30303030u : 0u;
         const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's TMEM lanes
         bool dead = false;
-        for (int g = 0; g < total; ++g) {
+        for (int g = 0; g < count; ++g) {
             const int slot = g % NSR;
             const uint32_t ph = (uint32_t)(g / NSR) & 1u;
-            const int buf = g & 1;
-            const uint32_t aph = (uint32_t)(g >> 1) & 1u;
+            const int buf = g % A_BUFS;
+            const uint32_t par = (uint32_t)(g / A_BUFS) & 1u;
             if (!dead && !mbar_wait(&raw_full[slot], ph)) dead = true;
             const uint8_t *blk = ring + slot * STAGE + r * 144;
             const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
             uint4 qw[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) qw[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * h + 16 * i);
-            // 6-bit scales / mins of sub-blocks 4h..4h+3, one per byte
+            // 6-bit scales of sub-blocks 4h..4h+3, one per byte
             const uint32_t sc4 = ((h ? hd.w : hd.y) & mA) | ((hd.y >> 2) & mB);
-            const uint32_t m4 = ((h ? (hd.w >> 4) : hd.z) & mA) | ((hd.z >> 2) & mB);
+            // this buffer's slots are free once the products of the super-block
+            // that used them before are complete
+            if (!dead && !mbar_wait(&item_done[buf], par ^ 1u)) dead = true;
+            tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * h + cc;           // 64-weight chunk of the super-block
                 const int as = 4 * buf + c;         // its A slot
-                if (!dead && !mbar_wait(&a_empty[as], aph ^ 1u)) dead = true;
-                if (cc == 0 && h == 0) {
-                    // (d, dmin) for the epilogue.  Slot g&3 was last read by the
-                    // epilogue four super-blocks ago; the wait above implies the
-                    // MMAs two super-blocks ago were issued, which waited for
-                    // that epilogue to finish.
-                    dmeta[g & 3][r] = make_float2(h2f(hd.x), h2f(hd.x >> 16));
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&dmeta_full[g & 3]);
-                }
-                if (cc == 0) {
-                    // mins row of the K=16 product: m_{4h..4h+3} at K = 4h..4h+3.
-                    // The wait above covers every product issued before this slot
-                    // was last read, which includes the mins product that last
-                    // read this buffer (two super-blocks ago): it is issued first.
-                    const __half2 m01 = __halves2half2(__int2half_rn((int)(m4 & 0xFF)),
-                                                       __int2half_rn((int)((m4 >> 8) & 0xFF)));
-                    const __half2 m23 = __halves2half2(__int2half_rn((int)((m4 >> 16) & 0xFF)),
-                                                       __int2half_rn((int)(m4 >> 24)));
-                    *reinterpret_cast<uint2 *>(amin + buf * AMIN_BYTES + kmaj_off(r, 4 * h, 256)) =
-                        make_uint2(h2_bits(m01), h2_bits(m23));
-                }
                 // scale pairs: low nibbles -> (1024+q)*sc - 1024*sc, high nibbles -> (1024+16q)*sc/16 - 64*sc
                 const __half slo = __int2half_rn((int)((sc4 >> (16 * cc)) & 0xFF));
                 const __half shi = __int2half_rn((int)((sc4 >> (16 * cc + 8)) & 0xFF));
@@ -484,21 +509,63 @@ __global__ void __launch_bounds__(THREADS, 1)
                     R[16 + 4 * a + 3] = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
                 }
                 tmem_st32(a_lane + (uint32_t)(A_COL + 32 * as), R);
-                tmem_st_wait();
-                if (cc == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // mins row
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[as]);
             }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[buf]);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 13) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
     }
+}
+
+// Split-K finish: block c adds up the tile whose first contributor is CTA c
+// (the last tile of c's range, when later CTAs share it), parts in CTA order.
+// Launched after the main kernel (programmatic dependent launch: it may be
+// resident early and waits for the main grid to complete).
+template <int NBP>
+__global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partials, float *__restrict__ y,
+                                               long long ldy, long long total, int nb, int n_out, int nb_cols) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int grid = (int)gridDim.x, c = (int)blockIdx.x;
+    const long long last_item = item_begin(c + 1, total, grid) - 1;
+    const int tile = (int)(last_item / nb);
+    const long long t0 = (long long)tile * nb;
+    if (item_owner(t0, total, grid) != c) return;                  // c is not the tile's first contributor
+    const int cl = item_owner(t0 + nb - 1, total, grid);
+    if (cl == c) return;                                            // not split
+    const int r = threadIdx.x, row = tile * TM + r;
+    float sum[NBP];
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) sum[b] = 0.f;
+    for (int cc = c; cc <= cl; ++cc) {
+        const int side = tile == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
+        const float *part = partials + ((size_t)(cc * 2 + side) * NBP) * TM;
+#pragma unroll
+        for (int b = 0; b < NBP; ++b) sum[b] += part[b * TM + r];
+    }
+    if (row < n_out) {
+#pragma unroll
+        for (int b = 0; b < NBP; ++b)
+            if (b < nb_cols) y[(size_t)b * ldy + row] = sum[b];
+    }
+}
+
+// Whether any tile is split over several CTAs.
+bool any_split(long long total, int nb, int grid) {
+    for (int c = 0; c < grid; ++c) {
+        const long long last_item = ((long long)(c + 1) * total) / grid - 1;
+        const long long t0 = last_item / nb * nb;
+        const int cf = (int)(((t0 + 1) * grid - 1) / total), cl = (int)(((t0 + nb) * grid - 1) / total);
+        if (cf == c && cl != c) return true;
+    }
+    return false;
 }
 
 // ---------------------------------------------------------------- host side
@@ -542,11 +609,20 @@ cudaMemPool_t scratch_pool() {
     return pools[dev];
 }
 
+// CTAs for a call: one per SM, at most one per work item.
+int tc_grid(int64_t n_out, int64_t k, const DeviceInfo &dev) {
+    const long long total = (long long)((n_out + TM - 1) / TM) * (k / 256);
+    long long g = dev.sm_count < kMaxGrid ? dev.sm_count : kMaxGrid;
+    if (g > total) g = total;
+    return (int)(g < 1 ? 1 : g);
+}
+
 template <int NBP>
 cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch, float *y,
-                       int64_t ldy, cudaStream_t s, const DeviceInfo &dev, uint8_t *img) {
-    constexpr int NP = 2 * NBP;
+                       int64_t ldy, cudaStream_t s, int grid, uint8_t *scratch) {
     const int nb = (int)(k / 256);
+    uint8_t *img = scratch;
+    float *partials = reinterpret_cast<float *>(scratch + scratch_img_bytes<NBP>(k));
     prep_x_tc<NBP><<<nb, 256, 0, s>>>(x, (int)k, batch, img);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -565,17 +641,17 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
 
     static bool configured = false;
     if (!configured) {
-        e = cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NP>());
+        e = cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int ntiles = (int)((n_out + TM - 1) / TM);
-    const int grid = ntiles < dev.sm_count ? ntiles : dev.sm_count;
-    TcParams p{w, img, y, (long long)ldy, (int)n_out, (int)k, batch};
+    const long long ntiles = (n_out + TM - 1) / TM;
+    const long long total = ntiles * nb;
+    TcParams p{img, y, partials, (long long)ldy, total, (int)n_out, (int)k, batch};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = (size_t)smem_bytes<NP>();
+    cfg.dynamicSmemBytes = (size_t)smem_bytes<NBP>();
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -583,16 +659,26 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess || !any_split(total, nb, grid)) return e;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TM);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, tc_finish<NBP>, (const float *)partials, y, (long long)ldy, total, nb, (int)n_out,
+                           batch);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Fixed scratch for the allocation-free entry point (pq_gemv_noalloc): the
-// fp16 x image for k up to kNoAllocMaxK at up to 16 columns, 1,114,112 bytes.
-// Every GPU that loads this library keeps it until the process exits.  In
-// host code the name is only a stand-in for the device array; its device
-// address comes from cudaGetSymbolAddress, once per device.
+// Fixed scratch for the allocation-free entry point (pq_gemv_noalloc): x image
+// for k up to kNoAllocMaxK at up to 16 columns and split-K partial sums for up
+// to kMaxGrid CTAs: 3,702,784 bytes.  Every GPU that loads
+// this library keeps it until the process exits.  In host code the name is
+// only a stand-in for the device array; its device address comes from
+// cudaGetSymbolAddress, once per device.
 constexpr int kNoAllocMaxK = 16384;
-constexpr size_t kNoAllocScratchBytes = (size_t)(kNoAllocMaxK / 256) * (size_t)btile_bytes<32>();
+constexpr size_t kNoAllocScratchBytes =
+    (size_t)(kNoAllocMaxK / 256) * (size_t)btile_bytes<16>() + (size_t)kMaxGrid * 2 * 16 * TM * 4;
+static_assert(kNoAllocScratchBytes == 3702784, "stated size");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 uint8_t *noalloc_scratch_ptr() {
@@ -614,10 +700,11 @@ int noalloc_max_k() { return kNoAllocMaxK; }
 cudaError_t launch_gemv_tc_noalloc(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
                                    float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev) {
     if (!tc_supported(PQ_Q4_K, n_out, k, batch) || k > kNoAllocMaxK) return cudaErrorInvalidValue;
-    uint8_t *img = noalloc_scratch_ptr();
-    if (!img) return cudaErrorInvalidSymbol;
-    return batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, dev, img)
-                      : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, dev, img);
+    uint8_t *scratch = noalloc_scratch_ptr();
+    if (!scratch) return cudaErrorInvalidSymbol;
+    const int grid = tc_grid(n_out, k, dev);
+    return batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, scratch)
+                      : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, scratch);
 }
 
 unsigned tc_wait_timeouts(bool reset) {
@@ -638,16 +725,16 @@ bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch) {
 cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
                            float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev) {
     if (!tc_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
-    const int NP = batch <= 8 ? 16 : 32;
-    const size_t bytes = (size_t)(k / 256) * (size_t)(NP * 256 * 2 + NP * 16 * 2);
+    const int grid = tc_grid(n_out, k, dev);
+    const size_t bytes = batch <= 8 ? scratch_bytes<8>(k, grid) : scratch_bytes<16>(k, grid);
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
-    void *img = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&img, bytes, pool, s);
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, pool, s);
     if (e != cudaSuccess) return e;
-    e = batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, dev, (uint8_t *)img)
-                   : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, dev, (uint8_t *)img);
-    const cudaError_t f = cudaFreeAsync(img, s);
+    e = batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch)
+                   : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch);
+    const cudaError_t f = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : f;
 }
 
