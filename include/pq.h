@@ -158,7 +158,7 @@ int pq_wait_timeouts(int reset);
  * capture, where allocation calls are not permitted.  pq_gemv's tensor-core
  * path (batch >= 5) takes a small per-call buffer from a stream-ordered pool;
  * this entry runs that same kernel with the buffer in a fixed device array
- * instead (3,702,784 bytes, part of the library image: every GPU that loads
+ * instead (3,735,552 bytes, part of the library image: every GPU that loads
  * the library holds it until the process exits).
  *
  * Same arguments, layouts and accuracy as pq_gemv; limits: fmt must be PQ_Q4_K

@@ -9,32 +9,35 @@
 // Exactness: a tile entry is the integer sc_j*q (q in 0..15, sc_j in 0..63,
 // so <= 945), exactly representable in fp16; x enters as two fp16 columns
 // (x_hi = fp16(x), x_lo = fp16(x - x_hi)), so every product is exact in the
-// f32 accumulator and only accumulation rounds.  Per super-block and row the
-// epilogue forms y += d*(A.x) - dmin*sum_j m_j*XS_j in f32, where XS_j is the
-// f32 sum of x over sub-block j (the mins term runs on CUDA cores).
+// f32 accumulator and only accumulation rounds.  The sub-block mins enter
+// through a second, K=16 product of the 6-bit mins with the fp16 hi/lo sums of
+// x over each 32-element sub-block.  Per super-block and row the epilogue forms
+// y += d*(A.x) - dmin*(m.XS) in f32.
 //
 // Work split: the (128-row tile, super-block) items of the matrix, in
 // tile-major order, are cut into one contiguous, equal-sized range per CTA
 // (one CTA per SM).  A tile whose items are spread over several CTAs is
 // split-K: each writes its partial sums to scratch, and a small kernel that
-// runs after the main one adds the parts in CTA order and writes y, so the
-// result does not depend on timing.
+// runs after the main one (resident beside it, waiting on it) adds the parts
+// in CTA order and writes y, so the result does not depend on timing.
 //
 // Pipeline inside a CTA:
 //   warp 12 producer: a 2-D TMA load (tensor map over W as [n_out][row bytes])
 //           brings one 128-row x 144-byte super-block column per stage, and a
 //           1-D bulk copy brings that super-block's x tile;
-//   warps 0-7 decoders: thread (r, h) turns the 128 weights of row r, half h
-//           of the super-block into fp16 sc*q (one LOP3 + one HFMA2 per two
-//           weights), 64 weights per slot, and writes them straight into
-//           tensor memory (tcgen05.st; TMEM lane = row, two K values per
-//           column), a ring of eight slots (two super-blocks);
-//   warp 13 MMA issuer (one thread): four tcgen05.mma (M=128, N=2*NBP, K=16,
-//           A from tensor memory, x from shared memory) per slot into the
-//           super-block's TMEM accumulator, then one commit per super-block;
-//   warps 8-11 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//           lanes 32(w%4).. = its rows), the row's d, dmin and mins from the
-//           raw block, f32 scaling; frees the stage and the accumulator.
+//   warps 0-15 decoders: thread (c, r) turns the 64 weights of chunk c of
+//           row r into fp16 sc*q (one LOP3 + one HFMA2 per two weights) and
+//           writes them straight into tensor memory (tcgen05.st; TMEM lane =
+//           row, two K values per column), a ring of eight slots (two
+//           super-blocks); the chunk-0 threads also write the row's mins;
+//   warps 21-24 MMA issuers (one thread each): for super-blocks g with
+//           g % 2 == buf, thread (buf, half) issues the eight tcgen05.mma
+//           (M=128, N=2*NBP, K=16, A from tensor memory, x from shared memory)
+//           of chunks 2*half, 2*half+1 into its own TMEM accumulator (half 0
+//           also the mins product), then commits;
+//   warps 16-19 epilogue: tcgen05.ld of the three accumulators (warp w reads
+//           TMEM lanes 32(w%4).. = its rows), d and dmin from the raw block,
+//           f32 scaling; frees the stage and the accumulators.
 // Accumulators are double-buffered in TMEM; every mbarrier wait is bounded.
 //
 // x is converted once per call by a small kernel into a per-super-block image
@@ -62,23 +65,27 @@ constexpr int A_BUFS = PQ_TC_ABUFS;           // super-blocks in flight between 
 constexpr int A_SLOTS = 4 * A_BUFS;           // 64-weight slots
 constexpr int TMEM_COLS = 512;
 constexpr int A_COL = TMEM_COLS - 32 * A_SLOTS;   // TMEM column of A slot 0 (32 columns per slot)
-constexpr int DEC_WARPS = 8, EPI_WARPS = 4;
+constexpr int AMIN_COL = A_COL - 8 * A_BUFS;       // mins operand of buffer b: 8 columns at AMIN_COL + 8b
+constexpr int DEC_WARPS = 16, EPI_WARPS = 4;
 constexpr int PRODUCER_WARP = DEC_WARPS + EPI_WARPS;
-constexpr int MMA_WARP = PRODUCER_WARP + 1;   // MMA_WARP + j issues the super-blocks with g % A_BUFS == j
-constexpr int THREADS = (MMA_WARP + A_BUFS) * 32;
+constexpr int MMA_WARP = PRODUCER_WARP + 1;   // MMA_WARP + 2*buf + half: see the issuer role
+constexpr int MMA_WARPS = 2 * A_BUFS;
+constexpr int THREADS = (MMA_WARP + MMA_WARPS) * 32;
 constexpr int kMaxGrid = 160;                 // CTAs at most (partial-sum slots are sized for it)
 
 // x image of one super-block for NBP columns (N' = 2*NBP MMA columns, the hi
 // parts then the lo parts): N' x 256 fp16, K-major 8x8 core matrices, 8-row
-// groups 4096 bytes apart; then f32 XS[8][NBP], the sums over each sub-block.
+// groups 4096 bytes apart; then the mins operand N' x 16 fp16 (K = j < 8: the
+// hi or lo part of the sum of x over sub-block j; K = 8..15: zero), 8-row
+// groups 256 bytes apart.
 template <int NBP> __host__ __device__ constexpr int xmain_bytes() { return 2 * NBP * 256 * 2; }
-template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xmain_bytes<NBP>() + 8 * NBP * 4; }
+template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xmain_bytes<NBP>() + 2 * NBP * 16 * 2; }
 template <int NBP> __host__ __device__ constexpr int raw_stages() { return NBP == 16 ? 6 : 8; }
 template <int NBP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NBP>(); }
 template <int NBP> __host__ __device__ constexpr int smem_bytes() { return raw_stages<NBP>() * stage_bytes<NBP>() + 1024; }
 static_assert(stage_bytes<8>() % 128 == 0 && stage_bytes<16>() % 128 == 0, "stage alignment");
 
-// Scratch of one call: x image, then partial sums [grid][2][NBP][TM] (slot
+// Scratch of one call: x image, then partial sums [grid][2][TM][NBP] (slot
 // 2c: CTA c's first tile, 2c+1: its last tile, when split).
 template <int NBP> size_t scratch_img_bytes(int64_t k) { return (size_t)(k / 256) * btile_bytes<NBP>(); }
 template <int NBP> size_t scratch_part_bytes(int grid) { return (size_t)grid * 2 * NBP * TM * 4; }
@@ -102,17 +109,23 @@ __host__ __device__ constexpr int kmaj_off(int n, int K, int sbo) {
 }
 
 // ---------------------------------------------------------------- x image
-// One block per super-block.  Lets the main kernel launch at once (programmatic dependent launch): it sets
-// up and streams weights while this runs, and waits for it only before its
-// first x tile.
+// One block per super-block.  Launched with programmatic dependent launch: it
+// may become resident while the previous kernel on the stream finishes, and
+// waits for that kernel before anything else.  Only then does it let the main
+// kernel launch, so that the weights the main kernel starts streaming at once
+// are complete even when the previous kernel wrote them; the main kernel waits
+// for this one only before its first x tile.
 template <int NBP>
 __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, int k, int nb_cols,
                                                  uint8_t *__restrict__ img) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int sb = blockIdx.x;
+    constexpr int NP = 2 * NBP;
     uint8_t *tile = img + (size_t)sb * btile_bytes<NBP>();
     __half *out = reinterpret_cast<__half *>(tile);
-    float *xs_out = reinterpret_cast<float *>(tile + xmain_bytes<NBP>());
+    __half *om = reinterpret_cast<__half *>(tile + xmain_bytes<NBP>());
+    __shared__ float xs[NBP][8];
     const int t = threadIdx.x;
     // sub-block sums, fixed order (thread per (column, sub-block), 8 vector loads)
     if (t < NBP * 8) {
@@ -126,7 +139,19 @@ __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, in
 #pragma unroll
             for (int i = 0; i < 8; ++i) s = s + v[i].x + v[i].y + v[i].z + v[i].w;
         }
-        xs_out[j * NBP + b] = s;
+        xs[b][j] = s;
+    }
+    __syncthreads();
+    // mins operand: K = j < 8 holds the sums (hi part for n < NBP, lo part after), K = 8..15 zero
+    for (int i = t; i < NP * 16; i += 256) {
+        const int n = i / 16, K = i % 16;
+        float v = 0.f;
+        if (K < 8) {
+            const float s = xs[n % NBP][K];
+            const __half hi = __float2half_rn(s);
+            v = n < NBP ? __half2float(hi) : __half2float(__float2half_rn(s - __half2float(hi)));
+        }
+        om[kmaj_off(n, K, 256) / 2] = __float2half_rn(v);
     }
     // main part: thread t = K index; all column loads in flight together
     const int K = t;
@@ -184,6 +209,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+// Each thread writes 8 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -277,12 +308,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int NSR = raw_stages<NBP>();
     constexpr int STAGE = stage_bytes<NBP>();
     constexpr uint32_t IDESC = instr_desc(TM, NP);
-    static_assert(A_BUFS * NP <= A_COL, "accumulators below the A slots");
+    static_assert(3 * A_BUFS * NP <= AMIN_COL, "accumulators below the A operands");
     static_assert(A_COL + 32 * A_SLOTS <= TMEM_COLS, "A slots fit in the allocation");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
-    __shared__ __align__(8) uint64_t a_full[A_BUFS];
+    __shared__ __align__(8) uint64_t a_full[A_BUFS][2];
     __shared__ __align__(8) uint64_t item_done[A_BUFS], acc_empty[A_BUFS];
     __shared__ uint32_t tmem_base_sh;
 
@@ -300,9 +331,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], EPI_WARPS);
         }
-        for (int s = 0; s < A_BUFS; ++s) mbar_init(&a_full[s], DEC_WARPS);
         for (int s = 0; s < A_BUFS; ++s) {
-            mbar_init(&item_done[s], 1);
+            mbar_init(&a_full[s][0], DEC_WARPS / 2);
+            mbar_init(&a_full[s][1], DEC_WARPS / 2);
+            mbar_init(&item_done[s], 2);
             mbar_init(&acc_empty[s], EPI_WARPS);
         }
         fence_mbar_init();
@@ -332,8 +364,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint8_t *st = ring + slot * STAGE;
                 mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)STAGE);
                 tma_load_2d(st, &wmap, sb * 144, tile * TM, &raw_full[slot]);
-                // the weights were complete before the x-prep kernel started; the x
-                // image is that kernel's output: wait for it once, before its first use
+                // the weights were complete before the x-prep kernel let this kernel
+                // launch; the x image is that kernel's output: wait for it once,
+                // before its first use
                 if (g == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NBP>(), (uint32_t)btile_bytes<NBP>(),
                               &raw_full[slot], pol);
@@ -341,40 +374,46 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp >= MMA_WARP) {
-        // ---------------- MMA issuers (one thread per A buffer) ----------------
-        // Several issuing threads keep the tensor core busy: one thread's
-        // tcgen05 instructions and waits are issued one after another.
-        const int buf = warp - MMA_WARP;
+        // ---------------- MMA issuers ----------------
+        // Thread (buf, half) issues, for the super-blocks g with g % A_BUFS ==
+        // buf, the eight products of chunks 2*half and 2*half+1 into its own
+        // accumulator.  Several issuing threads keep the tensor core busy: one
+        // thread's tcgen05 instructions and waits go out one after another.
+        const int buf = (warp - MMA_WARP) >> 1, half = (warp - MMA_WARP) & 1;
         if (lane == 0) {
             bool dead = false;
             for (int g = buf; g < count; g += A_BUFS) {
                 const int slot = g % NSR;
                 const uint32_t par = (uint32_t)(g / A_BUFS) & 1u;
                 // accumulator free (epilogue done with super-block g - A_BUFS), then
-                // the A tile decoded; the decoders saw the stage (weights and x tile)
-                // complete before they arrived
+                // the two A chunks decoded; the decoders saw the stage (weights and
+                // x tile) complete before they arrived
                 if (!dead && !mbar_wait(&acc_empty[buf], par ^ 1u)) dead = true;
-                if (!dead && !mbar_wait(&a_full[buf], par)) dead = true;
+                if (!dead && !mbar_wait(&a_full[buf][half], par)) dead = true;
                 tc_fence_after();
                 if (!dead) {
-                    // the super-block's 16 products back to back, no branch between them
-                    const uint32_t d_acc = tmem + (uint32_t)(buf * NP);
-                    const uint32_t a0 = tmem + (uint32_t)(A_COL + 32 * 4 * buf);
-                    const uint64_t b0 = smem_desc(smem_u32(ring + slot * STAGE + RAW_BYTES), 128u, 4096u);
+                    // eight products back to back, no branch between them
+                    const uint32_t d_acc = tmem + (uint32_t)((3 * buf + half) * NP);
+                    const uint32_t a0 = tmem + (uint32_t)(A_COL + 32 * (4 * buf + 2 * half));
+                    const uint32_t bst = smem_u32(ring + slot * STAGE + RAW_BYTES);
+                    const uint64_t b0 = smem_desc(bst + 2048 * half, 128u, 4096u);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_f16_ta(d_acc, a0 + (uint32_t)(32 * c + 8 * ks), b0 + (uint64_t)(16 * (4 * c + ks)),
-                                       IDESC, (c | ks) ? 1u : 0u);
+                            mma_f16_ta(d_acc, a0 + (uint32_t)(32 * cl + 8 * ks), b0 + (uint64_t)(16 * (4 * cl + ks)),
+                                       IDESC, (cl | ks) ? 1u : 0u);
+                    if (half == 0)
+                        mma_f16_ta(tmem + (uint32_t)((3 * buf + 2) * NP), tmem + (uint32_t)(AMIN_COL + 8 * buf),
+                                   smem_desc(bst + xmain_bytes<NBP>(), 128u, 256u), IDESC, 0u);
                 }
                 mma_commit(&item_done[buf]);
             }
         }
     } else if (warp >= DEC_WARPS) {
-        // ---------------- epilogue (warps 8-11) ----------------
-        const int r = 32 * (warp - DEC_WARPS) + lane;                       // row within the tile = TMEM lane
-        const uint32_t row_taddr = tmem + ((uint32_t)(32 * (warp - DEC_WARPS)) << 16);
+        // ---------------- epilogue (warps 16-19) ----------------
+        const int r = 32 * (warp & 3) + lane;                              // row within the tile = TMEM lane
+        const uint32_t row_taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const int first_tile = (int)(i0 / nb);
         float yacc[NBP];
 #pragma unroll
@@ -386,51 +425,39 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int slot = g % NSR;
             const int buf = g % A_BUFS;
             const uint32_t par = (uint32_t)(g / A_BUFS) & 1u;
+            // d and dmin of row r (the stage is held until this warp frees it)
+            const uint8_t *st = ring + slot * STAGE;
             if (!dead && !mbar_wait(&item_done[buf], par)) dead = true;
             tc_fence_after();
-            float dot[NBP];
-            if constexpr (NP == 32) {
-                uint32_t t0[32];
-                tmem_ld32(row_taddr + (uint32_t)(buf * NP), t0);
-                tmem_ld_wait(t0);
+            const uint32_t dd = *reinterpret_cast<const uint32_t *>(st + r * 144);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[slot]);
+            const float d = h2f(dd), dmin = h2f(dd >> 16);
+            // the super-block's three accumulators (two halves of the products,
+            // the mins product), each with hi and lo x columns
 #pragma unroll
-                for (int b = 0; b < NBP; ++b) dot[b] = __uint_as_float(t0[b]) + __uint_as_float(t0[NBP + b]);
-            } else {
-                uint32_t t0[16];
-                tmem_ld16(row_taddr + (uint32_t)(buf * NP), t0);
-                tmem_ld_wait(t0);
+            for (int part = 0; part < 3; ++part) {
+                const uint32_t taddr = row_taddr + (uint32_t)((3 * buf + part) * NP);
+                const float sc = part < 2 ? d : -dmin;
+                if constexpr (NP == 32) {
+                    uint32_t t[32];
+                    tmem_ld32(taddr, t);
+                    tmem_ld_wait(t);
 #pragma unroll
-                for (int b = 0; b < NBP; ++b) dot[b] = __uint_as_float(t0[b]) + __uint_as_float(t0[NBP + b]);
+                    for (int b = 0; b < NBP; ++b)
+                        yacc[b] = fmaf(sc, __uint_as_float(t[b]) + __uint_as_float(t[NBP + b]), yacc[b]);
+                } else {
+                    uint32_t t[16];
+                    tmem_ld16(taddr, t);
+                    tmem_ld_wait(t);
+#pragma unroll
+                    for (int b = 0; b < NBP; ++b)
+                        yacc[b] = fmaf(sc, __uint_as_float(t[b]) + __uint_as_float(t[NBP + b]), yacc[b]);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            // d, dmin and the eight 6-bit mins of row r; sub-block sums of x
-            const uint8_t *st = ring + slot * STAGE;
-            const uint4 hd = *reinterpret_cast<const uint4 *>(st + r * 144);
-            const uint32_t mlo = hd.z & 0x3F3F3F3Fu;
-            const uint32_t mhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-            const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-            const float4 *xs = reinterpret_cast<const float4 *>(st + RAW_BYTES + xmain_bytes<NBP>());
-            float mn[NBP];
-#pragma unroll
-            for (int b = 0; b < NBP; ++b) mn[b] = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float m = (float)((j < 4 ? (mlo >> (8 * j)) : (mhi >> (8 * (j - 4)))) & 0xFFu);
-#pragma unroll
-                for (int b4 = 0; b4 < NBP / 4; ++b4) {
-                    const float4 v = xs[j * (NBP / 4) + b4];
-                    mn[4 * b4 + 0] = fmaf(m, v.x, mn[4 * b4 + 0]);
-                    mn[4 * b4 + 1] = fmaf(m, v.y, mn[4 * b4 + 1]);
-                    mn[4 * b4 + 2] = fmaf(m, v.z, mn[4 * b4 + 2]);
-                    mn[4 * b4 + 3] = fmaf(m, v.w, mn[4 * b4 + 3]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[slot]);
-#pragma unroll
-            for (int b = 0; b < NBP; ++b) yacc[b] = fmaf(d, dot[b], fmaf(-dmin, mn[b], yacc[b]));
 
             if (sb == nb - 1 || g == count - 1) {
                 // the CTA's part of this tile is complete
@@ -446,9 +473,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
                     // split tile: this CTA's part, added up by the finishing kernel
                     const int side = tile == first_tile ? 0 : 1;
-                    float *mine = p.partials + ((size_t)(blockIdx.x * 2 + side) * NBP) * TM;
+                    float4 *mine = reinterpret_cast<float4 *>(p.partials + ((size_t)(blockIdx.x * 2 + side) * TM + r) * NBP);
 #pragma unroll
-                    for (int b = 0; b < NBP; ++b) mine[b * TM + r] = yacc[b];
+                    for (int b4 = 0; b4 < NBP / 4; ++b4)
+                        mine[b4] = make_float4(yacc[4 * b4], yacc[4 * b4 + 1], yacc[4 * b4 + 2], yacc[4 * b4 + 3]);
                 }
 #pragma unroll
                 for (int b = 0; b < NBP; ++b) yacc[b] = 0.f;
@@ -456,9 +484,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (++sb == nb) { sb = 0; ++tile; }
         }
     } else {
-        // ---------------- decoders (warps 0-7) ----------------
-        const int r = threadIdx.x & 127;        // row within the tile
-        const int h = threadIdx.x >> 7;         // half of the super-block: sub-blocks 4h..4h+3
+        // ---------------- decoders (warps 0-15) ----------------
+        // thread (c, r): chunk c (weights 64c..64c+63: sub-blocks 2c, 2c+1) of row r
+        const int c = warp >> 2;
+        const int r = 32 * (warp & 3) + lane;
+        const int h = c >> 1, cc = c & 1;
         const uint32_t mA = h ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
         const uint32_t mB = h ? 0x30303030u : 0u;
         const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's TMEM lanes
@@ -471,49 +501,57 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!dead && !mbar_wait(&raw_full[slot], ph)) dead = true;
             const uint8_t *blk = ring + slot * STAGE + r * 144;
             const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
-            uint4 qw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) qw[i] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * h + 16 * i);
-            // 6-bit scales of sub-blocks 4h..4h+3, one per byte
+            const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+            const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+            // 6-bit scales of sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
             const uint32_t sc4 = ((h ? hd.w : hd.y) & mA) | ((hd.y >> 2) & mB);
+            // scale pairs: low nibbles -> (1024+q)*sc - 1024*sc, high nibbles -> (1024+16q)*sc/16 - 64*sc
+            const __half slo = __int2half_rn((int)((sc4 >> (16 * cc)) & 0xFF));
+            const __half shi = __int2half_rn((int)((sc4 >> (16 * cc + 8)) & 0xFF));
+            const uint32_t Slo = h2_bits(__halves2half2(slo, slo));
+            const uint32_t Clo = h2_bits(__hmul2(__halves2half2(slo, slo), __float2half2_rn(-1024.0f)));
+            const uint32_t Shi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(0.0625f)));
+            const uint32_t Chi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(-64.0f)));
+            const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            // the chunk's 64 K values of row r: TMEM column j holds K = 2j, 2j+1
+            uint32_t R[32];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const uint32_t w0 = w[2 * a], w1 = w[2 * a + 1];
+                const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+                R[4 * a + 0] = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                R[4 * a + 1] = hfma2_u((s0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                R[4 * a + 2] = hfma2_u((w1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                R[4 * a + 3] = hfma2_u((s1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
+                R[16 + 4 * a + 0] = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                R[16 + 4 * a + 1] = hfma2_u((s0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                R[16 + 4 * a + 2] = hfma2_u((w1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                R[16 + 4 * a + 3] = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+            }
             // this buffer's slots are free once the products of the super-block
             // that used them before are complete
             if (!dead && !mbar_wait(&item_done[buf], par ^ 1u)) dead = true;
             tc_fence_after();
+            tmem_st32(a_lane + (uint32_t)(A_COL + 32 * (4 * buf + c)), R);
+            if (c == 0) {
+                // the row's mins product operand: m_0..m_7 at K = 0..7, zero at K = 8..15
+                const uint32_t mlo = hd.z & 0x3F3F3F3Fu;
+                const uint32_t mhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+                uint32_t M[8];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * h + cc;           // 64-weight chunk of the super-block
-                const int as = 4 * buf + c;         // its A slot
-                // scale pairs: low nibbles -> (1024+q)*sc - 1024*sc, high nibbles -> (1024+16q)*sc/16 - 64*sc
-                const __half slo = __int2half_rn((int)((sc4 >> (16 * cc)) & 0xFF));
-                const __half shi = __int2half_rn((int)((sc4 >> (16 * cc + 8)) & 0xFF));
-                const uint32_t Slo = h2_bits(__halves2half2(slo, slo));
-                const uint32_t Clo = h2_bits(__hmul2(__halves2half2(slo, slo), __float2half2_rn(-1024.0f)));
-                const uint32_t Shi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(0.0625f)));
-                const uint32_t Chi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(-64.0f)));
-                const uint32_t w[8] = {qw[2 * cc].x, qw[2 * cc].y, qw[2 * cc].z, qw[2 * cc].w,
-                                       qw[2 * cc + 1].x, qw[2 * cc + 1].y, qw[2 * cc + 1].z, qw[2 * cc + 1].w};
-                // the slot's 64 K values of row r: TMEM column j holds K = 2j, 2j+1
-                uint32_t R[32];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const uint32_t w0 = w[2 * a], w1 = w[2 * a + 1];
-                    const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-                    R[4 * a + 0] = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    R[4 * a + 1] = hfma2_u((s0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    R[4 * a + 2] = hfma2_u((w1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    R[4 * a + 3] = hfma2_u((s1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                    R[16 + 4 * a + 0] = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    R[16 + 4 * a + 1] = hfma2_u((s0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    R[16 + 4 * a + 2] = hfma2_u((w1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                    R[16 + 4 * a + 3] = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t src = i < 2 ? mlo : mhi;
+                    const int sh = 16 * (i & 1);
+                    M[i] = h2_bits(__halves2half2(__int2half_rn((int)((src >> sh) & 0xFFu)),
+                                                  __int2half_rn((int)((src >> (sh + 8)) & 0xFFu))));
+                    M[4 + i] = 0u;
                 }
-                tmem_st32(a_lane + (uint32_t)(A_COL + 32 * as), R);
+                tmem_st8(a_lane + (uint32_t)(AMIN_COL + 8 * buf), M);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[buf]);
+            if (lane == 0) mbar_arrive(&a_full[buf][h]);
         }
     }
 
@@ -527,11 +565,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // Split-K finish: block c adds up the tile whose first contributor is CTA c
 // (the last tile of c's range, when later CTAs share it), parts in CTA order.
-// Launched after the main kernel (programmatic dependent launch: it may be
-// resident early and waits for the main grid to complete).
+// Launched after the main kernel with programmatic dependent launch: it can be
+// resident beside it and waits for the main grid to complete.
 template <int NBP>
 __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partials, float *__restrict__ y,
                                                long long ldy, long long total, int nb, int n_out, int nb_cols) {
+    asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int grid = (int)gridDim.x, c = (int)blockIdx.x;
     const long long last_item = item_begin(c + 1, total, grid) - 1;
@@ -544,11 +583,31 @@ __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partia
     float sum[NBP];
 #pragma unroll
     for (int b = 0; b < NBP; ++b) sum[b] = 0.f;
-    for (int cc = c; cc <= cl; ++cc) {
-        const int side = tile == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
-        const float *part = partials + ((size_t)(cc * 2 + side) * NBP) * TM;
+    // four contributors' parts in flight at a time, added in CTA order
+    for (int c0 = c; c0 <= cl; c0 += 4) {
+        float4 v[4][NBP / 4];
 #pragma unroll
-        for (int b = 0; b < NBP; ++b) sum[b] += part[b * TM + r];
+        for (int u = 0; u < 4; ++u) {
+            const int cc = c0 + u;
+            if (cc <= cl) {
+                const int side = tile == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
+                const float4 *part = reinterpret_cast<const float4 *>(partials + ((size_t)(cc * 2 + side) * TM + r) * NBP);
+#pragma unroll
+                for (int b4 = 0; b4 < NBP / 4; ++b4) v[u][b4] = part[b4];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u <= cl) {
+#pragma unroll
+                for (int b4 = 0; b4 < NBP / 4; ++b4) {
+                    sum[4 * b4 + 0] += v[u][b4].x;
+                    sum[4 * b4 + 1] += v[u][b4].y;
+                    sum[4 * b4 + 2] += v[u][b4].z;
+                    sum[4 * b4 + 3] += v[u][b4].w;
+                }
+            }
+        }
     }
     if (row < n_out) {
 #pragma unroll
@@ -557,7 +616,7 @@ __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partia
     }
 }
 
-// Whether any tile is split over several CTAs.
+// Whether any tile is split over several CTAs (same arithmetic as item_begin/item_owner).
 bool any_split(long long total, int nb, int grid) {
     for (int c = 0; c < grid; ++c) {
         const long long last_item = ((long long)(c + 1) * total) / grid - 1;
@@ -623,8 +682,17 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     const int nb = (int)(k / 256);
     uint8_t *img = scratch;
     float *partials = reinterpret_cast<float *>(scratch + scratch_img_bytes<NBP>(k));
-    prep_x_tc<NBP><<<nb, 256, 0, s>>>(x, (int)k, batch, img);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3(nb);
+    pcfg.blockDim = dim3(256);
+    pcfg.stream = s;
+    pcfg.attrs = attr;
+    pcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&pcfg, prep_x_tc<NBP>, x, (int)k, batch, img);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     EncodeTiled enc = encode_fn();
@@ -653,9 +721,6 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = (size_t)smem_bytes<NBP>();
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
@@ -671,14 +736,14 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
 
 // Fixed scratch for the allocation-free entry point (pq_gemv_noalloc): x image
 // for k up to kNoAllocMaxK at up to 16 columns and split-K partial sums for up
-// to kMaxGrid CTAs: 3,702,784 bytes.  Every GPU that loads
+// to kMaxGrid CTAs: 3,735,552 bytes.  Every GPU that loads
 // this library keeps it until the process exits.  In host code the name is
 // only a stand-in for the device array; its device address comes from
 // cudaGetSymbolAddress, once per device.
 constexpr int kNoAllocMaxK = 16384;
 constexpr size_t kNoAllocScratchBytes =
     (size_t)(kNoAllocMaxK / 256) * (size_t)btile_bytes<16>() + (size_t)kMaxGrid * 2 * 16 * TM * 4;
-static_assert(kNoAllocScratchBytes == 3702784, "stated size");
+static_assert(kNoAllocScratchBytes == 3735552, "stated size");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 uint8_t *noalloc_scratch_ptr() {
