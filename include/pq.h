@@ -121,7 +121,14 @@ int pq_gemv_kernel(pq_fmt fmt, const void *w_blocks, int n_out, int k,
  * for arguments it would reject. */
 int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch);
 
-/* Number of kernel launches one pq_gemv call with these arguments makes. */
+/*
+ * Number of batch slices one pq_gemv call with these arguments runs (slices
+ * of up to 16 columns for the tensor-core kernel, up to 4 otherwise), each
+ * with one kernel choice.  A slice is one launch of its kernel, plus, for the
+ * tensor-core and the batch-2 long-row kernels, one small x-conversion launch
+ * before it, and for the tensor-core kernel one split-K finishing launch after
+ * it when CTAs share a row tile.
+ */
 int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch);
 
 /*

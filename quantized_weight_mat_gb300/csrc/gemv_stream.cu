@@ -136,7 +136,8 @@ __device__ __forceinline__ void prep_x_block(const float *xb, uint8_t *img, uint
 
 // The x image of one column, blocks q = first, first+step, ...: the loads of
 // up to eight blocks are in flight before any of them is converted.  x is
-// read from global memory, or (FROM_SMEM) from a shared-memory copy.
+// read from global memory, or (FROM_SMEM) from a shared-memory copy; a null
+// xb stands for a column of zeros.
 template <bool FROM_SMEM = false>
 __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_t *meta, int nb,
                                            int S, int first, int step, int lane) {
@@ -147,8 +148,11 @@ __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_
             const int q = q0 + r * step;
             if (q < nb) {
                 const float *xq = xb + q * 256 + 8 * lane;
-                const float4 a = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq) : ldg_f4(xq);
-                const float4 b = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq + 4) : ldg_f4(xq + 4);
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;   // a null xb is a zero column
+                if (xb) {
+                    a = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq) : ldg_f4(xq);
+                    b = FROM_SMEM ? *reinterpret_cast<const float4 *>(xq + 4) : ldg_f4(xq + 4);
+                }
                 v[r][0] = a.x; v[r][1] = a.y; v[r][2] = a.z; v[r][3] = a.w;
                 v[r][4] = b.x; v[r][5] = b.y; v[r][6] = b.z; v[r][7] = b.w;
             }
@@ -843,6 +847,423 @@ inline bool takes(int fmt, int64_t k, int64_t n_out) {
 }
 }  // namespace rowk
 
+// ---------------------------------------------------------------------------
+// Batch 2 (NB = 2; NB = 4 also works, batch 3 as 4 with a zero column, but is
+// not the fastest choice there), Q4_K: the whole-row kernel for NB columns.  A lane owns 256/(2*NB) weights of one super-block (chunk c
+// = 64 weights for NB = 2; half a chunk, 16 bytes of qs = 32 weights over two
+// sub-blocks, for NB = 4), so the x limbs of all NB columns for its k range
+// still fit in 64 registers; a warp covers 32/(2*NB) super-blocks and G warps
+// a row.  Stages are runs of whole rows (one bulk copy each) as at batch 1;
+// each lane's partial products of four rows x NB columns are reduced with one
+// transposed shuffle tree, split rows (G > 1) in shared memory in fixed order.
+//
+// x is converted once per call by prep_x_nb into the limb image (2.25 bytes
+// per element per column) in scratch memory; each CTA fetches that image with
+// one bulk copy.  Both kernels use programmatic dependent launch: prep_x_nb
+// waits for the previous kernel before it lets this one launch, so the
+// weights this kernel streams at once are complete, and this kernel waits for
+// prep_x_nb only before its x copy.
+namespace rowsnb {
+constexpr int CW = 15;                       // consumer warps (with the producer: 512 threads, 128 registers)
+constexpr int THREADS = (CW + 1) * 32;
+constexpr int MAX_STAGES = 8;
+constexpr int kStatic = 512;
+
+template <int NB> struct Geo {
+    static constexpr int LPB = 2 * NB;       // lanes per super-block
+    static constexpr int KW = 32 / LPB;      // super-blocks per warp
+    static constexpr int V = 4 * NB;         // values per lane per iteration (4 rows x NB columns)
+    static constexpr int LOGV = NB == 2 ? 3 : 4;
+};
+
+// Bytes of one column of the limb image: 2k of limb groups, then k/64 x 16
+// bytes of metadata (the layout prep_x_vals writes).
+inline __host__ __device__ int col_bytes(int64_t k) { return (int)(2 * k + (k / 64) * 16); }
+
+struct Params {
+    const uint8_t *w;
+    const uint8_t *x_img;   // NB columns of col_bytes(k), from prep_x_nb
+    float *y;
+    long long ldy;
+    int n_out;
+    int k;
+    int nb_cols;    // real columns (<= NB); the others are zero
+    int G;          // warps per row
+    int NG;         // row groups
+    int RS;         // rows per stage
+    int nstages;
+    int rows_cap;
+    int early_w;
+};
+
+template <int NB> inline int segments(int64_t k) { return (int)((k / 256 + Geo<NB>::KW - 1) / Geo<NB>::KW); }
+template <int NB> inline int red_bytes(const Params &p) {
+    return p.G > 1 ? (p.rows_cap * p.G * NB * 4 + 15) / 16 * 16 : 0;
+}
+
+template <int NB> inline bool plan(int64_t k, int64_t n_out, int grid, Params &p) {
+    if (k % 256 || grid < 1) return false;
+    const int G = segments<NB>(k);
+    if (G < 1 || G > CW) return false;
+    p.G = G;
+    p.NG = CW / G;
+    p.RS = 2 * p.NG;
+    p.rows_cap = (int)((n_out + grid - 1) / grid);
+    const int64_t stage = (int64_t)p.RS * (k / 256) * 144;
+    const int64_t avail = kSmemBudget - kStatic - (int64_t)NB * col_bytes(k) - red_bytes<NB>(p);
+    int64_t ns = avail / stage;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    p.nstages = (int)ns;
+    return ns >= 2;
+}
+
+// Sum over the warp's 32 lanes of each of V values; afterwards lane l holds the
+// total of value l >> (5 - LOGV) (a transposed tree: each step halves the
+// values a lane carries).
+template <int V, int LOGV>
+__device__ __forceinline__ float transposed_sum(float (&v)[V], int lane) {
+#pragma unroll
+    for (int st = 0; st < LOGV; ++st) {
+        const int o = 16 >> st, n = V >> st;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 >> LOGV; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// Limb image of NB columns: warp w of block (i, b) converts 256-value block
+// 8i + w of column b (zeros for b >= nb_cols).
+template <int NB>
+__global__ void __launch_bounds__(256) prep_x_nb(const float *__restrict__ x, int k, int nb_cols,
+                                                 uint8_t *__restrict__ img) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = blockIdx.x * 8 + warp, b = blockIdx.y;
+    const int nb = k / 256;
+    if (q >= nb) return;
+    uint8_t *col = img + (size_t)b * col_bytes(k);
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (b < nb_cols) {
+        const float *xq = x + (size_t)b * k + q * 256 + 8 * lane;
+        const float4 a = ldg_f4(xq), c = ldg_f4(xq + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    }
+    prep_x_vals(v, col, col + 2 * k, q, k / 64, lane);
+}
+
+template <int NB>
+__global__ void __launch_bounds__(THREADS, 1) gemv_rows_nb(Params p) {
+    using Gm = Geo<NB>;
+    constexpr int W4 = 8 / (NB / 2);         // qs words per lane: 8 (NB = 2) or 4 (NB = 4)
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t x_bar;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.k / 256;
+    const int S = p.k / 64;
+    const int CB = col_bytes(p.k);
+    const uint32_t rowbytes = (uint32_t)nb * 144u;
+    const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
+    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
+    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
+    const int units = (nrows + RS - 1) / RS;
+    const int NS = p.nstages;
+    const uint32_t stage_bytes = (uint32_t)RS * rowbytes;
+    uint8_t *ximg = smem + (size_t)NS * stage_bytes;            // NB columns of CB bytes
+    float *red = reinterpret_cast<float *>(ximg + (size_t)NB * CB);
+    const uint32_t ring_s = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], CA);
+        }
+        mbar_init(&x_bar, 1);
+        fence_mbar_init();
+    }
+    rowk::grid_dep_launch();
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer: one contiguous copy per stage ----------------
+        if (lane == 0) {
+            // the first ring's worth of weights, then (after prep_x_nb) the x image
+            const int early = units < NS ? units : NS;
+            const uint64_t pol = make_evict_first_policy();
+            const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
+            int slot = 0;
+            uint32_t ph = 0;
+            for (int u = 0; u <= units; ++u) {
+                if (u == early) {
+                    rowk::grid_dep_wait();
+                    mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
+                    bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                }
+                if (u == units) break;
+                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
+                const uint32_t bytes = (uint32_t)rows * rowbytes;
+                if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_g2s_hint(smem + (size_t)slot * stage_bytes, src, bytes, &full_bar[slot], pol);
+                src += (size_t)RS * rowbytes;
+                if (++slot == NS) { slot = 0; ph ^= 1u; }
+            }
+        }
+        return;
+    }
+
+    if (warp >= CA) return;
+    bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
+    if (!mbar_wait(&x_bar, 0)) dead = true;
+
+    const int gi = warp / G, seg = warp - gi * G;
+    const int part = lane % Gm::LPB;
+    const int kb = seg * Gm::KW + lane / Gm::LPB;
+    const bool valid = kb < nb;
+    const int kbc = valid ? kb : nb - 1;       // idle lanes read a real block, weight 0
+    // chunk c (sub-blocks 2c, 2c+1) and, for NB = 4, the 16-byte half h of its qs
+    const int c = NB == 2 ? part : part >> 1;
+    const int h = NB == 2 ? 0 : (part & 1);
+    const int slice = 4 * kbc + c;
+
+    // x limbs of the lane's positions, per column: [b][0..W4) xh of sub-block 2c,
+    // then 2c+1; xl likewise
+    uint32_t xh0[NB][W4], xh1[NB][W4], xl0[NB][W4], xl1[NB][W4];
+    int xs0[NB], xs1[NB];
+    float u[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const uint8_t *img = ximg + (size_t)b * CB;
+        const uint8_t *meta = img + 2 * p.k;
+        if constexpr (NB == 2) {
+            uint4 g[8];
+#pragma unroll
+            for (int gi2 = 0; gi2 < 8; ++gi2) g[gi2] = *reinterpret_cast<const uint4 *>(img + (gi2 * S + slice) * 16);
+            const uint32_t *gw = reinterpret_cast<const uint32_t *>(g);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                xh0[b][i] = gw[i];
+                xh1[b][i] = gw[8 + i];
+                xl0[b][i] = gw[16 + i];
+                xl1[b][i] = gw[24 + i];
+            }
+        } else {
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(img + ((0 + h) * S + slice) * 16);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(img + ((2 + h) * S + slice) * 16);
+            const uint4 a2 = *reinterpret_cast<const uint4 *>(img + ((4 + h) * S + slice) * 16);
+            const uint4 a3 = *reinterpret_cast<const uint4 *>(img + ((6 + h) * S + slice) * 16);
+            const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w}, w1[4] = {a1.x, a1.y, a1.z, a1.w};
+            const uint32_t w2[4] = {a2.x, a2.y, a2.z, a2.w}, w3[4] = {a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xh0[b][i] = w0[i];
+                xh1[b][i] = w1[i];
+                xl0[b][i] = w2[i];
+                xl1[b][i] = w3[i];
+            }
+        }
+        const int4 mt = *reinterpret_cast<const int4 *>(meta + slice * 16);
+        // the sub-block sums go with one lane of each sub-block pair (h == 0)
+        xs0[b] = h == 0 ? mt.x : 0;
+        xs1[b] = h == 0 ? mt.y : 0;
+        u[b] = valid ? __int_as_float(mt.z) : 0.f;
+    }
+
+    // byte selectors for (sc, m) of sub-blocks 2c and 2c+1 from the packed scales
+    const uint32_t c2 = 2u * (uint32_t)(c & 1);
+    const uint32_t selP = c2 | ((c2 + 1) << 4) | ((c2 + 4) << 8) | ((c2 + 5) << 12);
+    const uint32_t selQ = c2 | ((c2 + 1) << 4) | (c2 << 8) | ((c2 + 1) << 12);
+    const uint32_t lane_base = ring_s + (uint32_t)kbc * 144u;
+    const uint32_t qoff = 16u + 32u * (uint32_t)c + 16u * (uint32_t)h;
+
+    // products of one row (block at shared address blk) with all NB columns
+    auto row_dot = [&](uint32_t blk, float (&out)[NB]) {
+        const uint4 hd = lds128(blk);
+        uint32_t wq[W4];
+        {
+            const uint4 qa = lds128(blk + qoff);
+            wq[0] = qa.x; wq[1] = qa.y; wq[2] = qa.z; wq[3] = qa.w;
+            if constexpr (W4 == 8) {
+                const uint4 qb = lds128(blk + qoff + 16);
+                wq[4] = qb.x; wq[5] = qb.y; wq[6] = qb.z; wq[7] = qb.w;
+            }
+        }
+        const uint32_t P = __byte_perm(hd.y, hd.z, selP);
+        uint32_t r4;
+        if (c < 2) {
+            r4 = P & 0x3F3F3F3Fu;
+        } else {
+            const uint32_t Q = __byte_perm(hd.w, 0u, selQ);
+            r4 = ((P >> 2) & 0x30303030u) | (Q & 0x00000F0Fu) | ((Q >> 4) & 0x0F0F0000u);
+        }
+        const int sc0x16 = (int)((r4 << 4) & 0xFF0u), sc1 = (int)((r4 >> 8) & 0xFFu);
+        const int m0 = (int)((r4 >> 16) & 0xFFu), m1 = (int)(r4 >> 24);
+        const float d16 = h2f(hd.x) * 0.0625f, dmin = h2f(hd.x >> 16);
+        uint32_t lo[W4], hi[W4];
+#pragma unroll
+        for (int i = 0; i < W4; ++i) {
+            lo[i] = wq[i] & 0x0F0F0F0Fu;
+            hi[i] = wq[i] & 0xF0F0F0F0u;     // 16*q: rescaled by d/16 below
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0;
+#pragma unroll
+            for (int i = 0; i < W4; ++i) {
+                dh0 = dp4a_ss(lo[i], xh0[b][i], dh0);
+                dl0 = dp4a_ss(lo[i], xl0[b][i], dl0);
+                dh1 = dp4a_us(hi[i], xh1[b][i], dh1);
+                dl1 = dp4a_us(hi[i], xl1[b][i], dl1);
+            }
+            const int H = sc0x16 * dh0 + sc1 * dh1;
+            const int L = sc0x16 * dl0 + sc1 * dl1;
+            const int M = m0 * xs0[b] + m1 * xs1[b];
+            out[b] = u[b] * (d16 * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+        }
+    };
+
+    const uint32_t rA0 = (uint32_t)gi * rowbytes, rA1 = (uint32_t)(gi + NG) * rowbytes;
+    constexpr int SHIFT = 5 - Gm::LOGV;                 // lane >> SHIFT = value index after the tree
+    const int my_v = lane >> SHIFT;
+    const int my_t = my_v / NB, my_b = my_v % NB;       // row slot (0,1 stage A; 2,3 stage B), column
+    const int my_rowoff = gi + ((my_t & 1) ? NG : 0);
+
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int uu = 0; uu < units; uu += 2) {
+        const bool hasB = uu + 1 < units;
+        const int slotA = slot;
+        const uint32_t phA = ph;
+        if (++slot == NS) { slot = 0; ph ^= 1u; }
+        const int slotB = slot;
+        const uint32_t phB = ph;
+        if (hasB) {
+            if (++slot == NS) { slot = 0; ph ^= 1u; }
+        }
+        const int nA = nrows - uu * RS < RS ? nrows - uu * RS : RS;
+        const int nB = hasB ? (nrows - (uu + 1) * RS < RS ? nrows - (uu + 1) * RS : RS) : 0;
+        float v[Gm::V];
+        float tmp[NB];
+        if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
+        {
+            const uint32_t sA = lane_base + (uint32_t)slotA * stage_bytes;
+            row_dot(sA + rA0, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[b] = gi < nA ? tmp[b] : 0.f;
+            row_dot(sA + rA1, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[NB + b] = gi + NG < nA ? tmp[b] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slotA]);
+        if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
+        {
+            const uint32_t sB = lane_base + (uint32_t)slotB * stage_bytes;
+            row_dot(sB + rA0, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[2 * NB + b] = gi < nB ? tmp[b] : 0.f;
+            row_dot(sB + rA1, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[3 * NB + b] = gi + NG < nB ? tmp[b] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0 && hasB) mbar_arrive(&empty_bar[slotB]);
+        const float tot = transposed_sum<Gm::V, Gm::LOGV>(v, lane);
+        if ((lane & ((1 << SHIFT) - 1)) == 0 && my_b < p.nb_cols) {
+            const int n_here = my_t >= 2 ? nB : nA;
+            if (my_rowoff < n_here) {
+                const int row = (uu + (my_t >= 2 ? 1 : 0)) * RS + my_rowoff;   // relative to r0
+                if (G == 1)
+                    p.y[(size_t)my_b * p.ldy + r0 + row] = tot;
+                else
+                    red[((size_t)row * G + seg) * NB + my_b] = tot;
+            }
+        }
+    }
+    if (G > 1) {
+        named_sync(2, CA * 32);
+        for (int i = warp * 32 + lane; i < nrows * NB; i += CA * 32) {
+            const int row = i / NB, b = i % NB;
+            if (b >= p.nb_cols) continue;
+            float sum = red[((size_t)row * G) * NB + b];
+            for (int g2 = 1; g2 < G; ++g2) sum += red[((size_t)row * G + g2) * NB + b];
+            p.y[(size_t)b * p.ldy + r0 + row] = sum;
+        }
+    }
+}
+
+template <int NB>
+cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int nb_cols, float *y, int64_t ldy,
+                   int grid, cudaStream_t s) {
+    Params p{w, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
+    if (!plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * 144 + NB * col_bytes(k) + red_bytes<NB>(p);
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows_nb<NB>);
+        if (e != cudaSuccess) return e;
+        if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(gemv_rows_nb<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - kStatic);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaMemPool_t pool = scratch_pool();
+    if (!pool) return cudaErrorMemoryAllocation;
+    void *img = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&img, (size_t)NB * col_bytes(k), pool, s);
+    if (e != cudaSuccess) return e;
+    p.x_img = static_cast<const uint8_t *>(img);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3((unsigned)((k / 256 + 7) / 8), NB);
+    pcfg.blockDim = dim3(256);
+    pcfg.stream = s;
+    pcfg.attrs = attr;
+    pcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pcfg, prep_x_nb<NB>, x, (int)k, nb_cols, static_cast<uint8_t *>(img));
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_rows_nb<NB>, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    const cudaError_t f = cudaFreeAsync(img, s);
+    return e != cudaSuccess ? e : f;
+}
+
+// Whether this kernel runs Q4_K (k, n_out) at `batch` columns.  It is used at
+// batch 2 for long rows (k >= 8192), where it beats the chunked kernel
+// (4096x14336: 14.0 vs 18.6 us); at k = 4096 the chunked kernel is faster,
+// and at batch 3-4 (NB = 4) the chunked or tensor-core kernels are.
+inline bool takes(int64_t k, int64_t n_out, int batch) {
+    Params p{};
+    const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
+    const int grid = (int)(n_out < grid_est ? n_out : grid_est);
+    return batch == 2 && k >= 8192 && plan<2>(k, n_out, grid, p);
+}
+}  // namespace rowsnb
+
 }  // namespace
 
 unsigned stream_wait_timeouts(bool reset) {
@@ -872,6 +1293,8 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
         return rowk::launch<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch());
     if (batch == 1 && fmt == PQ_Q6_K && rowk::takes(fmt, k, n_out))
         return rowk::launch<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch());
+    if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
+        return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);
     switch (batch) {
     case 1: return launch_nb<1>(p, grid, s);
     case 2: return launch_nb<2>(p, grid, s);

@@ -646,27 +646,6 @@ EncodeTiled encode_fn() {
     return fn;
 }
 
-// Stream-ordered scratch for the x image: a library-owned memory pool per
-// device that keeps freed memory for reuse.
-cudaMemPool_t scratch_pool() {
-    static cudaMemPool_t pools[64] = {};
-    static std::once_flag once[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::call_once(once[dev], [dev] {
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaMemPool_t pool = nullptr;
-        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
-            uint64_t keep = ~0ull;
-            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-            pools[dev] = pool;
-        }
-    });
-    return pools[dev];
-}
 
 // CTAs for a call: one per SM, at most one per work item.
 int tc_grid(int64_t n_out, int64_t k, const DeviceInfo &dev) {

@@ -1,8 +1,8 @@
 // C ABI of the library: argument checks, kernel choice, launches.
 //
 // Every check runs on the host before any launch, so a rejected call never
-// touches the GPU.  Nothing is allocated here; the only state is a
-// per-device record of properties, filled once per device.
+// touches the GPU.  The state kept here: a per-device record of properties,
+// filled once per device, and a per-device scratch memory pool.
 
 #include <atomic>
 #include <cstdint>
@@ -48,6 +48,29 @@ const DeviceInfo *device_info() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::call_once(g_once[dev], fill_info, dev);
     return g_ok[dev] ? &g_info[dev] : nullptr;
+}
+
+// Stream-ordered scratch for kernels that need some (x images, partial
+// sums): a library-owned memory pool per device that keeps freed memory for
+// reuse.
+cudaMemPool_t scratch_pool() {
+    static cudaMemPool_t pools[64] = {};
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::call_once(once[dev], [dev] {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+            uint64_t keep = ~0ull;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            pools[dev] = pool;
+        }
+    });
+    return pools[dev];
 }
 
 }  // namespace pqk
@@ -103,9 +126,13 @@ int check_gemv(int fmt, const void *w, int n_out, int k, const float *x, int bat
     return PQ_OK;
 }
 
-// Kernel for one chunk of `nb` batch columns.
+// Kernel for one chunk of `nb` batch columns.  The tensor-core kernel costs
+// about the same at any batch up to 16, so it also takes batch 3-4 where the
+// CUDA-core kernels are slower: long rows (k >= 8192), and at batch 4 large
+// matrices (>= 2^25 weights); measured on 4096x14336, 14336x4096, 28672x4096.
 int choose(int fmt, int64_t n_out, int64_t k, int nb) {
-    if (nb >= 5 && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
+    const bool tc_pays = nb >= 5 || (nb >= 3 && k >= 8192) || (nb == 4 && n_out * k >= (INT64_C(1) << 25));
+    if (tc_pays && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
     if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
     return PQ_KERNEL_GENERIC;
 }

@@ -24,6 +24,10 @@ struct DeviceInfo {
 // Cached per-device properties of the current device; nullptr on failure.
 const DeviceInfo *device_info();
 
+// Library-owned stream-ordered memory pool of the current device (scratch
+// memory taken with cudaMallocFromPoolAsync, kept for reuse); null on failure.
+cudaMemPool_t scratch_pool();
+
 // Launchers: arguments already validated; return cudaError_t of the launch.
 cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, float *out,
                            cudaStream_t s);
