@@ -139,6 +139,53 @@ def dist_init():
     return world, rank, local
 
 
+# The workloads of the method, each timed alone (config name, fmt, n_out, k, batch).
+CONFIGS = [
+    ("Q8_0 896x896, batch 1", "q8_0", 896, 896, 1),
+    ("Q4_K 4096x4096, batch 1", "q4_k", 4096, 4096, 1),
+    ("Q6_K LM head 128256x4096, batch 1", "q6_k", 128256, 4096, 1),
+] + [(f"Q4_K {n}x{k}, batch {b}", "q4_k", n, k, b)
+     for (n, k) in ((14336, 4096), (4096, 14336)) for b in (1, 2, 4, 8, 16)]
+
+
+def per_config(pq, dev, peak, l2_bytes):
+    """Each workload alone: pq_gemv launched back to back in a CUDA graph, the
+    weights rotating over copies that together exceed twice the L2, CUDA
+    events around one replay.  Returns one record per workload."""
+    import torch
+    out = []
+    for name, fmt, n, k, b in CONFIGS:
+        nbytes = synth.weight_bytes(fmt, n, k)
+        copies = max(2, -(-2 * l2_bytes // nbytes))
+        base = torch.from_numpy(synth.random_records(fmt, n, k, seed=11)).to(dev)
+        W = [base] + [base.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(synth.normal_x(b, k, seed=12)).to(dev)
+        y = torch.empty(b * n, dtype=torch.float32, device=dev)
+        launches = max(20, min(400, int(4e8 // nbytes)))
+        for i in range(3):
+            pq.pq_gemv(fmt, W[i % copies], n, k, x, b, y)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cur = torch.cuda.current_stream()
+            for i in range(launches):
+                pq.pq_gemv(fmt, W[i % copies], n, k, x, b, y, cur)
+        g.replay()
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(e) * 1e3 / launches
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out.append({"workload": name, "kernel": int(pq.pq_gemv_choice(fmt, n, k, b)), "us": round(us, 3),
+                    "weight_GBs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4)})
+        del W, base, g
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -258,6 +305,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = timed(args.steps, e2e=True)
     clocks.stop()
+    peak, peak_src = measured_hbm_peak()
+    configs = per_config(pq, dev, peak, torch.cuda.get_device_properties(local).L2_cache_size) \
+        if not args.no_per_config else None
 
     if world > 1:
         t = torch.tensor([ms, e2e_ms, dom_ms], dtype=torch.float64, device=dev)
@@ -267,7 +317,6 @@ def run_ours(args):
     nbytes = set_bytes()
     gbs = nbytes * args.steps * world / (ms * 1e-3) / 1e9
     e2e_gbs = nbytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
-    peak, peak_src = measured_hbm_peak()
     dom_bytes = synth.weight_bytes(FMT, *[(n, k) for name, n, k in SET if name == DOMINANT][0])
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else float("nan")
     src_hash = kernel_source_hash()
@@ -309,6 +358,12 @@ def run_ours(args):
                      "kernel_source": src_hash},
         "clocks": clocks.summary(),
     }
+    if configs is not None:
+        result["per_config"] = {"method": "each workload alone, pq_gemv back to back in one CUDA graph, "
+                                          "weights rotating over copies larger than twice the L2, "
+                                          "CUDA events; kernel = pq_gemv_choice id (0 generic, "
+                                          "1 stream, 2 tensor core)",
+                                "peak_GBs": peak, "results": configs}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -439,6 +494,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip timing each workload alone")
     ap.add_argument("--shape", default=None, help="fmt:NxK[:batch]: launch one shape only")
     ap.add_argument("--launches", type=int, default=6)
     ap.add_argument("--kernel", default="auto")

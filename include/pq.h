@@ -103,9 +103,12 @@ const char *pq_strerror(int status);
  * (fmt, batch, n_out, k); pq_gemv_kernel runs a named one instead:
  *   PQ_KERNEL_AUTO     the same choice pq_gemv makes
  *   PQ_KERNEL_GENERIC  warp-per-row kernel, any format / shape / batch
- *   PQ_KERNEL_STREAM   bulk-copy ring + integer dot products (Q4_K, Q8_0,
- *                      Q6_K, I8_ROW; batch <= 4)
- *   PQ_KERNEL_TC       tcgen05 tensor-core kernel (Q4_K, batch >= 2)
+ *   PQ_KERNEL_STREAM   bulk-copy ring + integer dot products (Q4_K at
+ *                      batch 1-4, Q6_K at batch 1)
+ *   PQ_KERNEL_TC       tcgen05 tensor-core kernel (Q4_K, batch 1-16, k a
+ *                      multiple of 256 up to 65536; pq_gemv chooses it at
+ *                      batch >= 5, and at batch 3-4 for long rows or large
+ *                      matrices)
  * A kernel that cannot run the given case returns PQ_ERR_KERNEL without
  * launching anything.
  */
