@@ -139,6 +139,24 @@ def dist_init():
     return world, rank, local
 
 
+def max_over_ranks(values, world, device=None):
+    """Each value's maximum over all ranks (one all-reduce; the identity on
+    one rank).  Times are taken as the slowest rank's."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(bytes_per_step, steps, world, ms):
+    """Whole-job throughput in GB/s: every rank processed `steps` steps of
+    `bytes_per_step` in `ms` milliseconds (the slowest rank's time)."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 # The workloads of the method, each timed alone (config name, fmt, n_out, k, batch).
 CONFIGS = [
     ("Q8_0 896x896, batch 1", "q8_0", 896, 896, 1),
@@ -309,14 +327,11 @@ def run_ours(args):
     configs = per_config(pq, dev, peak, torch.cuda.get_device_properties(local).L2_cache_size) \
         if not args.no_per_config else None
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms, dom_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, dom_ms = t.tolist()
+    ms, e2e_ms, dom_ms = max_over_ranks([ms, e2e_ms, dom_ms], world, dev)
 
     nbytes = set_bytes()
-    gbs = nbytes * args.steps * world / (ms * 1e-3) / 1e9
-    e2e_gbs = nbytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
+    gbs = whole_job_rate(nbytes, args.steps, world, ms)
+    e2e_gbs = whole_job_rate(nbytes, args.steps, world, e2e_ms)
     dom_bytes = synth.weight_bytes(FMT, *[(n, k) for name, n, k in SET if name == DOMINANT][0])
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else float("nan")
     src_hash = kernel_source_hash()
