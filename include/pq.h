@@ -158,6 +158,18 @@ int pq_set_weight_prefetch(int enable);
 int pq_wait_timeouts(int reset);
 
 /*
+ * Self-test of that failure detection (no counterpart on the pages: the
+ * pages run no GPU kernels of this kind).  Launches one thread on `stream`
+ * that waits on a barrier nothing completes, bounded by limit_us
+ * microseconds (1 .. 1,000,000); the wait runs out, is counted in
+ * pq_wait_timeouts, and the kernel returns normally, leaving the context
+ * usable.  Synchronises `stream`.  Returns 1 when the wait ran out as
+ * designed, 0 if it completed (never expected), PQ_ERR_ARG for a limit out of
+ * range, PQ_ERR_DEVICE, or PQ_ERR_LAUNCH.
+ */
+int pq_selftest_wait_timeout(unsigned limit_us, struct CUstream_st *stream);
+
+/*
  * Mat-vec that allocates no memory at all (no counterpart on the pages: an
  * addition of this library for callers that cannot allocate).
  *

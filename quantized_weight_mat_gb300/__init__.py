@@ -25,7 +25,7 @@ LIB_PATH = os.environ.get("PQ_LIB_PATH") or os.path.join(
     os.path.dirname(os.path.abspath(__file__)), "libpq.so")
 EXPORTS = ("pq_gemv", "pq_dequant", "pq_weight_bytes", "pq_strerror",
            "pq_gemv_kernel", "pq_gemv_choice", "pq_gemv_launches", "pq_wait_timeouts",
-           "pq_set_weight_prefetch", "pq_gemv_noalloc")
+           "pq_set_weight_prefetch", "pq_gemv_noalloc", "pq_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.pq_gemv_launches.restype = i32
             L.pq_wait_timeouts.argtypes = [i32]
             L.pq_wait_timeouts.restype = i32
+            L.pq_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+            L.pq_selftest_wait_timeout.restype = i32
             L.pq_gemv_noalloc.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
             L.pq_gemv_noalloc.restype = i32
             L.pq_set_weight_prefetch.argtypes = [i32]
@@ -151,3 +153,8 @@ def pq_gemv_noalloc(fmt, w_blocks, n_out: int, k: int, x, batch: int, y, stream=
     if check and st:
         raise PQError(st, "pq_gemv_noalloc")
     return st
+
+
+def pq_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    """Bounded-wait self-test (see include/pq.h): 1 when the wait ran out as designed."""
+    return int(lib().pq_selftest_wait_timeout(int(limit_us), _stream(stream)))

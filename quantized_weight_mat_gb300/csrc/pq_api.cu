@@ -134,17 +134,26 @@ int choose(int fmt, int64_t n_out, int64_t k, int nb) {
     const bool tc_pays = nb >= 5 || (nb >= 3 && k >= 8192) || (nb == 4 && n_out * k >= (INT64_C(1) << 25));
     if (tc_pays && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
     if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
+    // Q6_K has a streaming kernel for one column only; one launch per column
+    // still beats the generic kernel (LM head 128256x4096: 2 x 65 us against
+    // 301 us at batch 2)
+    if (fmt == PQ_Q6_K && stream_supported(fmt, n_out, k, 1)) return PQ_KERNEL_STREAM;
     return PQ_KERNEL_GENERIC;
 }
 
 // Chunking of the batch: chunks of up to 16 columns; a chunk that no
-// tensor-core kernel takes is split further into chunks of up to 4.
+// tensor-core kernel takes is split further into chunks of up to 4, and into
+// single columns for a streaming kernel that only takes one (Q6_K).
 template <class F>
 int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &&f) {
     for (int b0 = 0; b0 < batch;) {
         int nb = batch - b0 < 16 ? batch - b0 : 16;
         int kern = forced >= 0 ? forced : choose(fmt, n_out, k, nb);
         if (kern != PQ_KERNEL_TC && nb > 4) nb = 4;
+        // a streaming kernel that takes one column at a time runs column by column
+        if (kern == PQ_KERNEL_STREAM && nb > 1 && !stream_supported(fmt, n_out, k, nb) &&
+            stream_supported(fmt, n_out, k, 1))
+            nb = 1;
         if (kern == PQ_KERNEL_STREAM && !stream_supported(fmt, n_out, k, nb)) return PQ_ERR_KERNEL;
         if (kern == PQ_KERNEL_TC && !tc_supported(fmt, n_out, k, nb)) return PQ_ERR_KERNEL;
         int st = f(kern, b0, nb);
@@ -239,8 +248,18 @@ int pq_set_weight_prefetch(int enable) {
 int pq_wait_timeouts(int reset) {
     const DeviceInfo *dev = nullptr;
     if (check_device(&dev)) return PQ_ERR_DEVICE;
-    const unsigned n = stream_wait_timeouts(reset != 0) + tc_wait_timeouts(reset != 0);
+    const unsigned n =
+        stream_wait_timeouts(reset != 0) + tc_wait_timeouts(reset != 0) + selftest_wait_timeouts(reset != 0);
     return n > 0x7fffffffu ? 0x7fffffff : (int)n;
+}
+
+// Failure-detection self-test (see pq.h).
+int pq_selftest_wait_timeout(unsigned limit_us, struct CUstream_st *stream) {
+    if (limit_us < 1 || limit_us > 1000000) return PQ_ERR_ARG;
+    const DeviceInfo *dev = nullptr;
+    if (check_device(&dev)) return PQ_ERR_DEVICE;
+    const int r = run_selftest_wait(1000ull * limit_us, stream);
+    return r < 0 ? PQ_ERR_LAUNCH : r;
 }
 
 // Allocation-free mat-vec (tensor-core kernel with fixed scratch).  Checks as

@@ -62,5 +62,9 @@ int weight_prefetch();
 // Bounded waits that ran out in each kernel file since the last reset.
 unsigned stream_wait_timeouts(bool reset);
 unsigned tc_wait_timeouts(bool reset);
+unsigned selftest_wait_timeouts(bool reset);
+// Bounded-wait self-test: 1 if the wait ran out and the kernel returned, 0 if
+// it completed, -1 on a CUDA error.  Synchronises `s`.
+int run_selftest_wait(unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace pqk

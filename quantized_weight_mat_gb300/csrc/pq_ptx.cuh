@@ -57,17 +57,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  On timeout records it in g_wait_timeouts and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// limit_ns.  On timeout records it in g_wait_timeouts and returns false.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicAdd(&g_wait_timeouts, 1u);
             return false;
         }
     }
     return true;
+}
+
+// The kernels' wait: bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Bulk copy global -> this CTA's shared memory, completing on `bar` by bytes.

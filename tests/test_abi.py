@@ -101,7 +101,9 @@ def test_kernel_choice_table():
             c = pq.pq_gemv_choice(fmt, 4096, k, b)
             assert c in (pq.KERNEL_GENERIC, pq.KERNEL_STREAM, pq.KERNEL_TC)
             n = pq.pq_gemv_launches(fmt, 4096, k, b)
-            assert (b + 15) // 16 <= n <= (b + 3) // 4
+            # slices of up to 16 (tensor core) or 4 columns, or one column at a
+            # time for a one-column streaming kernel (Q6_K)
+            assert (b + 15) // 16 <= n <= (b if fmt == "q6_k" else (b + 3) // 4)
 
 
 def test_bad_kernel_id_rejected():
@@ -118,3 +120,9 @@ def test_noalloc_argument_checks():
     import torch
     if not torch.cuda.is_available():
         assert L.pq_gemv_noalloc(1, A16, 4, 16384, A16 * 2, 1, A16 * 3, 0) == pq.PQ_ERR_DEVICE
+
+
+def test_selftest_limit_is_checked_before_any_launch():
+    L = pq.lib()
+    assert L.pq_selftest_wait_timeout(0, 0) == pq.PQ_ERR_ARG
+    assert L.pq_selftest_wait_timeout(1000001, 0) == pq.PQ_ERR_ARG
