@@ -93,23 +93,32 @@ int plan_stages(int64_t k, int nb_cols) {
 // Consecutive lanes read consecutive 16-byte groups: no bank conflicts.
 __device__ __forceinline__ void prep_x_vals(const float (&v)[8], uint8_t *img, uint8_t *meta,
                                             int q, int S, int lane) {
-    float amax = 0.f;
+    // block maximum of |x|: the bit patterns of non-negative floats order like
+    // their values, so one integer warp reduction gives it
+    uint32_t mb = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    for (int i = 0; i < 8; ++i) mb = max(mb, __float_as_uint(v[i]) & 0x7fffffffu);
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    const float amax = __uint_as_float(mb);
     const float s = amax * (1.0f / 127.0f);
-    const float inv = amax > 0.f ? 127.0f / amax : 0.f;
-    const float inv2 = amax > 0.f ? (254.0f * 127.0f) / amax : 0.f;
+    // one reciprocal for both scales (a block whose values are all below 1e-30
+    // contributes nothing measurable and gets zero limbs)
+    const float rcp = amax > 1e-30f ? __frcp_rn(amax) : 0.f;
+    const float inv = 127.0f * rcp, inv2 = (254.0f * 127.0f) * rcp;
+    // round to nearest even by adding 1.5 * 2^23 (exact for |t| < 2^22): the
+    // integer is the low bits of the sum; |x*inv| <= 127 by construction, the
+    // remainder's limb is clamped
+    constexpr float kMagic = 12582912.0f;
+    constexpr int kMagicBits = 0x4B400000;
     uint32_t h[2] = {0, 0}, l[2] = {0, 0};
     int xs = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        int hi = __float2int_rn(v[i] * inv);
-        hi = max(-127, min(127, hi));
-        const float r = fmaf(-s, (float)hi, v[i]);
-        int lo = __float2int_rn(r * inv2);
-        lo = max(-127, min(127, lo));
+        const float th = fmaf(v[i], inv, kMagic);
+        const int hi = __float_as_int(th) - kMagicBits;
+        const float r = fmaf(-s, th - kMagic, v[i]);
+        const float tl = fminf(fmaxf(r * inv2, -127.0f), 127.0f) + kMagic;
+        const int lo = __float_as_int(tl) - kMagicBits;
         xs += 254 * hi + lo;
         h[i >> 2] |= (uint32_t)(hi & 0xff) << (8 * (i & 3));
         l[i >> 2] |= (uint32_t)(lo & 0xff) << (8 * (i & 3));
