@@ -2,10 +2,10 @@
 //
 // The operation is the ember pull request's fused "dequantize+mat-vec that
 // never expands weights back to f32" (quant.rs description) for GGUF-style
-// Q4_K super-blocks (the K-family the PESTI README dequantizes, "What This
-// Is").  At batch 1 it moves 0.5625 B per weight and does 2 flops per
-// weight: it is bound by HBM bandwidth, and the design goal is to keep HBM
-// busy while spending as few issue slots per weight as possible.
+// Q4_K and Q6_K super-blocks (the K-family the PESTI README dequantizes,
+// "What This Is").  At batch 1 it moves 0.5625 B (Q4_K) per weight and does 2
+// flops per weight: it is bound by HBM bandwidth, and the design goal is to
+// keep HBM busy while spending as few issue slots per weight as possible.
 //
 // Common structure (one persistent CTA per SM, each owning a contiguous,
 // balanced range of rows):
@@ -14,23 +14,27 @@
 //     in bytes on an mbarrier per stage, slots handed back on a second one);
 //   * x is converted once per CTA into two int8 limbs per element with one
 //     scale per 256 values: x ~= u * (254*xh + xl), |error| <= max|x|/64516,
-//     so each 32-weight sub-block's dot product sum_i q_i*x_i becomes dp4a
-//     integer dot products (exact);
-//   * per super-block the 6-bit scales and mins are applied in 32-bit
-//     integers (H = sum_j sc_j*dot_j over both limbs, M = sum_j m_j*sum X_i),
-//     then a few f32 operations: y += u*(d*(254*H + L) - dmin*M);
+//     so each sub-block's dot product sum_i q_i*x_i becomes dp4a integer dot
+//     products (exact);
+//   * per super-block the scales and mins are applied in 32-bit integers
+//     (H = sum_j sc_j*dot_j over both limbs, M = sum_j m_j*sum X_i), then a
+//     few f32 operations: y += u*(d*(254*H + L) - dmin*M) for Q4_K;
 //   * partial sums are reduced with warp shuffles (and, for long rows split
 //     over several warps, in shared memory in a fixed order).
 // No atomics, fixed summation order: results are deterministic.
 //
-// Two kernels share that structure:
-//   gemv_rows_q4_k     batch 1: a stage is a run of whole rows fetched with
-//                      ONE contiguous bulk copy; each lane owns 128 weights
-//                      (half a super-block) of a fixed k range and keeps that
-//                      range of x in registers for the whole kernel;
-//   gemv_stream_q4_k   batch 1..4, any k: a stage is 32 rows x 8 super-blocks
-//                      (one copy per row segment), x read from the shared
-//                      image per stage and reused across a warp's rows.
+// Three kernels share that structure:
+//   rowk::gemv_rows<Q4K|Q6K>  batch 1: a stage is a run of whole rows fetched
+//                      with ONE contiguous bulk copy; each lane owns 128
+//                      weights (half a super-block) of a fixed k range and
+//                      keeps that range of x in registers for the whole kernel;
+//   rowsnb::gemv_rows_nb<2>   batch 2, long rows: the same with a lane owning
+//                      64 weights, x for both columns in registers, x made
+//                      once per call by a small kernel;
+//   gemv_stream_q4_k<NB>      batch 1..4, any k: a stage is 32 rows x 8
+//                      super-blocks (one copy per row segment), x read from
+//                      the shared image per stage and reused across a warp's
+//                      rows.
 //
 // Every mbarrier wait is bounded in time (pq_ptx.cuh); on timeout the
 // kernel records it and the warp stops.
