@@ -51,9 +51,9 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel from one ncu capture, keyed by the sha256 of the kernel source (code
-# only, comments removed) it was
-# taken on; any edit of that source makes the figure stale (reported as null).
+# kernel from one ncu capture, keyed by the sha256 of the kernel source it was
+# taken on (code only, comments removed); any edit of that code makes the
+# figure stale (reported as null).
 NCU_TRAFFIC = {"c187c47a1ab5d394": 66_169_600}
 
 
