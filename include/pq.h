@@ -25,14 +25,20 @@
  * W is n_out rows; row r holds k/QK consecutive blocks (QK = 32, 256, 256, 1),
  * rows contiguous, no padding.
  *
- * Ownership and threading: the caller allocates and owns every buffer (device
- * memory, e.g. from cudaMalloc or a framework allocator).  The library
- * allocates nothing and keeps no state beyond a per-device record of the
- * device's properties, so calls are reentrant and may run concurrently on
- * different streams.  Calls are asynchronous on `stream` (NULL = legacy
- * default stream); a fault during execution surfaces at the caller's next
- * synchronization.  All argument checks run on the host before any launch,
- * so a rejected call launches nothing.
+ * Ownership and threading: the caller allocates and owns every buffer it
+ * passes (device memory, e.g. from cudaMalloc or a framework allocator).  The
+ * library keeps a per-device record of the device's properties and one
+ * library-owned stream-ordered memory pool per device.  pq_gemv draws a small
+ * per-call buffer from that pool, allocated and freed on `stream`, for the
+ * tensor-core kernel (x image and split-K partial sums, under 8 MB) and
+ * for the batch-2 long-row kernel (x image, 4.5 * k bytes); every
+ * other path allocates nothing.  The pool keeps freed memory for reuse, so
+ * after the first call of a shape no call reaches the device allocator.  Calls
+ * are reentrant and may run concurrently on different streams.  Calls are
+ * asynchronous on `stream` (NULL = legacy default stream); a fault during
+ * execution surfaces at the caller's next synchronization.  All argument
+ * checks run on the host before any launch, so a rejected call launches
+ * nothing.  pq_gemv_noalloc (below) runs the tensor-core path with no pool.
  */
 #ifndef PQ_H
 #define PQ_H
@@ -60,7 +66,7 @@ typedef enum {
 #define PQ_ERR_ALIGN (-4)    /* w_blocks, x or out not 16-byte aligned, or y not 4-byte aligned */
 #define PQ_ERR_SIZE (-5)     /* byte or element counts overflow 64-bit arithmetic */
 #define PQ_ERR_DEVICE (-6)   /* current device is not compute capability 10.3 (sm_103) */
-#define PQ_ERR_LAUNCH (-7)   /* the CUDA launch itself failed (cudaGetLastError after launch) */
+#define PQ_ERR_LAUNCH (-7)   /* a launch, or the pool allocation before it, failed */
 #define PQ_ERR_KERNEL (-8)   /* unknown kernel id passed to pq_gemv_kernel */
 
 /*
