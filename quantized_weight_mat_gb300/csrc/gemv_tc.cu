@@ -22,7 +22,7 @@
 // in CTA order and writes y, so the result does not depend on timing.
 //
 // Pipeline inside a CTA:
-//   warp 12 producer: a 2-D TMA load (tensor map over W as [n_out][row bytes])
+//   warp 20 producer: a 2-D TMA load (tensor map over W as [n_out][row bytes])
 //           brings one 128-row x 144-byte super-block column per stage, and a
 //           1-D bulk copy brings that super-block's x tile;
 //   warps 0-15 decoders: thread (c, r) turns the 64 weights of chunk c of

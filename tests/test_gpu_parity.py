@@ -206,28 +206,31 @@ def test_workload_dequant_output_head_sampled():
         assert np.array_equal(o[r].cpu().numpy().view(np.uint32), ref.view(np.uint32)), r
 
 
+@pytest.mark.parametrize("batch", [1, 8])
 @pytest.mark.parametrize("prefetch", [False, True])
-def test_chained_calls_respect_stream_order(prefetch):
+def test_chained_calls_respect_stream_order(prefetch, batch):
     # y1 = W1 x, y2 = W2 y1, y3 = W3 y2 issued back to back on one stream: each
     # call must read its predecessor's finished output, also when its kernel is
-    # scheduled while the predecessor is still running
+    # scheduled while the predecessor is still running.  At batch 8 the three
+    # shapes run the tensor-core kernel with whole tiles (14336 x 4096) and
+    # split-K with the finishing kernel (4096 x 14336, 4096 x 4096).
     import torch
-    n, k = 4096, 4096
-    ws = [weights("q4_k", n, k, "quantized", 60 + j) for j in range(3)]
+    shapes = [(14336, 4096), (4096, 14336), (4096, 4096)]
+    ws = [weights("q4_k", n, k, "quantized", 60 + j) for j, (n, k) in enumerate(shapes)]
     wd = [dev(w) for w in ws]
-    x = x_for(1, k, 63)
-    ys = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3)]
+    x = x_for(batch, shapes[0][1], 63)
+    ys = [torch.empty(batch * n, dtype=torch.float32, device="cuda") for n, _ in shapes]
     old = pq.pq_set_weight_prefetch(prefetch)
     try:
         for rep in range(3):
             cur = dev(x)
-            for j in range(3):
-                pq.pq_gemv("q4_k", wd[j], n, k, cur, 1, ys[j])
+            for j, (n, k) in enumerate(shapes):
+                pq.pq_gemv("q4_k", wd[j], n, k, cur, batch, ys[j])
                 cur = ys[j]
             torch.cuda.synchronize()
             prev = x
-            for j in range(3):
-                got = ys[j].cpu().numpy()[None, :]
+            for j, (n, k) in enumerate(shapes):
+                got = ys[j].cpu().numpy().reshape(batch, n)
                 ref = oracle.gemv("q4_k", ws[j], n, k, prev)
                 ok, err, bound = tolerance_ok(got, ref)
                 assert ok, (rep, j, err, bound)
@@ -236,25 +239,26 @@ def test_chained_calls_respect_stream_order(prefetch):
         pq.pq_set_weight_prefetch(bool(old))
 
 
-def test_weights_written_by_the_preceding_kernel():
+@pytest.mark.parametrize("batch", [1, 8])
+def test_weights_written_by_the_preceding_kernel(batch):
     # with prefetch off (the default), a kernel that writes the weight buffer
-    # right before pq_gemv must be fully visible to it
+    # right before pq_gemv must be fully visible to it (batch 8: tensor core)
     import torch
     n, k = 2048, 4096
     wa, wb = weights("q4_k", n, k, "random", 70), weights("q4_k", n, k, "random", 71)
     da, db = dev(wa), dev(wb)
     mask = torch.bitwise_xor(da, db)
     wbuf = da.clone()
-    x = x_for(1, k, 72)
+    x = x_for(batch, k, 72)
     xd = dev(x)
-    y = torch.empty(n, dtype=torch.float32, device="cuda")
+    y = torch.empty(batch * n, dtype=torch.float32, device="cuda")
     assert pq.pq_set_weight_prefetch(False) in (0, 1)
     for _ in range(3):
         torch.bitwise_xor(da, mask, out=wbuf)          # a kernel writes W = wb
-        pq.pq_gemv("q4_k", wbuf, n, k, xd, 1, y)
+        pq.pq_gemv("q4_k", wbuf, n, k, xd, batch, y)
         torch.bitwise_xor(db, mask, out=wbuf)          # and back to wa
         torch.cuda.synchronize()
-        ok, err, bound = tolerance_ok(y.cpu().numpy()[None, :], oracle.gemv("q4_k", wb, n, k, x))
+        ok, err, bound = tolerance_ok(y.cpu().numpy().reshape(batch, n), oracle.gemv("q4_k", wb, n, k, x))
         assert ok, (err, bound)
 
 
