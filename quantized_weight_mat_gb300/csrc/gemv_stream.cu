@@ -109,32 +109,37 @@ __device__ __forceinline__ void prep_x_vals(const float (&v)[8], uint8_t *img, u
     // contributes nothing measurable and gets zero limbs)
     const float rcp = amax > 1e-30f ? __frcp_rn(amax) : 0.f;
     const float inv = 127.0f * rcp, inv2 = (254.0f * 127.0f) * rcp;
-    // round to nearest even by adding 1.5 * 2^23 (exact for |t| < 2^22): the
-    // integer is the low bits of the sum; |x*inv| <= 127 by construction, the
-    // remainder's limb is clamped
+    // Round to nearest even by adding 1.5 * 2^23: for |t| < 2^22 the sum is
+    // exact and its bit pattern is 0x4B400000 + t, so the low byte of the bits
+    // is t as a two's-complement byte, ready to pack.  |x*inv| <= 127 by
+    // construction; the remainder r obeys |r| <= s/2 up to a relative 3e-5, so
+    // |r*inv2| <= 127.01 also rounds into [-127, 127].
     constexpr float kMagic = 12582912.0f;
-    constexpr int kMagicBits = 0x4B400000;
-    uint32_t h[2] = {0, 0}, l[2] = {0, 0};
-    int xs = 0;
+    uint32_t th[8], tl[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const float th = fmaf(v[i], inv, kMagic);
-        const int hi = __float_as_int(th) - kMagicBits;
-        const float r = fmaf(-s, th - kMagic, v[i]);
-        const float tl = fminf(fmaxf(r * inv2, -127.0f), 127.0f) + kMagic;
-        const int lo = __float_as_int(tl) - kMagicBits;
-        xs += 254 * hi + lo;
-        h[i >> 2] |= (uint32_t)(hi & 0xff) << (8 * (i & 3));
-        l[i >> 2] |= (uint32_t)(lo & 0xff) << (8 * (i & 3));
+        const float t = fmaf(v[i], inv, kMagic);
+        const float r = fmaf(-s, t - kMagic, v[i]);
+        th[i] = __float_as_uint(t);
+        tl[i] = __float_as_uint(fmaf(r, inv2, kMagic));
     }
+    // low bytes of four words -> one word, value i in byte i
+    auto pack4 = [](uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+        return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+    };
+    const uint32_t h0 = pack4(th[0], th[1], th[2], th[3]), h1 = pack4(th[4], th[5], th[6], th[7]);
+    const uint32_t l0 = pack4(tl[0], tl[1], tl[2], tl[3]), l1 = pack4(tl[4], tl[5], tl[6], tl[7]);
+    // sum of 254*xh + xl over the lane's eight values (signed bytes times one)
+    int xs = 254 * dp4a_ss(h0, 0x01010101u, dp4a_ss(h1, 0x01010101u, 0)) +
+             dp4a_ss(l0, 0x01010101u, dp4a_ss(l1, 0x01010101u, 0));
     xs += __shfl_xor_sync(0xffffffffu, xs, 1);
     xs += __shfl_xor_sync(0xffffffffu, xs, 2);
     const int j = lane >> 2, c = j >> 1, half = j & 1;
     const int slice = 4 * q + c;
     const int g = 2 * half + ((lane & 3) >> 1);
     const int off8 = 8 * (lane & 1);
-    *reinterpret_cast<uint2 *>(img + (g * S + slice) * 16 + off8) = make_uint2(h[0], h[1]);
-    *reinterpret_cast<uint2 *>(img + ((g + 4) * S + slice) * 16 + off8) = make_uint2(l[0], l[1]);
+    *reinterpret_cast<uint2 *>(img + (g * S + slice) * 16 + off8) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2 *>(img + ((g + 4) * S + slice) * 16 + off8) = make_uint2(l0, l1);
     if ((lane & 3) == 0) *reinterpret_cast<int *>(meta + slice * 16 + 4 * half) = xs;
     if ((lane & 7) == 0) *reinterpret_cast<float *>(meta + slice * 16 + 8) = s * (1.0f / 254.0f);
 }
