@@ -366,14 +366,12 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
     Params p = p0;
     p.nstages = plan_stages(p.k, NB);
     const int smem = p.nstages * STAGE + x_image_bytes(p.k, NB);
-    static bool configured = false;   // attribute is per function; setting it twice is harmless
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_stream_q4_k<NB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBudget - kStaticSmem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDeviceOnce configured;
+    const cudaError_t ce = configured.run([] {
+        return cudaFuncSetAttribute(gemv_stream_q4_k<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBudget - kStaticSmem);
+    });
+    if (ce != cudaSuccess) return ce;
     gemv_stream_q4_k<NB><<<grid, THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
@@ -830,16 +828,15 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
     if (!plan(k, n_out, grid, F::kBlockBytes, staged, p)) return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_stage_bytes(k, staged) +
                      x_image_bytes(k, 1) + red_bytes(p);
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;
+    const cudaError_t ce = configured.run([] {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows<F>);
         if (e != cudaSuccess) return e;
         if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
+    });
+    if (ce != cudaSuccess) return ce;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
@@ -1228,16 +1225,16 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, i
     Params p{w, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
     if (!plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * 144 + NB * col_bytes(k) + red_bytes<NB>(p);
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;
+    const cudaError_t ce = configured.run([] {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows_nb<NB>);
         if (e != cudaSuccess) return e;
         if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(gemv_rows_nb<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - kStatic);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaFuncSetAttribute(gemv_rows_nb<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBudget - kStatic);
+    });
+    if (ce != cudaSuccess) return ce;
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
     void *img = nullptr;

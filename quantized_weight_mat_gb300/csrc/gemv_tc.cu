@@ -693,12 +693,11 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    static bool configured = false;
-    if (!configured) {
-        e = cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDeviceOnce configured;
+    e = configured.run([] {
+        return cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
+    });
+    if (e != cudaSuccess) return e;
     const long long ntiles = (n_out + TM - 1) / TM;
     const long long total = ntiles * nb;
     TcParams p{img, y, partials, (long long)ldy, total, (int)n_out, (int)k, batch};

@@ -2,11 +2,33 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "pq.h"
 
 namespace pqk {
+
+constexpr int kMaxDeviceIds = 64;   // device ordinals served by the per-device state below
+
+// A set-up step that must run once on every device a kernel is launched on
+// (function attributes are per device): thread-safe, and a failed step keeps
+// its status, so every later call on that device returns it.
+class PerDeviceOnce {
+public:
+    template <class F> cudaError_t run(F step) {
+        int dev = 0;
+        const cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDeviceIds) return cudaErrorInvalidDevice;
+        std::call_once(flag_[dev], [&] { status_[dev] = step(); });
+        return status_[dev];
+    }
+
+private:
+    std::once_flag flag_[kMaxDeviceIds];
+    cudaError_t status_[kMaxDeviceIds] = {};
+};
 
 constexpr int kQK[4] = {32, 256, 256, 1};        // weights per block
 constexpr int kBlockBytes[4] = {34, 144, 210, 1}; // bytes per block
