@@ -14,6 +14,9 @@ Parity pins (checked by ``tests/test_oracle.py``):
   * Q8_0 / Q4_K / Q6_K / per-row int8 decode: hand-built blocks with closed
     forms, and single-bit flips that must change exactly the predicted
     weights;
+  * Q5_K / Q3_K / Q2_K decode: the same kinds of pins (closed forms on
+    hand-built blocks, every single-bit flip of random blocks against the
+    weights and amounts the layout predicts); no quantizer for them;
   * f64 mat-vec: integer-valued special cases against numpy's float64
     matmul, and exact rational sums on tiny shapes;
   * quantizers: brute-force best code on tiny matrices, re-quantization
@@ -28,8 +31,12 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K, I8_ROW = 0, 1, 2, 3
-FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "i8_row": I8_ROW}
+Q8_0, Q4_K, Q6_K, I8_ROW, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5, 6
+FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "i8_row": I8_ROW,
+           "q5_k": Q5_K, "q3_k": Q3_K, "q2_k": Q2_K}
+# weights and bytes per block of the block formats
+BLOCKS = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176),
+          Q3_K: (256, 110), Q2_K: (256, 84)}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pq_oracle.c")
@@ -63,11 +70,14 @@ def lib():
             L.pqo_double_to_half.restype = ctypes.c_uint16
             L.pqo_weight_bytes.argtypes = [i32, i64, i64]
             L.pqo_weight_bytes.restype = i64
-            for name in ("pqo_decode_q8_0", "pqo_decode_q4_k", "pqo_decode_q6_k"):
+            for name in ("pqo_decode_q8_0", "pqo_decode_q4_k", "pqo_decode_q6_k",
+                         "pqo_decode_q5_k", "pqo_decode_q3_k", "pqo_decode_q2_k"):
                 getattr(L, name).argtypes = [vp, vp]
                 getattr(L, name).restype = None
             L.pqo_q4_k_scale_min.argtypes = [vp, i32, vp, vp]
             L.pqo_q4_k_scale_min.restype = None
+            L.pqo_q3_k_scale.argtypes = [vp, i32]
+            L.pqo_q3_k_scale.restype = i32
             L.pqo_dequant.argtypes = [i32, vp, i64, i64, vp, i32]
             L.pqo_dequant.restype = i32
             L.pqo_gemv.argtypes = [i32, vp, i64, i64, vp, i64, vp, i32]
@@ -119,13 +129,13 @@ def double_to_half(v: float) -> int:
 def decode_block(fmt, blk: np.ndarray) -> np.ndarray:
     fmt = _fmt(fmt)
     blk = np.ascontiguousarray(blk, dtype=np.uint8)
-    n = {Q8_0: 32, Q4_K: 256, Q6_K: 256}[fmt]
-    need = {Q8_0: 34, Q4_K: 144, Q6_K: 210}[fmt]
+    n, need = BLOCKS[fmt]
     if blk.size != need:
         raise ValueError(f"block of format {fmt} has {need} bytes, got {blk.size}")
     out = np.empty(n, dtype=np.float32)
-    fn = {Q8_0: lib().pqo_decode_q8_0, Q4_K: lib().pqo_decode_q4_k,
-          Q6_K: lib().pqo_decode_q6_k}[fmt]
+    L = lib()
+    fn = {Q8_0: L.pqo_decode_q8_0, Q4_K: L.pqo_decode_q4_k, Q6_K: L.pqo_decode_q6_k,
+          Q5_K: L.pqo_decode_q5_k, Q3_K: L.pqo_decode_q3_k, Q2_K: L.pqo_decode_q2_k}[fmt]
     fn(_ptr(blk), _ptr(out))
     return out
 
@@ -135,6 +145,12 @@ def q4_k_scale_min(scales12: np.ndarray, j: int) -> tuple[int, int]:
     sc, m = ctypes.c_int(), ctypes.c_int()
     lib().pqo_q4_k_scale_min(_ptr(s), j, ctypes.addressof(sc), ctypes.addressof(m))
     return sc.value, m.value
+
+
+def q3_k_scale(scales12: np.ndarray, s: int) -> int:
+    """Signed 6-bit scale of group s (0..15) of a Q3_K super-block."""
+    t = np.ascontiguousarray(scales12, dtype=np.uint8)
+    return int(lib().pqo_q3_k_scale(_ptr(t), s))
 
 
 def _check_w(fmt, w: np.ndarray, n_out: int, k: int) -> np.ndarray:

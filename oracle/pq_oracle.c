@@ -19,7 +19,9 @@
  *
  * The pages never print a block's byte layout.  The layouts below are the
  * public GGUF layouts, read as a byte specification (sizes: Q8_0 34 B per
- * 32 weights, Q4_K 144 B per 256, Q6_K 210 B per 256).  Per-row int8 has
+ * 32 weights, Q4_K 144 B per 256, Q6_K 210 B per 256, and for the rest of
+ * the K family the PESTI README names, Q5_K 176 B, Q3_K 110 B, Q2_K 84 B
+ * per 256).  Per-row int8 has
  * no published layout; the one used here is: int8 q[n_out*k] row-major,
  * then, at the next 16-byte boundary, float scale[n_out].
  *
@@ -42,7 +44,7 @@
 #include <omp.h>
 #endif
 
-enum { PQO_Q8_0 = 0, PQO_Q4_K = 1, PQO_Q6_K = 2, PQO_I8_ROW = 3 };
+enum { PQO_Q8_0 = 0, PQO_Q4_K = 1, PQO_Q6_K = 2, PQO_I8_ROW = 3, PQO_Q5_K = 4, PQO_Q3_K = 5, PQO_Q2_K = 6 };
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16                                                   */
@@ -121,6 +123,9 @@ int pqo_block_weights(int fmt)
     case PQO_Q4_K: return 256;
     case PQO_Q6_K: return 256;
     case PQO_I8_ROW: return 1;
+    case PQO_Q5_K: return 256;
+    case PQO_Q3_K: return 256;
+    case PQO_Q2_K: return 256;
     }
     return -1;
 }
@@ -132,6 +137,9 @@ int pqo_block_bytes(int fmt)
     case PQO_Q4_K: return 144;
     case PQO_Q6_K: return 210;
     case PQO_I8_ROW: return 1;
+    case PQO_Q5_K: return 176;
+    case PQO_Q3_K: return 110;
+    case PQO_Q2_K: return 84;
     }
     return -1;
 }
@@ -244,6 +252,88 @@ void pqo_decode_q6_k(const uint8_t *blk, float *w)
     }
 }
 
+/* Q5_K (176 B): f16 d @0, f16 dmin @2, 12 scale bytes @4 (packed exactly as
+ * Q4_K's), qh[32] @16, qs[128] @48.  As in Q4_K, chunk c of 64 weights holds
+ * sub-block 2c (low nibbles of qs[32c..32c+31]) then sub-block 2c+1 (high
+ * nibbles of the same bytes); the fifth bit of weight 64c+32h+l (h = 0, 1,
+ * l < 32) is bit 2c+h of qh[l].  q = nibble + 16*bit, in 0..31.
+ * w = (d*sc_j)*q - dmin*m_j in f32: both products are exact, the subtraction
+ * rounds. */
+void pqo_decode_q5_k(const uint8_t *blk, float *w)
+{
+    float d = pqo_half_to_float(rd16(blk));
+    float dmin = pqo_half_to_float(rd16(blk + 2));
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    for (int i = 0; i < 256; ++i) {
+        int c = i / 64, p = i % 64;
+        int h = p / 32, l = p % 32;
+        int j = 2 * c + h;
+        int lo4 = h == 0 ? (qs[32 * c + l] & 0x0f) : (qs[32 * c + l] >> 4);
+        int q = lo4 + 16 * ((qh[l] >> j) & 1);
+        int sc, m;
+        pqo_q4_k_scale_min(scales, j, &sc, &m);
+        float dl = d * (float)sc;
+        float ml = dmin * (float)m;
+        w[i] = dl * (float)q - ml;
+    }
+}
+
+/* The signed 6-bit scale of group s (0..15, 16 weights each) of a Q3_K
+ * super-block, from the 12 packed bytes t[0..11]: the low four bits are the
+ * low nibble of t[s] (s < 8) or the high nibble of t[s-8] (s >= 8); the top two
+ * bits are bits 2*(s/4), 2*(s/4)+1 of t[8 + s%4]; the stored value is offset
+ * by 32. */
+int pqo_q3_k_scale(const uint8_t *t, int s)
+{
+    int lo4 = s < 8 ? (t[s] & 0x0f) : (t[s - 8] >> 4);
+    int hi2 = (t[8 + s % 4] >> (2 * (s / 4))) & 3;
+    return (lo4 | (hi2 << 4)) - 32;
+}
+
+/* Q3_K (110 B): hmask[32] @0, qs[64] @32, 12 scale bytes @96, f16 d @108.
+ * Two halves of 128 weights; in half n, weight 128n+32j+l (j = 0..3, l < 32)
+ * takes bits 2j, 2j+1 of qs[32n+l] as a 2-bit code and bit 4n+j of hmask[l]
+ * as its high bit: value = code - 4 when that bit is clear, code when set
+ * (range -4..3).  Weight i uses scale group i/16.  w = (d*sc)*value, exact in
+ * f32. */
+void pqo_decode_q3_k(const uint8_t *blk, float *w)
+{
+    const uint8_t *hmask = blk, *qs = blk + 32, *scales = blk + 96;
+    float d = pqo_half_to_float(rd16(blk + 108));
+    for (int i = 0; i < 256; ++i) {
+        int n = i / 128, r = i % 128;
+        int j = r / 32, l = r % 32;
+        int code = (qs[32 * n + l] >> (2 * j)) & 3;
+        int high = (hmask[l] >> (4 * n + j)) & 1;
+        int value = code - (high ? 0 : 4);
+        float ds = d * (float)pqo_q3_k_scale(scales, i / 16);
+        w[i] = ds * (float)value;
+    }
+}
+
+/* Q2_K (84 B): scales[16] @0 (low nibble: scale, high nibble: min, one byte
+ * per group of 16 weights), qs[64] @16, f16 d @80, f16 dmin @82.  Weight
+ * 128n+32j+l takes bits 2j, 2j+1 of qs[32n+l] (code 0..3) and group i/16.
+ * w = (d*sc)*code - dmin*m in f32: both products exact, the subtraction
+ * rounds. */
+void pqo_decode_q2_k(const uint8_t *blk, float *w)
+{
+    const uint8_t *scales = blk, *qs = blk + 16;
+    float d = pqo_half_to_float(rd16(blk + 80));
+    float dmin = pqo_half_to_float(rd16(blk + 82));
+    for (int i = 0; i < 256; ++i) {
+        int n = i / 128, r = i % 128;
+        int j = r / 32, l = r % 32;
+        int code = (qs[32 * n + l] >> (2 * j)) & 3;
+        int g = scales[i / 16];
+        float dl = d * (float)(g & 0x0f);
+        float ml = dmin * (float)(g >> 4);
+        w[i] = dl * (float)code - ml;
+    }
+}
+
 /* Decode row r of a whole matrix into w[0..k). */
 static void decode_row(int fmt, const uint8_t *W, int64_t n_out, int64_t k, int64_t r, float *w)
 {
@@ -261,12 +351,14 @@ static void decode_row(int fmt, const uint8_t *W, int64_t n_out, int64_t k, int6
     for (int64_t b = 0; b < nb; ++b) {
         const uint8_t *blk = row + b * bb;
         float *o = w + b * qk;
-        if (fmt == PQO_Q8_0)
-            pqo_decode_q8_0(blk, o);
-        else if (fmt == PQO_Q4_K)
-            pqo_decode_q4_k(blk, o);
-        else
-            pqo_decode_q6_k(blk, o);
+        switch (fmt) {
+        case PQO_Q8_0: pqo_decode_q8_0(blk, o); break;
+        case PQO_Q4_K: pqo_decode_q4_k(blk, o); break;
+        case PQO_Q6_K: pqo_decode_q6_k(blk, o); break;
+        case PQO_Q5_K: pqo_decode_q5_k(blk, o); break;
+        case PQO_Q3_K: pqo_decode_q3_k(blk, o); break;
+        default: pqo_decode_q2_k(blk, o); break;
+        }
     }
 }
 
@@ -485,6 +577,10 @@ int pqo_quantize(int fmt, const float *v, int64_t n_out, int64_t k, uint8_t *out
 {
     int64_t total = pqo_weight_bytes(fmt, n_out, k);
     if (total < 0)
+        return -1;
+    /* no quantizer for Q5_K / Q3_K / Q2_K: their test inputs are random
+     * records (every field bit pattern), which need none */
+    if (fmt == PQO_Q5_K || fmt == PQO_Q3_K || fmt == PQO_Q2_K)
         return -1;
     int nt = nthreads_or_default(nthreads);
     (void)nt;

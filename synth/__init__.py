@@ -19,14 +19,16 @@ Generators (numpy PCG64 via ``default_rng``):
   decoders see all of them.
 
 Byte offsets of the fp16 fields (the only layout facts used here):
-Q8_0 d @0; Q4_K d @0, dmin @2; Q6_K d @208.  Per-row int8: codes
-[n_out*k] then f32 scales at the next 16-byte boundary.
+Q8_0 d @0; Q4_K d @0, dmin @2; Q6_K d @208; Q5_K d @0, dmin @2; Q3_K d @108;
+Q2_K d @80, dmin @82.  Per-row int8: codes [n_out*k] then f32 scales at the
+next 16-byte boundary.
 """
 from __future__ import annotations
 
 import numpy as np
 
-BLOCK = {"q8_0": (32, 34), "q4_k": (256, 144), "q6_k": (256, 210), "i8_row": (1, 1)}
+BLOCK = {"q8_0": (32, 34), "q4_k": (256, 144), "q6_k": (256, 210), "i8_row": (1, 1),
+         "q5_k": (256, 176), "q3_k": (256, 110), "q2_k": (256, 84)}
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -97,4 +99,12 @@ def random_records(fmt: str, n_out: int, k: int, seed: int,
         rec[:, 2:4] = _f16_field(g, nblk, *dmin_range)
     elif fmt == "q6_k":
         rec[:, 208:210] = _f16_field(g, nblk, *d_range)
+    elif fmt == "q5_k":
+        rec[:, 0:2] = _f16_field(g, nblk, *d_range)
+        rec[:, 2:4] = _f16_field(g, nblk, *dmin_range)
+    elif fmt == "q3_k":
+        rec[:, 108:110] = _f16_field(g, nblk, *d_range)
+    elif fmt == "q2_k":
+        rec[:, 80:82] = _f16_field(g, nblk, *d_range)
+        rec[:, 82:84] = _f16_field(g, nblk, *dmin_range)
     return rec.reshape(-1)
