@@ -172,7 +172,9 @@ CONFIGS = [
     ("Q4_K 4096x4096, batch 1", "q4_k", 4096, 4096, 1),
     ("Q6_K LM head 128256x4096, batch 1", "q6_k", 128256, 4096, 1),
 ] + [(f"Q4_K {n}x{k}, batch {b}", "q4_k", n, k, b)
-     for (n, k) in ((14336, 4096), (4096, 14336)) for b in (1, 2, 4, 8, 16)]
+     for (n, k) in ((14336, 4096), (4096, 14336)) for b in (1, 2, 4, 8, 16)
+] + [(f"{f.upper()} 14336x4096, batch 1 (generic kernel)", f, 14336, 4096, 1)
+     for f in ("q5_k", "q3_k", "q2_k")]
 
 
 def per_config(pq, dev, peak, l2_bytes):

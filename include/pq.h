@@ -22,8 +22,17 @@
  *            int8 sc[16] (one per 16 weights), f16 d.   w = (d*sc)*(q-32)
  *   PQ_I8_ROW per-row symmetric int8: int8 q[n_out*k] row-major, then at the
  *            next 16-byte boundary f32 scale[n_out].      w = scale[r]*q
- * W is n_out rows; row r holds k/QK consecutive blocks (QK = 32, 256, 256, 1),
- * rows contiguous, no padding.
+ *   PQ_Q5_K  176 B per 256: f16 d, f16 dmin, 12 B of (scale, min) pairs packed
+ *            as in Q4_K, 32 B qh (fifth bits), 128 B of 4-bit q.
+ *            w = (d*sc)*q - dmin*m, q in 0..31
+ *   PQ_Q3_K  110 B per 256: 32 B hmask (high bits), 64 B of 2-bit q, 12 B of
+ *            16 packed signed 6-bit scales, f16 d.  w = (d*sc)*v, v in -4..3
+ *   PQ_Q2_K   84 B per 256: 16 B of 4-bit (scale, min) pairs, 64 B of 2-bit
+ *            q, f16 d, f16 dmin.                 w = (d*sc)*q - dmin*m
+ * (The last three are the rest of the K family the PESTI README names; they
+ * run on the generic kernels.)
+ * W is n_out rows; row r holds k/QK consecutive blocks (QK = 32 for Q8_0, 1
+ * for PQ_I8_ROW, 256 for the K formats), rows contiguous, no padding.
  *
  * Ownership and threading: the caller allocates and owns every buffer it
  * passes (device memory, e.g. from cudaMalloc or a framework allocator).  The
@@ -55,7 +64,10 @@ typedef enum {
     PQ_Q8_0 = 0,
     PQ_Q4_K = 1,
     PQ_Q6_K = 2,
-    PQ_I8_ROW = 3
+    PQ_I8_ROW = 3,
+    PQ_Q5_K = 4,
+    PQ_Q3_K = 5,
+    PQ_Q2_K = 6
 } pq_fmt;
 
 /* Status codes. */

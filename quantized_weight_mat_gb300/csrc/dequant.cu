@@ -1,7 +1,7 @@
 // pq_dequant kernels: decode every block of W to f32, bit-exact to the
-// layout rules (GGUF-style Q8_0 / Q4_K / Q6_K blocks that the PESTI README,
-// "What This Is", dequantizes byte-exactly; per-row int8 of the ember
-// pull request's quant.rs description).
+// layout rules (GGUF-style Q8_0 / Q4_K / Q6_K / Q5_K / Q3_K / Q2_K blocks that
+// the PESTI README, "What This Is", dequantizes byte-exactly; per-row int8 of
+// the ember pull request's quant.rs description).
 //
 // Write-bound: 4 B of output per weight against 0.56-1.06 B read.  One warp
 // decodes one super-block (Q4_K, Q6_K) or eight Q8_0 blocks per step, each
@@ -110,6 +110,22 @@ __global__ void __launch_bounds__(kThreads) dequant_q8_0(const uint8_t *__restri
     }
 }
 
+// Q5_K / Q3_K / Q2_K: one warp per super-block, lane l writes weights
+// 8l..8l+7 (pq_kfamily.cuh).
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) dequant_kfamily(const uint8_t *__restrict__ w,
+                                                            int64_t nblk, float *__restrict__ out) {
+    constexpr int BB = kBlockBytes[FMT];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t gb = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); gb < nblk;
+         gb += warps) {
+        float v[8];
+        kfamily_lane<FMT>(w + gb * BB, lane, v);
+        store8(out + gb * 256 + 8 * lane, v);
+    }
+}
+
 // Per-row int8, four outputs per thread when k % 4 == 0.
 __global__ void __launch_bounds__(kThreads) dequant_i8_row_v4(const uint8_t *__restrict__ w,
                                                               int64_t n_out, int64_t k,
@@ -167,6 +183,19 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, 
     case PQ_Q8_0: {
         const int64_t nblk = n_out * (k / 32);
         dequant_q8_0<<<grid_for((nblk + 7) / 8, wpb), kThreads, 0, s>>>(w, nblk, out);
+        break;
+    }
+    case PQ_Q5_K:
+    case PQ_Q3_K:
+    case PQ_Q2_K: {
+        const int64_t nblk = n_out * (k / 256);
+        const int grid = grid_for(nblk, wpb);
+        if (fmt == PQ_Q5_K)
+            dequant_kfamily<PQ_Q5_K><<<grid, kThreads, 0, s>>>(w, nblk, out);
+        else if (fmt == PQ_Q3_K)
+            dequant_kfamily<PQ_Q3_K><<<grid, kThreads, 0, s>>>(w, nblk, out);
+        else
+            dequant_kfamily<PQ_Q2_K><<<grid, kThreads, 0, s>>>(w, nblk, out);
         break;
     }
     case PQ_I8_ROW: {

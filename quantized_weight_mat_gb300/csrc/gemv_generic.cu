@@ -155,6 +155,34 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Q5_K / Q3_K / Q2_K: lane l decodes weights 8l..8l+7 of each super-block
+// of the row (pq_kfamily.cuh) and multiplies them by x.
+template <int FMT, int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_kfamily(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                         float *__restrict__ y, int64_t ldy) {
+    constexpr int BB = kBlockBytes[FMT];
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const int nb = k / 256;
+    const uint8_t *wr = w + (int64_t)row * nb * BB;
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+#pragma unroll 2
+    for (int blk = 0; blk < nb; ++blk) {
+        float wv[8];
+        kfamily_lane<FMT>(wr + (int64_t)blk * BB, lane, wv);
+        fma8<NB>(acc, wv, x, k, (int64_t)blk * 256 + 8 * lane, false);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = v;
+    }
+}
+
 // Per-row int8: lanes stride the row 4 codes at a time when k % 4 == 0
 // (row starts are then 4-byte aligned), else one code at a time.
 template <int NB>
@@ -206,6 +234,9 @@ cudaError_t launch_nb(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const
     case PQ_Q4_K: gemv_generic_q4_k<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
     case PQ_Q6_K: gemv_generic_q6_k<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
     case PQ_Q8_0: gemv_generic_q8_0<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_Q5_K: gemv_generic_kfamily<PQ_Q5_K, NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_Q3_K: gemv_generic_kfamily<PQ_Q3_K, NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
+    case PQ_Q2_K: gemv_generic_kfamily<PQ_Q2_K, NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy); break;
     case PQ_I8_ROW:
         gemv_generic_i8_row<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy,
                                                           i8row_scale_offset(n_out, k));

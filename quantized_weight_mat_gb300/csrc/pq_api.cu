@@ -79,7 +79,7 @@ using namespace pqk;
 
 namespace {
 
-bool valid_fmt(int fmt) { return fmt >= PQ_Q8_0 && fmt <= PQ_I8_ROW; }
+bool valid_fmt(int fmt) { return fmt >= 0 && fmt < kNumFmts; }
 
 // Bytes of W, or -1 when the shape is invalid / overflows.
 int64_t weight_bytes64(int fmt, int64_t n_out, int64_t k) {

@@ -4,6 +4,9 @@
 #include <cstdint>
 #include <cuda_fp16.h>
 
+#include "pq.h"
+#include "pq_kfamily.cuh"
+
 namespace pqk {
 
 // IEEE binary16 bits -> f32 (exact hardware conversion).
@@ -45,6 +48,29 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
         sc = ((s2 >> b) & 15) | (((s0 >> (b + 6)) & 3) << 4);
         m = ((s2 >> (b + 4)) & 15) | (((s1 >> (b + 6)) & 3) << 4);
     }
+}
+
+// Read-only loads at byte offsets of one block, for the K-family decoders
+// (pq_kfamily.cuh); the decoders keep every access aligned to its width.
+struct BlockLoad {
+    const uint8_t *p;
+    __device__ __forceinline__ uint32_t u8(int o) const { return __ldg(p + o); }
+    __device__ __forceinline__ uint32_t u16(int o) const { return ldg_u16(p + o); }
+    __device__ __forceinline__ uint32_t u32(int o) const { return ldg_u32(p + o); }
+    __device__ __forceinline__ float f16(int o) const { return h2f(ldg_u16(p + o)); }
+};
+
+// Weights 8*lane .. 8*lane+7 of one Q5_K / Q3_K / Q2_K super-block.
+template <int FMT>
+__device__ __forceinline__ void kfamily_lane(const uint8_t *blk, int lane, float (&w)[8]) {
+    static_assert(FMT == PQ_Q5_K || FMT == PQ_Q3_K || FMT == PQ_Q2_K, "K-family format");
+    const BlockLoad ld{blk};
+    if constexpr (FMT == PQ_Q5_K)
+        q5k_lane(ld, lane, w);
+    else if constexpr (FMT == PQ_Q3_K)
+        q3k_lane(ld, lane, w);
+    else
+        q2k_lane(ld, lane, w);
 }
 
 }  // namespace pqk

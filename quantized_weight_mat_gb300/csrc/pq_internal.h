@@ -30,8 +30,9 @@ private:
     cudaError_t status_[kMaxDeviceIds] = {};
 };
 
-constexpr int kQK[4] = {32, 256, 256, 1};        // weights per block
-constexpr int kBlockBytes[4] = {34, 144, 210, 1}; // bytes per block
+constexpr int kNumFmts = 7;                                    // pq_fmt values 0..6
+constexpr int kQK[kNumFmts] = {32, 256, 256, 1, 256, 256, 256};  // weights per block
+constexpr int kBlockBytes[kNumFmts] = {34, 144, 210, 1, 176, 110, 84};   // bytes per block
 
 // Byte offset of the f32 scales of a per-row int8 matrix.
 inline int64_t i8row_scale_offset(int64_t n_out, int64_t k) { return (n_out * k + 15) / 16 * 16; }

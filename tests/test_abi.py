@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_weight_bytes_agree_with_oracle():
-    for fmt in ("q8_0", "q4_k", "q6_k", "i8_row"):
+    for fmt in ("q8_0", "q4_k", "q6_k", "i8_row", "q5_k", "q3_k", "q2_k"):
         for n_out, k in [(1, 256), (7, 512), (896, 896 if fmt in ("q8_0", "i8_row") else 1024),
                          (128256, 4096)]:
             assert pq.pq_weight_bytes(fmt, n_out, k) == oracle.weight_bytes(fmt, n_out, k)
@@ -64,6 +64,8 @@ A16 = 1 << 20        # a 16-byte aligned fake address (never dereferenced)
     (("q4_k", A16, 4, 256, A16 * 2, 0, A16 * 3), pq.PQ_ERR_ARG),
     (("q4_k", A16, 4, 100, A16 * 2, 1, A16 * 3), pq.PQ_ERR_K),
     (("q8_0", A16, 4, 48, A16 * 2, 1, A16 * 3), pq.PQ_ERR_K),
+    (("q5_k", A16, 4, 128, A16 * 2, 1, A16 * 3), pq.PQ_ERR_K),
+    (("q2_k", A16, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_OK),
     (("q4_k", A16 + 8, 4, 256, A16 * 2, 1, A16 * 3), pq.PQ_ERR_ALIGN),
     (("q4_k", A16, 4, 256, A16 * 2 + 4, 1, A16 * 3), pq.PQ_ERR_ALIGN),
     (("q4_k", A16, 4, 256, A16 * 2, 1, A16 * 3 + 2), pq.PQ_ERR_ALIGN),
@@ -88,7 +90,8 @@ def test_dequant_argument_checks():
     assert L.pq_dequant(1, A16, 4, 256, 0, 0) == pq.PQ_ERR_ARG
     assert L.pq_dequant(1, A16, 4, 256, A16 * 2 + 4, 0) == pq.PQ_ERR_ALIGN
     assert L.pq_dequant(1, A16, 4, 255, A16 * 2, 0) == pq.PQ_ERR_K
-    assert L.pq_dequant(5, A16, 4, 256, A16 * 2, 0) == pq.PQ_ERR_FMT
+    assert L.pq_dequant(9, A16, 4, 256, A16 * 2, 0) == pq.PQ_ERR_FMT
+    assert L.pq_dequant(pq.Q3_K, A16, 4, 200, A16 * 2, 0) == pq.PQ_ERR_K
     assert L.pq_dequant(1, A16, 4, 256, A16 + 32, 0) == pq.PQ_ERR_ARG   # out overlaps w
 
 
@@ -104,6 +107,15 @@ def test_kernel_choice_table():
             # slices of up to 16 (tensor core) or 4 columns, or one column at a
             # time for a one-column streaming kernel (Q6_K)
             assert (b + 15) // 16 <= n <= (b if fmt == "q6_k" else (b + 3) // 4)
+
+
+def test_k_family_formats_take_the_generic_kernel():
+    # Q5_K / Q3_K / Q2_K run on the generic kernel at every batch, 4 columns a launch
+    for fmt in ("q5_k", "q3_k", "q2_k"):
+        assert pq.pq_gemv_choice(fmt, 4096, 100, 1) == pq.PQ_ERR_K
+        for b in (1, 2, 4, 5, 16, 17):
+            assert pq.pq_gemv_choice(fmt, 4096, 4096, b) == pq.KERNEL_GENERIC
+            assert pq.pq_gemv_launches(fmt, 4096, 4096, b) == (b + 3) // 4
 
 
 def test_bad_kernel_id_rejected():

@@ -63,11 +63,18 @@ DQ_CASES = [
     ("q4_k", 1, 256), ("q4_k", 7, 768), ("q4_k", 129, 4096), ("q4_k", 37, 14336),
     ("q6_k", 1, 256), ("q6_k", 7, 768), ("q6_k", 129, 4096), ("q6_k", 9, 14336),
     ("i8_row", 1, 1), ("i8_row", 7, 13), ("i8_row", 129, 100), ("i8_row", 33, 4096),
+    ("q5_k", 1, 256), ("q5_k", 7, 768), ("q5_k", 129, 4096), ("q5_k", 9, 14336),
+    ("q3_k", 1, 256), ("q3_k", 7, 768), ("q3_k", 129, 4096), ("q3_k", 9, 14336),
+    ("q2_k", 1, 256), ("q2_k", 7, 768), ("q2_k", 129, 4096), ("q2_k", 9, 14336),
 ]
+# formats the oracle can quantize; the others (Q5_K, Q3_K, Q2_K) are tested on
+# random records, which hold every bit pattern of every field
+QUANTIZABLE = {"q8_0", "q4_k", "q6_k", "i8_row"}
+DQ_PARAMS = [(f, n, k, kind) for (f, n, k) in DQ_CASES
+             for kind in (("quantized", "random") if f in QUANTIZABLE else ("random",))]
 
 
-@pytest.mark.parametrize("kind", ["quantized", "random"])
-@pytest.mark.parametrize("fmt,n_out,k", DQ_CASES)
+@pytest.mark.parametrize("fmt,n_out,k,kind", DQ_PARAMS)
 def test_dequant_bit_exact(fmt, n_out, k, kind):
     import torch
     w = weights(fmt, n_out, k, kind, 100 + n_out)
@@ -87,6 +94,9 @@ GEMV_SHAPES = {
     "q4_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (37, 14336)],
     "q6_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (9, 14336)],
     "i8_row": [(1, 1), (7, 13), (129, 100), (300, 4096), (33, 2048)],
+    "q5_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
+    "q3_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
+    "q2_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
 }
 CASES = [(f, n, k) for f, shapes in GEMV_SHAPES.items() for (n, k) in shapes]
 
@@ -95,7 +105,8 @@ CASES = [(f, n, k) for f, shapes in GEMV_SHAPES.items() for (n, k) in shapes]
 @pytest.mark.parametrize("kernel", ["auto", "generic", "stream", "tc"])
 @pytest.mark.parametrize("fmt,n_out,k", CASES)
 def test_gemv_parity(fmt, n_out, k, kernel, batch):
-    w = weights(fmt, n_out, k, "random" if n_out % 2 else "quantized", 200 + n_out)
+    kind = "random" if n_out % 2 or fmt not in QUANTIZABLE else "quantized"
+    w = weights(fmt, n_out, k, kind, 200 + n_out)
     x = x_for(batch, k, 300 + batch)
     y = run_gemv(fmt, w, n_out, k, x, kernel)
     if y is None:
@@ -107,7 +118,8 @@ def test_gemv_parity(fmt, n_out, k, kernel, batch):
 
 
 @pytest.mark.parametrize("fmt,n_out,k,batch", [("q4_k", 4096, 4096, 1), ("q6_k", 1000, 4096, 2),
-                                               ("q4_k", 4096, 4096, 16), ("q8_0", 896, 896, 1)])
+                                               ("q4_k", 4096, 4096, 16), ("q8_0", 896, 896, 1),
+                                               ("q5_k", 1000, 4096, 3), ("q2_k", 700, 2048, 5)])
 def test_gemv_deterministic(fmt, n_out, k, batch):
     import torch
     w = weights(fmt, n_out, k, "random", 7)
