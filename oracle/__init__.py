@@ -17,6 +17,8 @@ Parity pins (checked by ``tests/test_oracle.py``):
   * Q5_K / Q3_K / Q2_K decode: the same kinds of pins (closed forms on
     hand-built blocks, every single-bit flip of random blocks against the
     weights and amounts the layout predicts); no quantizer for them;
+  * per-row int4: closed form incl. the scale offset and sign extension,
+    single-bit flips, brute-force nearest code for the quantizer;
   * f64 mat-vec: integer-valued special cases against numpy's float64
     matmul, and exact rational sums on tiny shapes;
   * quantizers: brute-force best code on tiny matrices, re-quantization
@@ -31,9 +33,9 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K, I8_ROW, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5, 6
+Q8_0, Q4_K, Q6_K, I8_ROW, Q5_K, Q3_K, Q2_K, I4_ROW = 0, 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "i8_row": I8_ROW,
-           "q5_k": Q5_K, "q3_k": Q3_K, "q2_k": Q2_K}
+           "q5_k": Q5_K, "q3_k": Q3_K, "q2_k": Q2_K, "i4_row": I4_ROW}
 # weights and bytes per block of the block formats
 BLOCKS = {Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176),
           Q3_K: (256, 110), Q2_K: (256, 84)}

@@ -23,7 +23,10 @@
  * the K family the PESTI README names, Q5_K 176 B, Q3_K 110 B, Q2_K 84 B
  * per 256).  Per-row int8 has
  * no published layout; the one used here is: int8 q[n_out*k] row-major,
- * then, at the next 16-byte boundary, float scale[n_out].
+ * then, at the next 16-byte boundary, float scale[n_out].  Per-row int4 (the
+ * ember page's "INT8/INT4") likewise: two signed 4-bit codes per byte, weight
+ * 2i in the low nibble of byte i and weight 2i+1 in the high nibble, rows of
+ * k/2 bytes (k even), then float scale[n_out] at the next 16-byte boundary.
  *
  * Quantizers: the pages give none (PESTI dequantizes files made by other
  * tools).  The ones here are a plain, deterministic, non-iterative reading
@@ -44,7 +47,8 @@
 #include <omp.h>
 #endif
 
-enum { PQO_Q8_0 = 0, PQO_Q4_K = 1, PQO_Q6_K = 2, PQO_I8_ROW = 3, PQO_Q5_K = 4, PQO_Q3_K = 5, PQO_Q2_K = 6 };
+enum { PQO_Q8_0 = 0, PQO_Q4_K = 1, PQO_Q6_K = 2, PQO_I8_ROW = 3, PQO_Q5_K = 4, PQO_Q3_K = 5, PQO_Q2_K = 6,
+       PQO_I4_ROW = 7 };
 
 /* ------------------------------------------------------------------ */
 /* IEEE-754 binary16                                                   */
@@ -126,6 +130,7 @@ int pqo_block_weights(int fmt)
     case PQO_Q5_K: return 256;
     case PQO_Q3_K: return 256;
     case PQO_Q2_K: return 256;
+    case PQO_I4_ROW: return 2;
     }
     return -1;
 }
@@ -140,6 +145,7 @@ int pqo_block_bytes(int fmt)
     case PQO_Q5_K: return 176;
     case PQO_Q3_K: return 110;
     case PQO_Q2_K: return 84;
+    case PQO_I4_ROW: return 1;
     }
     return -1;
 }
@@ -156,6 +162,8 @@ int64_t pqo_weight_bytes(int fmt, int64_t n_out, int64_t k)
     int qk = pqo_block_weights(fmt), bb = pqo_block_bytes(fmt);
     if (qk <= 0 || k % qk)
         return -1;
+    if (fmt == PQO_I4_ROW)
+        return (n_out * (k / 2) + 15) / 16 * 16 + 4 * n_out;
     return n_out * (k / qk) * bb;
 }
 
@@ -163,6 +171,14 @@ static int64_t i8row_scale_offset(int64_t n_out, int64_t k)
 {
     return (n_out * k + 15) / 16 * 16;
 }
+
+static int64_t i4row_scale_offset(int64_t n_out, int64_t k)
+{
+    return (n_out * (k / 2) + 15) / 16 * 16;
+}
+
+/* Signed value of the 4-bit two's-complement code c (0..15): -8..7. */
+static int i4_value(int c) { return c >= 8 ? c - 16 : c; }
 
 /* ------------------------------------------------------------------ */
 /* Block decoders (one block -> f32)                                   */
@@ -343,6 +359,16 @@ static void decode_row(int fmt, const uint8_t *W, int64_t n_out, int64_t k, int6
         memcpy(&s, W + i8row_scale_offset(n_out, k) + 4 * r, 4);
         for (int64_t i = 0; i < k; ++i)
             w[i] = s * (float)q[i];
+        return;
+    }
+    if (fmt == PQO_I4_ROW) {
+        const uint8_t *q = W + r * (k / 2);
+        float s;
+        memcpy(&s, W + i4row_scale_offset(n_out, k) + 4 * r, 4);
+        for (int64_t i = 0; i < k; ++i) {
+            int c = (i % 2 == 0) ? (q[i / 2] & 0x0f) : (q[i / 2] >> 4);
+            w[i] = s * (float)i4_value(c);
+        }
         return;
     }
     int qk = pqo_block_weights(fmt), bb = pqo_block_bytes(fmt);
@@ -598,6 +624,25 @@ int pqo_quantize(int fmt, const float *v, int64_t n_out, int64_t k, uint8_t *out
             for (int64_t i = 0; i < k; ++i) {
                 int q = s > 0.0f ? clampi(round((double)vr[i] / (double)s), -127, 127) : 0;
                 out[r * k + i] = (uint8_t)(int8_t)q;
+            }
+            memcpy(out + soff + 4 * r, &s, 4);
+        }
+        return 0;
+    }
+    if (fmt == PQO_I4_ROW) {
+        /* per-row symmetric: s = max|v_r|/7 (f32), q = clamp(round(v/s), -7, 7) */
+        int64_t soff = i4row_scale_offset(n_out, k);
+        memset(out, 0, (size_t)total);
+#pragma omp parallel for schedule(static) num_threads(nt)
+        for (int64_t r = 0; r < n_out; ++r) {
+            const float *vr = v + r * k;
+            double amax = 0.0;
+            for (int64_t i = 0; i < k; ++i)
+                if (fabs((double)vr[i]) > amax) amax = fabs((double)vr[i]);
+            float s = (float)(amax / 7.0);
+            for (int64_t i = 0; i < k; ++i) {
+                int q = s > 0.0f ? clampi(round((double)vr[i] / (double)s), -7, 7) : 0;
+                out[r * (k / 2) + i / 2] |= (uint8_t)((q & 0x0f) << (4 * (int)(i % 2)));
             }
             memcpy(out + soff + 4 * r, &s, 4);
         }

@@ -21,7 +21,7 @@ Generators (numpy PCG64 via ``default_rng``):
 Byte offsets of the fp16 fields (the only layout facts used here):
 Q8_0 d @0; Q4_K d @0, dmin @2; Q6_K d @208; Q5_K d @0, dmin @2; Q3_K d @108;
 Q2_K d @80, dmin @82.  Per-row int8: codes [n_out*k] then f32 scales at the
-next 16-byte boundary.
+next 16-byte boundary; per-row int4 the same with two codes per byte.
 """
 from __future__ import annotations
 
@@ -52,6 +52,9 @@ def normal_x(batch: int, k: int, seed: int) -> np.ndarray:
 def weight_bytes(fmt: str, n_out: int, k: int) -> int:
     if fmt == "i8_row":
         return (n_out * k + 15) // 16 * 16 + 4 * n_out
+    if fmt == "i4_row":
+        assert k % 2 == 0
+        return (n_out * k // 2 + 15) // 16 * 16 + 4 * n_out
     qk, bb = BLOCK[fmt]
     assert k % qk == 0
     return n_out * (k // qk) * bb
@@ -80,11 +83,12 @@ def random_records(fmt: str, n_out: int, k: int, seed: int,
                    d_range=(2e-5, 4e-4), dmin_range=(1e-4, 2e-3)) -> np.ndarray:
     """Uniform random bytes with finite positive fp16 scale fields."""
     g = rng(seed)
-    if fmt == "i8_row":
+    if fmt in ("i8_row", "i4_row"):
         total = weight_bytes(fmt, n_out, k)
+        nq = n_out * k if fmt == "i8_row" else n_out * k // 2
         buf = np.zeros(total, dtype=np.uint8)
-        buf[: n_out * k] = np.frombuffer(g.bytes(n_out * k), dtype=np.uint8)
-        soff = (n_out * k + 15) // 16 * 16
+        buf[:nq] = np.frombuffer(g.bytes(nq), dtype=np.uint8)
+        soff = (nq + 15) // 16 * 16
         s = g.uniform(1e-4, 4e-4, size=n_out).astype(np.float32)
         buf[soff: soff + 4 * n_out] = s.astype("<f4").view(np.uint8)
         return buf

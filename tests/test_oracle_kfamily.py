@@ -279,3 +279,59 @@ def test_gemv_exact_rational_tiny(fmt):
 def test_no_quantizer(fmt):
     with pytest.raises(RuntimeError):
         oracle.quantize(fmt, np.zeros((2, 256), dtype=np.float32))
+
+
+# ---------------------------------------------------------------- per-row int4
+
+def pack_i4_row(q, scales) -> np.ndarray:
+    """q: [n_out, k] ints in -8..7; scales: n_out f32."""
+    n_out, k = q.shape
+    nq = n_out * k // 2
+    buf = np.zeros((nq + 15) // 16 * 16 + 4 * n_out, dtype=np.uint8)
+    codes = (np.asarray(q, dtype=np.int64) & 15).reshape(-1)
+    buf[:nq] = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+    off = (nq + 15) // 16 * 16
+    buf[off:off + 4 * n_out] = np.asarray(scales, dtype="<f4").view(np.uint8)
+    return buf
+
+
+def test_i4_row_closed_form_sign_and_layout():
+    n_out, k = 3, 10                       # 15 code bytes: the scales start at byte 16
+    q = np.array([[(r * 7 + i * 3) % 16 - 8 for i in range(k)] for r in range(n_out)])
+    scales = [0.5, -0.25, 3.0]
+    w = pack_i4_row(q, scales)
+    assert oracle.weight_bytes("i4_row", n_out, k) == len(w) == 16 + 12
+    got = oracle.dequant("i4_row", w, n_out, k)
+    want = np.array([[np.float32(scales[r]) * np.float32(q[r, i]) for i in range(k)]
+                     for r in range(n_out)], dtype=np.float32)
+    assert np.array_equal(got, want)
+    assert got.min() == -8 * 3.0          # code 8 reads as -8
+    with pytest.raises(ValueError):
+        oracle.weight_bytes("i4_row", 2, 7)
+
+
+def test_i4_row_bit_flips():
+    n_out, k = 2, 16
+    w = synth.random_records("i4_row", n_out, k, seed=41)
+    base = oracle.dequant("i4_row", w, n_out, k).ravel()
+    for byte in range(n_out * k // 2):
+        for bit in range(8):
+            w2 = w.copy()
+            w2[byte] ^= 1 << bit
+            ch = set(np.nonzero(oracle.dequant("i4_row", w2, n_out, k).ravel() != base)[0].tolist())
+            assert ch == {2 * byte + (1 if bit >= 4 else 0)}, (byte, bit)
+
+
+def test_i4_row_quantizer_nearest_code():
+    g = np.random.default_rng(42)
+    v = g.normal(0, 0.02, size=(4, 64)).astype(np.float32)
+    w = oracle.quantize("i4_row", v)
+    deq = oracle.dequant("i4_row", w, 4, 64).astype(np.float64)
+    off = (4 * 32 + 15) // 16 * 16
+    s = w[off:off + 16].view("<f4").astype(np.float64)
+    assert np.allclose(s, np.abs(v).max(axis=1) / 7.0, rtol=1e-6)
+    for r in range(4):
+        cand = s[r] * np.arange(-7, 8)               # every code the quantizer may choose
+        best = np.abs(v[r][:, None].astype(np.float64) - cand[None, :]).min(axis=1)
+        err = np.abs(v[r].astype(np.float64) - deq[r])
+        assert np.all(err <= best + 1e-6 * s[r])
