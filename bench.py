@@ -174,7 +174,7 @@ CONFIGS = [
 ] + [(f"Q4_K {n}x{k}, batch {b}", "q4_k", n, k, b)
      for (n, k) in ((14336, 4096), (4096, 14336)) for b in (1, 2, 4, 8, 16)
 ] + [(f"{f.upper()} 14336x4096, batch 1 (generic kernel)", f, 14336, 4096, 1)
-     for f in ("q5_k", "q3_k", "q2_k")]
+     for f in ("q5_k", "q3_k", "q2_k", "i4_row")]
 
 
 def per_config(pq, dev, peak, l2_bytes):

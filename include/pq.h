@@ -29,10 +29,15 @@
  *            16 packed signed 6-bit scales, f16 d.  w = (d*sc)*v, v in -4..3
  *   PQ_Q2_K   84 B per 256: 16 B of 4-bit (scale, min) pairs, 64 B of 2-bit
  *            q, f16 d, f16 dmin.                 w = (d*sc)*q - dmin*m
- * (The last three are the rest of the K family the PESTI README names; they
- * run on the generic kernels.)
+ *   PQ_I4_ROW per-row symmetric int4 (k even): two's-complement 4-bit codes,
+ *            weight 2i in the low nibble of byte i of the row, 2i+1 in the
+ *            high nibble, rows of k/2 bytes; then at the next 16-byte
+ *            boundary f32 scale[n_out].         w = scale[r]*q, q in -8..7
+ * (Q5_K, Q3_K and Q2_K are the rest of the K family the PESTI README names;
+ * they and PQ_I4_ROW run on the generic kernels.)
  * W is n_out rows; row r holds k/QK consecutive blocks (QK = 32 for Q8_0, 1
- * for PQ_I8_ROW, 256 for the K formats), rows contiguous, no padding.
+ * for PQ_I8_ROW, 2 for PQ_I4_ROW, 256 for the K formats), rows contiguous,
+ * no padding.
  *
  * Ownership and threading: the caller allocates and owns every buffer it
  * passes (device memory, e.g. from cudaMalloc or a framework allocator).  The
@@ -67,7 +72,8 @@ typedef enum {
     PQ_I8_ROW = 3,
     PQ_Q5_K = 4,
     PQ_Q3_K = 5,
-    PQ_Q2_K = 6
+    PQ_Q2_K = 6,
+    PQ_I4_ROW = 7
 } pq_fmt;
 
 /* Status codes. */

@@ -12,9 +12,9 @@ import ctypes
 import os
 import threading
 
-Q8_0, Q4_K, Q6_K, I8_ROW, Q5_K, Q3_K, Q2_K = 0, 1, 2, 3, 4, 5, 6
+Q8_0, Q4_K, Q6_K, I8_ROW, Q5_K, Q3_K, Q2_K, I4_ROW = 0, 1, 2, 3, 4, 5, 6, 7
 FORMATS = {"q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "i8_row": I8_ROW,
-           "q5_k": Q5_K, "q3_k": Q3_K, "q2_k": Q2_K}
+           "q5_k": Q5_K, "q3_k": Q3_K, "q2_k": Q2_K, "i4_row": I4_ROW}
 KERNEL_AUTO, KERNEL_GENERIC, KERNEL_STREAM, KERNEL_TC = -1, 0, 1, 2
 KERNELS = {"auto": KERNEL_AUTO, "generic": KERNEL_GENERIC, "stream": KERNEL_STREAM, "tc": KERNEL_TC}
 

@@ -156,6 +156,41 @@ __global__ void __launch_bounds__(kThreads) dequant_i8_row_v1(const uint8_t *__r
         out[i] = __fmul_rn(__ldg(scale + i / k), (float)(int8_t)__ldg(w + i));
 }
 
+// Per-row int4: eight outputs per thread from one 32-bit word when k % 8 == 0
+// (rows then start 4-byte aligned and a word never crosses a row), else two
+// outputs from one byte (k is even, so a byte never crosses a row).  Weight e
+// of a word is its nibble e.
+__global__ void __launch_bounds__(kThreads) dequant_i4_row_v8(const uint8_t *__restrict__ w,
+                                                              int64_t n_out, int64_t k,
+                                                              int64_t soff, float *__restrict__ out) {
+    const int64_t n8 = n_out * k / 8;
+    const float *scale = reinterpret_cast<const float *>(w + soff);
+    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < n8;
+         t += (int64_t)gridDim.x * kThreads) {
+        const int64_t i0 = 8 * t;
+        const float s = __ldg(scale + i0 / k);
+        const uint32_t q = ldg_u32(w + 4 * t);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(s, i4_value((q >> (4 * e)) & 15u));
+        store8(out + i0, v);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_i4_row_v2(const uint8_t *__restrict__ w,
+                                                              int64_t n_out, int64_t k,
+                                                              int64_t soff, float *__restrict__ out) {
+    const int64_t nq = n_out * k / 2;
+    const float *scale = reinterpret_cast<const float *>(w + soff);
+    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < nq;
+         t += (int64_t)gridDim.x * kThreads) {
+        const float s = __ldg(scale + 2 * t / k);
+        const uint32_t b = __ldg(w + t);
+        reinterpret_cast<float2 *>(out)[t] =
+            make_float2(__fmul_rn(s, i4_value(b & 15u)), __fmul_rn(s, i4_value(b >> 4)));
+    }
+}
+
 int grid_for(int64_t work_items, int per_block) {
     int64_t g = (work_items + per_block - 1) / per_block;
     const DeviceInfo *dev = device_info();
@@ -196,6 +231,16 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, 
             dequant_kfamily<PQ_Q3_K><<<grid, kThreads, 0, s>>>(w, nblk, out);
         else
             dequant_kfamily<PQ_Q2_K><<<grid, kThreads, 0, s>>>(w, nblk, out);
+        break;
+    }
+    case PQ_I4_ROW: {
+        const int64_t soff = i4row_scale_offset(n_out, k);
+        if (k % 8 == 0)
+            dequant_i4_row_v8<<<grid_for(n_out * k / 8, kThreads), kThreads, 0, s>>>(w, n_out, k,
+                                                                                    soff, out);
+        else
+            dequant_i4_row_v2<<<grid_for(n_out * k / 2, kThreads), kThreads, 0, s>>>(w, n_out, k,
+                                                                                    soff, out);
         break;
     }
     case PQ_I8_ROW: {

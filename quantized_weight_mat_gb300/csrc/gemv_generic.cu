@@ -225,6 +225,46 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Per-row int4: lanes stride the row 8 codes (one 32-bit word) at a time when
+// k % 8 == 0 (row starts are then 4-byte aligned), else 2 codes (one byte).
+template <int NB>
+__global__ void __launch_bounds__(kThreads)
+    gemv_generic_i4_row(const uint8_t *__restrict__ w, int n_out, int k, const float *__restrict__ x,
+                        float *__restrict__ y, int64_t ldy, int64_t soff) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (row >= n_out) return;
+    const uint8_t *wr = w + (int64_t)row * (k / 2);
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    if ((k & 7) == 0) {
+        for (int i = 8 * lane; i < k; i += 256) {
+            const uint32_t q = ldg_u32(wr + i / 2);
+            float wv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wv[e] = i4_value((q >> (4 * e)) & 15u);
+            fma8<NB>(acc, wv, x, k, i, false);
+        }
+    } else {
+        for (int i = 2 * lane; i < k; i += 64) {
+            const uint32_t b8 = __ldg(wr + i / 2);
+            const float q0 = i4_value(b8 & 15u), q1 = i4_value(b8 >> 4);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                acc[b] = fmaf(q0, __ldg(x + (int64_t)b * k + i), acc[b]);
+                acc[b] = fmaf(q1, __ldg(x + (int64_t)b * k + i + 1), acc[b]);
+            }
+        }
+    }
+    const float s = __ldg(reinterpret_cast<const float *>(w + soff) + row);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const float v = warp_sum(acc[b]);
+        if (lane == 0) y[b * ldy + row] = s * v;
+    }
+}
+
 template <int NB>
 cudaError_t launch_nb(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x,
                       float *y, int64_t ldy, cudaStream_t s) {
@@ -240,6 +280,10 @@ cudaError_t launch_nb(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const
     case PQ_I8_ROW:
         gemv_generic_i8_row<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy,
                                                           i8row_scale_offset(n_out, k));
+        break;
+    case PQ_I4_ROW:
+        gemv_generic_i4_row<NB><<<grid, kThreads, 0, s>>>(w, n, kk, x, y, ldy,
+                                                          i4row_scale_offset(n_out, k));
         break;
     default: return cudaErrorInvalidValue;
     }

@@ -87,6 +87,7 @@ int64_t weight_bytes64(int fmt, int64_t n_out, int64_t k) {
     if (k % kQK[fmt]) return -1;
     if (n_out > (INT64_C(1) << 40) / k) return -1;   // n_out*k <= 2^40 weights
     if (fmt == PQ_I8_ROW) return i8row_scale_offset(n_out, k) + 4 * n_out;
+    if (fmt == PQ_I4_ROW) return i4row_scale_offset(n_out, k) + 4 * n_out;
     return n_out * (k / kQK[fmt]) * kBlockBytes[fmt];
 }
 

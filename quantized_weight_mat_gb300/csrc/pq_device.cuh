@@ -50,6 +50,9 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
     }
 }
 
+// Value of a 4-bit two's-complement code (0..15 -> -8..7), as f32.
+__device__ __forceinline__ float i4_value(uint32_t nib) { return (float)((int)(nib ^ 8u) - 8); }
+
 // Read-only loads at byte offsets of one block, for the K-family decoders
 // (pq_kfamily.cuh); the decoders keep every access aligned to its width.
 struct BlockLoad {

@@ -30,12 +30,14 @@ private:
     cudaError_t status_[kMaxDeviceIds] = {};
 };
 
-constexpr int kNumFmts = 7;                                    // pq_fmt values 0..6
-constexpr int kQK[kNumFmts] = {32, 256, 256, 1, 256, 256, 256};  // weights per block
-constexpr int kBlockBytes[kNumFmts] = {34, 144, 210, 1, 176, 110, 84};   // bytes per block
+constexpr int kNumFmts = 8;                                       // pq_fmt values 0..7
+constexpr int kQK[kNumFmts] = {32, 256, 256, 1, 256, 256, 256, 2};  // weights per block
+constexpr int kBlockBytes[kNumFmts] = {34, 144, 210, 1, 176, 110, 84, 1};   // bytes per block
 
 // Byte offset of the f32 scales of a per-row int8 matrix.
 inline int64_t i8row_scale_offset(int64_t n_out, int64_t k) { return (n_out * k + 15) / 16 * 16; }
+// Byte offset of the f32 scales of a per-row int4 matrix (k even).
+inline int64_t i4row_scale_offset(int64_t n_out, int64_t k) { return (n_out * (k / 2) + 15) / 16 * 16; }
 
 struct DeviceInfo {
     int sm_count;

@@ -33,12 +33,13 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_weight_bytes_agree_with_oracle():
-    for fmt in ("q8_0", "q4_k", "q6_k", "i8_row", "q5_k", "q3_k", "q2_k"):
+    for fmt in ("q8_0", "q4_k", "q6_k", "i8_row", "q5_k", "q3_k", "q2_k", "i4_row"):
         for n_out, k in [(1, 256), (7, 512), (896, 896 if fmt in ("q8_0", "i8_row") else 1024),
                          (128256, 4096)]:
             assert pq.pq_weight_bytes(fmt, n_out, k) == oracle.weight_bytes(fmt, n_out, k)
     assert pq.pq_weight_bytes("q4_k", 4, 100) == 0
-    assert pq.pq_weight_bytes(7, 4, 256) == 0
+    assert pq.pq_weight_bytes(8, 4, 256) == 0
+    assert pq.pq_weight_bytes("i4_row", 4, 7) == 0                # odd k
     assert pq.pq_weight_bytes("q4_k", 0, 256) == 0
     assert pq.pq_weight_bytes("q4_k", 1 << 30, 1 << 30) == 0     # overflow guard
 
@@ -109,10 +110,11 @@ def test_kernel_choice_table():
             assert (b + 15) // 16 <= n <= (b if fmt == "q6_k" else (b + 3) // 4)
 
 
-def test_k_family_formats_take_the_generic_kernel():
-    # Q5_K / Q3_K / Q2_K run on the generic kernel at every batch, 4 columns a launch
-    for fmt in ("q5_k", "q3_k", "q2_k"):
-        assert pq.pq_gemv_choice(fmt, 4096, 100, 1) == pq.PQ_ERR_K
+def test_generic_only_formats_take_the_generic_kernel():
+    # Q5_K / Q3_K / Q2_K and per-row int4 run on the generic kernel at every
+    # batch, 4 columns a launch
+    for fmt in ("q5_k", "q3_k", "q2_k", "i4_row"):
+        assert pq.pq_gemv_choice(fmt, 4096, 100 if fmt != "i4_row" else 101, 1) == pq.PQ_ERR_K
         for b in (1, 2, 4, 5, 16, 17):
             assert pq.pq_gemv_choice(fmt, 4096, 4096, b) == pq.KERNEL_GENERIC
             assert pq.pq_gemv_launches(fmt, 4096, 4096, b) == (b + 3) // 4

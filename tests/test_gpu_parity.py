@@ -66,10 +66,11 @@ DQ_CASES = [
     ("q5_k", 1, 256), ("q5_k", 7, 768), ("q5_k", 129, 4096), ("q5_k", 9, 14336),
     ("q3_k", 1, 256), ("q3_k", 7, 768), ("q3_k", 129, 4096), ("q3_k", 9, 14336),
     ("q2_k", 1, 256), ("q2_k", 7, 768), ("q2_k", 129, 4096), ("q2_k", 9, 14336),
+    ("i4_row", 1, 2), ("i4_row", 7, 14), ("i4_row", 129, 100), ("i4_row", 33, 4096),
 ]
 # formats the oracle can quantize; the others (Q5_K, Q3_K, Q2_K) are tested on
 # random records, which hold every bit pattern of every field
-QUANTIZABLE = {"q8_0", "q4_k", "q6_k", "i8_row"}
+QUANTIZABLE = {"q8_0", "q4_k", "q6_k", "i8_row", "i4_row"}
 DQ_PARAMS = [(f, n, k, kind) for (f, n, k) in DQ_CASES
              for kind in (("quantized", "random") if f in QUANTIZABLE else ("random",))]
 
@@ -97,6 +98,7 @@ GEMV_SHAPES = {
     "q5_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
     "q3_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
     "q2_k": [(1, 256), (7, 768), (129, 4096), (9, 14336)],
+    "i4_row": [(1, 2), (7, 14), (129, 100), (300, 4096), (33, 2048)],
 }
 CASES = [(f, n, k) for f, shapes in GEMV_SHAPES.items() for (n, k) in shapes]
 
