@@ -2,13 +2,13 @@
  * pq.h -- C ABI of the block-quantized mat-vec library for GB300 (sm_103a).
  *
  * The operation: the decode-step mat-vec y = W x with W kept in
- * block-quantized form and decoded on the fly, "a fused dequantize+mat-vec
- * that never expands weights back to f32" (ember pull request "Project
- * scaffold: modules, CLI, and correctness harness", quant.rs description),
- * applied to the row-major mat-vec "that dominates a decode step" (same
- * page, tensor.rs description).  The block formats are the K-family and
- * Q8_0 formats that the PESTI README ("What This Is", "Architecture")
- * dequantizes byte-exactly, plus the per-row symmetric int8 format of the
+ * block-quantized form and decoded inside the kernel, so that no f32 copy of
+ * W is ever made (ember pull request "Project scaffold: modules, CLI, and
+ * correctness harness", quant.rs description); the mat-vec is the row-major
+ * one that costs the most in a decode step (same page, tensor.rs
+ * description).  The block formats are the K-family and Q8_0 formats whose
+ * decoding the PESTI README ("What This Is", "Architecture") reports as
+ * exact to the byte, plus the per-row symmetric int8 and int4 formats of the
  * ember page.  The inferno README ("Design notes") fixes the boundary
  * style: contiguous row-major buffers in and out.
  *

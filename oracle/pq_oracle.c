@@ -10,12 +10,13 @@
  *   1. decode every quantized block to f32 by the layout rules below;
  *   2. y[b][r] = sum_i (double)w[r][i] * (double)x[b][i], summed in f64 in
  *      index order and returned in f64.
- * Source of the operation: the fused "dequantize + mat-vec that never
- * expands weights back to f32" of the ember pull request ("Project scaffold:
- * modules, CLI, and correctness harness", quant.rs description) over the
- * row-major mat-vec "that dominates a decode step" (same page, tensor.rs
- * description), with the K-family block formats that the PESTI README
- * ("What This Is", "Architecture") dequantizes byte-exactly.
+ * Source of the operation: the ember pull request ("Project scaffold:
+ * modules, CLI, and correctness harness", quant.rs description) fuses the
+ * decoding of W into the mat-vec so that no f32 copy of W is made; the
+ * mat-vec is the row-major one that costs the most in a decode step (same
+ * page, tensor.rs description); the block formats are the K family whose
+ * decoding the PESTI README ("What This Is", "Architecture") reports as
+ * exact to the byte.
  *
  * The pages never print a block's byte layout.  The layouts below are the
  * public GGUF layouts, read as a byte specification (sizes: Q8_0 34 B per
@@ -24,7 +25,7 @@
  * per 256).  Per-row int8 has
  * no published layout; the one used here is: int8 q[n_out*k] row-major,
  * then, at the next 16-byte boundary, float scale[n_out].  Per-row int4 (the
- * ember page's "INT8/INT4") likewise: two signed 4-bit codes per byte, weight
+ * ember page lists int4 beside int8) likewise: two signed 4-bit codes per byte, weight
  * 2i in the low nibble of byte i and weight 2i+1 in the high nibble, rows of
  * k/2 bytes (k even), then float scale[n_out] at the next 16-byte boundary.
  *

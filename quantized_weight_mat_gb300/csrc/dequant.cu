@@ -1,6 +1,6 @@
 // pq_dequant kernels: decode every block of W to f32, bit-exact to the
-// layout rules (GGUF-style Q8_0 / Q4_K / Q6_K / Q5_K / Q3_K / Q2_K blocks that
-// the PESTI README, "What This Is", dequantizes byte-exactly; per-row int8 of
+// layout rules (GGUF-style Q8_0 / Q4_K / Q6_K / Q5_K / Q3_K / Q2_K blocks, the
+// formats the PESTI README decodes, "What This Is"; per-row int8 and int4 of
 // the ember pull request's quant.rs description).
 //
 // Write-bound: 4 B of output per weight against 0.56-1.06 B read.  One warp

@@ -1,8 +1,8 @@
 // Generic fused dequant + mat-vec: one warp per output row, any format,
 // any shape, batch processed in chunks of up to 4 columns.
 //
-// This is the plain form of the operation (ember pull request, quant.rs:
-// "fused dequantize+mat-vec that never expands weights back to f32"): the
+// This is the plain form of the operation (ember pull request, quant.rs
+// description: decoding fused into the mat-vec, no f32 copy of W): the
 // warp walks its row's blocks, each lane decodes 8 weights per Q4_K / Q6_K
 // super-block (or per Q8_0 block group) to f32 in registers, multiplies by
 // x (read through the read-only cache; x is small and shared by every warp

@@ -1,9 +1,9 @@
 // Weight-streaming fused dequant + mat-vec for batch 1..4 on CUDA cores.
 //
-// The operation is the ember pull request's fused "dequantize+mat-vec that
-// never expands weights back to f32" (quant.rs description) for GGUF-style
-// Q4_K and Q6_K super-blocks (the K-family the PESTI README dequantizes,
-// "What This Is").  At batch 1 it moves 0.5625 B (Q4_K) per weight and does 2
+// The operation is the ember pull request's mat-vec with the decoding of W
+// fused into it, so that no f32 copy of W is made (quant.rs description),
+// for GGUF-style Q4_K and Q6_K super-blocks (the K family that the PESTI
+// README decodes, "What This Is").  At batch 1 it moves 0.5625 B (Q4_K) per weight and does 2
 // flops per weight: it is bound by HBM bandwidth, and the design goal is to
 // keep HBM busy while spending as few issue slots per weight as possible.
 //

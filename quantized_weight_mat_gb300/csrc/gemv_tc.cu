@@ -1,7 +1,7 @@
 // Tensor-core fused dequant + mat-vec for Q4_K at batch 5..16 (tcgen05).
 //
-// The operation is the same fused "dequantize + mat-vec" (ember pull request,
-// quant.rs description) on GGUF-style Q4_K super-blocks (PESTI README, "What
+// The operation is the same mat-vec with the decoding of W fused into it
+// (ember pull request, quant.rs description) on GGUF-style Q4_K super-blocks (PESTI README, "What
 // This Is"), for several x columns at once.  At batch 8-16 each weight feeds
 // 8-16 multiply-adds, too many for CUDA cores at HBM speed, so the products go
 // to the 5th-generation tensor cores while the weights still stream once.

@@ -1,7 +1,7 @@
 // Decoders of the Q5_K, Q3_K and Q2_K super-blocks (256 weights each), the
-// rest of the K family that the PESTI README ("What This Is") dequantizes
-// byte-exactly.  The pages print no layout; these are the public GGUF ones,
-// read as a byte specification:
+// rest of the K family that the PESTI README ("What This Is") decodes.  The
+// pages print no layout; these are the public GGUF ones, read as a byte
+// specification:
 //   Q5_K 176 B: f16 d @0, f16 dmin @2, 12 bytes of packed 6-bit (scale, min)
 //        pairs @4 (packed as in Q4_K), qh[32] @16, qs[128] @48.  Chunk c of
 //        64 weights: sub-block 2c from the low nibbles of qs[32c..32c+31],
@@ -28,8 +28,6 @@
 #include <cstdint>
 
 namespace pqk {
-
-constexpr int kQ5KBytes = 176, kQ3KBytes = 110, kQ2KBytes = 84;
 
 __host__ __device__ inline float kf_mul(float a, float b) {
 #ifdef __CUDA_ARCH__

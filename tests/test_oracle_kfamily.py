@@ -1,7 +1,7 @@
 """Pins for the oracle's Q5_K, Q3_K and Q2_K decoders.
 
 The pages name these formats only as members of the K family that PESTI
-dequantizes byte-exactly (PESTI README, "What This Is"); their byte layouts
+decodes (PESTI README, "What This Is"); their byte layouts
 are the public GGUF ones, read as a byte specification.  Each decoder is tied
 here to things other than itself: hand-built blocks packed by an inverse map
 written separately from the decoder (closed forms, exact rational rounding),
