@@ -4,6 +4,8 @@ Argument marshalling only: every function forwards to the C ABI declared in
 ``include/pq.h`` under the same name.  Pointer arguments accept a torch
 tensor (its ``data_ptr()``) or a plain integer address; ``stream`` accepts a
 ``torch.cuda.Stream``, a raw handle, or None for torch's current stream.
+``fmt`` is a name from ``FORMATS`` ("q8_0", "q4_k", "q6_k", "q5_k", "q3_k",
+"q2_k", "i8_row", "i4_row") or the ``pq_fmt`` value itself.
 A missing or unloadable library raises: there is no fallback.
 """
 from __future__ import annotations
