@@ -140,3 +140,23 @@ def test_selftest_limit_is_checked_before_any_launch():
     L = pq.lib()
     assert L.pq_selftest_wait_timeout(0, 0) == pq.PQ_ERR_ARG
     assert L.pq_selftest_wait_timeout(1000001, 0) == pq.PQ_ERR_ARG
+
+
+def test_q4_k_dispatch_matches_the_measured_winners():
+    # batch 1-4 winners measured on the decode-layer shapes (CUDA graph, GB300):
+    # the streaming kernels up to the batch where the tensor-core kernel wins,
+    # the tensor-core kernel from batch 5 on
+    S, T = pq.KERNEL_STREAM, pq.KERNEL_TC
+    table = {
+        (14336, 4096): [S, S, S, T, T, T, T],
+        (4096, 14336): [S, S, T, T, T, T, T],
+        (28672, 4096): [S, S, S, T, T, T, T],
+        (6144, 4096): [S, S, S, S, T, T, T],
+        (4096, 4096): [S, S, S, S, T, T, T],
+    }
+    for (n, k), want in table.items():
+        got = [pq.pq_gemv_choice("q4_k", n, k, b) for b in (1, 2, 3, 4, 5, 8, 16)]
+        assert got == want, (n, k, got)
+    # the Q6_K head streams one column at a time at any batch
+    assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 4)] == [S, S, S]
+    assert pq.pq_gemv_launches("q6_k", 128256, 4096, 4) == 4
