@@ -99,8 +99,13 @@ typedef enum {
  *
  * Accuracy: partial sums are accumulated in f32; the result agrees with the
  * exact dot product of the decoded f32 weights within
- * 2e-3 * RMS(y) + 1e-6 (see the tests).  Deterministic: repeated calls with the
- * same inputs give bit-identical y.  There is no host fallback: every step
+ * 2e-3 * RMS(y) + 1e-6 (see the tests).  Range of x: the tensor-core kernel
+ * (Q4_K at batch >= 5, and at batch 3-4 for long rows or large matrices;
+ * see pq_gemv_choice) takes x as fp16 pairs x_hi + x_lo, so it needs
+ * |x| < 65504 -- larger values overflow to inf -- and resolves values below
+ * 2^-14 only to 2^-25 absolutely; the other kernels scale x per 256 values
+ * or use it in f32 and have neither limit.  Deterministic: repeated calls
+ * with the same inputs give bit-identical y.  There is no host fallback: every step
  * runs in this library's CUDA kernels.
  */
 int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k,

@@ -1,0 +1,146 @@
+"""The arithmetic facts the kernels' precision rests on, checked on the CPU.
+
+1. Tensor-core decode: a 4-bit code q and a 6-bit scale sc become the fp16
+   value sc*q through one fused multiply-add on a biased operand, (1024+q)*sc
+   - 1024*sc for low nibbles and (1024+16q)*(sc/16) - 64*sc for high nibbles.
+   Every operand is an exact fp16 value and the exact result sc*q <= 945 is
+   an fp16 integer, so the single rounding of the fused operation is exact.
+2. Tensor-core x operand: x = x_hi + x_lo with x_hi = fp16(x) and x_lo =
+   fp16(x - x_hi) leaves a residual of at most 2^-21 |x| + 2^-25 (x_lo turns
+   subnormal below 2^-14, where fp16 has a fixed step of 2^-24), and it
+   holds only for |x| < 65520, above which x_hi overflows; every product
+   (sc*q) * x_hi and (sc*q) * x_lo is exact in the f32 accumulator.
+3. Batch-1 x limbs: per 256 values, x ~= u*(254*xh + xl) with int8 limbs
+   made by the 1.5*2^23 round-to-nearest shift.  Both limbs stay in
+   [-127, 127] without any clamp (the kernel relies on it), and the error is
+   at most about max|x|/64516.
+The emulation rounds each step exactly as the kernel does: fused operations
+are computed exactly with rationals and rounded once to f32.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+
+def f16_exact(v) -> bool:
+    return Fraction(float(np.float16(float(v)))) == Fraction(v)
+
+
+def f32(v) -> np.float32:
+    """Round an exact value (Fraction or float) to f32, nearest-even."""
+    if isinstance(v, Fraction):
+        # f64 first is exact enough only for short rationals; go through
+        # numpy's correctly rounded conversion of the nearest f64 when exact
+        d = float(v)
+        if Fraction(d) == v:
+            return np.float32(d)
+        # not representable in f64: pick the nearer f32 neighbour exactly
+        lo = np.float32(d)
+        cands = [lo, np.nextafter(lo, np.float32(np.inf)), np.nextafter(lo, np.float32(-np.inf))]
+        best = min(cands, key=lambda c: (abs(Fraction(float(c)) - v), int(np.float32(c).view(np.uint32)) & 1))
+        return np.float32(best)
+    return np.float32(v)
+
+
+def fma32(a, b, c) -> np.float32:
+    """fmaf: a*b + c computed exactly, rounded once to f32."""
+    return f32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+
+
+# ------------------------------------------------------------------ 1
+
+
+@pytest.mark.parametrize("sc", range(64))
+def test_fp16_bias_trick_is_exact(sc):
+    for q in range(16):
+        # low nibble: (1024+q)*sc - 1024*sc
+        a, b, c = 1024 + q, sc, -1024 * sc
+        assert f16_exact(a) and f16_exact(b) and f16_exact(c)
+        exact = Fraction(a) * b + c
+        assert exact == sc * q and f16_exact(exact)
+        # high nibble: the byte's high nibble is kept in place, (1024+16q)*(sc/16) - 64*sc
+        a, b, c = 1024 + 16 * q, Fraction(sc, 16), -64 * sc
+        assert f16_exact(a) and f16_exact(b) and f16_exact(c)
+        exact = Fraction(a) * b + c
+        assert exact == sc * q and f16_exact(exact)
+
+
+# ------------------------------------------------------------------ 2
+
+
+def test_x_hi_lo_split_residual_and_exact_products():
+    g = np.random.default_rng(60)
+    x = np.concatenate([g.normal(0, 1, 4000), g.normal(0, 1e-3, 1000), g.normal(0, 30, 1000)]).astype(np.float32)
+    x_hi = x.astype(np.float16)
+    x_lo = (x - x_hi.astype(np.float32)).astype(np.float16)
+    for xi, h, l in zip(x[:2000], x_hi[:2000], x_lo[:2000]):
+        res = abs(Fraction(float(xi)) - Fraction(float(h)) - Fraction(float(l)))
+        assert res <= Fraction(abs(float(xi))) / 2 ** 21 + Fraction(1, 2 ** 25)
+        for scq in (1, 7, 945):
+            # fp16 * fp16 with |sc*q| <= 945: at most 10 + 11 significant bits
+            for part in (h, l):
+                p = Fraction(scq) * Fraction(float(part))
+                assert Fraction(float(np.float32(float(p)))) == p
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+def test_x_hi_lo_range_limits():
+    # the largest x the pair holds, and the first one it cannot
+    assert np.isfinite(np.float16(np.float32(65519.0)))
+    assert np.isinf(np.float16(np.float32(65520.0)))
+    # below the smallest fp16 subnormal (2^-24) half-way point, x is lost
+    tiny = np.float32(2.0 ** -26)
+    hi = np.float16(tiny)
+    assert float(hi) == 0.0 and float(np.float16(tiny - np.float32(hi))) == 0.0
+
+
+# ------------------------------------------------------------------ 3
+
+K_MAGIC = np.float32(12582912.0)   # 1.5 * 2^23
+
+
+def limbs(v: np.ndarray):
+    """The batch-1 conversion of one 256-value block, step by step in f32."""
+    amax = np.float32(np.max(np.abs(v)))
+    s = np.float32(amax * np.float32(1.0 / 127.0))
+    rcp = np.float32(1.0) / amax if amax > np.float32(1e-30) else np.float32(0.0)
+    inv = np.float32(np.float32(127.0) * rcp)
+    inv2 = np.float32(np.float32(254.0 * 127.0) * rcp)
+    hi, lo = [], []
+    for x in v:
+        t = fma32(x, inv, K_MAGIC)
+        h = np.float32(t - K_MAGIC)                       # exact
+        r = fma32(-s, h, x)
+        tl = fma32(r, inv2, K_MAGIC)
+        hi.append(int(np.float32(t - K_MAGIC)))
+        lo.append(int(np.float32(tl - K_MAGIC)))
+        assert float(h) == hi[-1]
+    return np.array(hi), np.array(lo), s, amax
+
+
+@pytest.mark.parametrize("case", ["normal", "wide", "edge", "tiny", "spiky"])
+def test_int8_limbs_stay_in_range_and_meet_the_bound(case):
+    g = np.random.default_rng({"normal": 61, "wide": 62, "edge": 63, "tiny": 64, "spiky": 65}[case])
+    for _ in range(12):
+        if case == "normal":
+            v = g.normal(0, 1, 256)
+        elif case == "wide":
+            v = g.normal(0, 1, 256) * 10.0 ** g.uniform(-6, 6, 256)
+        elif case == "edge":
+            amax = g.uniform(0.5, 2.0)
+            v = g.choice([-1, 1], 256) * amax * (np.arange(256) % 128) / 127.0
+            v[0] = amax                                    # exact multiples of s and the extremes
+        elif case == "tiny":
+            v = g.normal(0, 1e-20, 256)
+        else:
+            v = g.normal(0, 1e-3, 256)
+            v[g.integers(0, 256)] = 5.0                    # one large value sets the scale
+        v = v.astype(np.float32)
+        hi, lo, s, amax = limbs(v)
+        # no clamp needed: both limbs are int8 values
+        assert np.all(np.abs(hi) <= 127) and np.all(np.abs(lo) <= 127), (case, hi.max(), lo.max())
+        u = Fraction(float(s)) / 254
+        for x, h, l in zip(v, hi, lo):
+            err = abs(Fraction(float(x)) - u * (254 * int(h) + int(l)))
+            assert err <= Fraction(float(amax)) / 64516 * Fraction(1001, 1000) + Fraction(1, 2 ** 140)
