@@ -90,6 +90,12 @@ def lib():
             L.pqo_quantize.restype = i32
             L.pqo_threads.argtypes = [i32]
             L.pqo_threads.restype = i32
+            L.pqo_silu.argtypes = [ctypes.c_double]
+            L.pqo_silu.restype = ctypes.c_double
+            L.pqo_gemv_swiglu.argtypes = [i32, vp, i64, i64, vp, i64, vp, i32]
+            L.pqo_gemv_swiglu.restype = i32
+            L.pqo_gemv_bias.argtypes = [i32, vp, i64, i64, vp, i64, vp, vp, i32]
+            L.pqo_gemv_bias.restype = i32
             _lib = L
     return _lib
 
@@ -197,6 +203,38 @@ def gemv_rows(fmt, w: np.ndarray, n_out: int, k: int, x: np.ndarray,
                              _ptr(rows), rows.size, _ptr(y), nthreads)
     if rc:
         raise RuntimeError(f"pqo_gemv_rows failed ({rc})")
+    return y
+
+
+def silu(z: float) -> float:
+    return float(lib().pqo_silu(float(z)))
+
+
+def gemv_swiglu(fmt, w: np.ndarray, n_ff: int, k: int, x: np.ndarray,
+                nthreads: int = 0) -> np.ndarray:
+    """h[b, j] = silu((W x_b)[j]) * (W x_b)[n_ff + j] for a fused gate+up W of
+    2*n_ff rows, in f64; [batch, n_ff]."""
+    w = _check_w(fmt, w, 2 * n_ff, k)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    h = np.empty((x.shape[0], n_ff), dtype=np.float64)
+    rc = lib().pqo_gemv_swiglu(_fmt(fmt), _ptr(w), n_ff, k, _ptr(x), x.shape[0], _ptr(h), nthreads)
+    if rc:
+        raise RuntimeError(f"pqo_gemv_swiglu failed ({rc})")
+    return h
+
+
+def gemv_bias(fmt, w: np.ndarray, n_out: int, k: int, x: np.ndarray, bias: np.ndarray,
+              nthreads: int = 0) -> np.ndarray:
+    """y[b, r] = (W x_b)[r] + bias[r] in f64; [batch, n_out]."""
+    w = _check_w(fmt, w, n_out, k)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    bias = np.ascontiguousarray(bias, dtype=np.float32)
+    assert bias.shape == (n_out,)
+    y = np.empty((x.shape[0], n_out), dtype=np.float64)
+    rc = lib().pqo_gemv_bias(_fmt(fmt), _ptr(w), n_out, k, _ptr(x), x.shape[0], _ptr(bias), _ptr(y),
+                             nthreads)
+    if rc:
+        raise RuntimeError(f"pqo_gemv_bias failed ({rc})")
     return y
 
 

@@ -478,6 +478,56 @@ int pqo_gemv(int fmt, const uint8_t *W, int64_t n_out, int64_t k,
 }
 
 /* ------------------------------------------------------------------ */
+/* Epilogues on the decode-layer mat-vecs                              */
+/* ------------------------------------------------------------------ */
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z), in f64 (the PESTI README,
+ * "Conformance": the MLP's SwiGLU multiplies the sigmoid-based silu of the
+ * gate projection by the up projection).  Written as z / (1 + exp(-z)) for z >= 0 and as
+ * z * e^z / (1 + e^z) for z < 0, so that neither form overflows. */
+double pqo_silu(double z)
+{
+    if (z >= 0.0)
+        return z / (1.0 + exp(-z));
+    double e = exp(z);
+    return z * e / (1.0 + e);
+}
+
+/* SwiGLU on a fused gate+up matrix: W has 2*n_ff rows, rows [0, n_ff) the
+ * gate projection and rows [n_ff, 2*n_ff) the up projection (the order the
+ * name gate+up gives).  h[b][j] = silu(g) * u with g, u the f64 mat-vec rows
+ * j and n_ff + j.  h is [batch][n_ff]. */
+int pqo_gemv_swiglu(int fmt, const uint8_t *W, int64_t n_ff, int64_t k,
+                    const float *x, int64_t batch, double *h, int nthreads)
+{
+    double *y = (double *)malloc(sizeof(double) * (size_t)(batch * 2 * n_ff > 0 ? batch * 2 * n_ff : 1));
+    if (!y)
+        return -2;
+    int rc = pqo_gemv(fmt, W, 2 * n_ff, k, x, batch, y, nthreads);
+    if (rc == 0)
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t j = 0; j < n_ff; ++j) {
+                double g = y[b * 2 * n_ff + j], u = y[b * 2 * n_ff + n_ff + j];
+                h[b * n_ff + j] = pqo_silu(g) * u;
+            }
+    free(y);
+    return rc;
+}
+
+/* y[b][r] = (W x_b)[r] + bias[r] in f64 (the PESTI README, "Conformance":
+ * the QKV projections carry a bias). */
+int pqo_gemv_bias(int fmt, const uint8_t *W, int64_t n_out, int64_t k,
+                  const float *x, int64_t batch, const float *bias, double *y, int nthreads)
+{
+    int rc = pqo_gemv(fmt, W, n_out, k, x, batch, y, nthreads);
+    if (rc == 0)
+        for (int64_t b = 0; b < batch; ++b)
+            for (int64_t r = 0; r < n_out; ++r)
+                y[b * n_out + r] += (double)bias[r];
+    return rc;
+}
+
+/* ------------------------------------------------------------------ */
 /* Quantizers (make test inputs)                                       */
 /* ------------------------------------------------------------------ */
 
