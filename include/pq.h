@@ -99,14 +99,15 @@ typedef enum {
  *
  * Accuracy: partial sums are accumulated in f32; the result agrees with the
  * exact dot product of the decoded f32 weights within
- * 2e-3 * RMS(y) + 1e-6 (see the tests).  Range of x: the tensor-core kernel
- * (Q4_K at batch >= 5, and at batch 3-4 for long rows or large matrices;
- * see pq_gemv_choice) takes x as fp16 pairs x_hi + x_lo, so it needs
- * |x| < 65504 -- larger values overflow to inf -- and resolves values below
- * 2^-14 only to 2^-25 absolutely; the other kernels scale x per 256 values
- * or use it in f32 and have neither limit.  Deterministic: repeated calls
- * with the same inputs give bit-identical y.  There is no host fallback: every step
- * runs in this library's CUDA kernels.
+ * 2e-3 * RMS(y) + 1e-6 (see the tests).  Range of x: any finite x.  Every
+ * kernel scales x per 256 values of each column before narrowing it: the
+ * batch 1-4 kernels into two int8 limbs per value, the tensor-core kernel
+ * (Q4_K at batch >= 5, and at batch 3-4 for long rows or large matrices; see
+ * pq_gemv_choice) by a power of two into an fp16 pair x_hi + x_lo; the
+ * generic kernel uses x in f32.  Non-finite x or scale fields give
+ * non-finite outputs in the rows they reach.  Deterministic: repeated calls
+ * with the same inputs give bit-identical y.  There is no host fallback:
+ * every step runs in this library's CUDA kernels.
  */
 int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k,
             const float *x, int batch, float *y, struct CUstream_st *stream);
@@ -209,19 +210,25 @@ int pq_selftest_wait_timeout(unsigned limit_us, struct CUstream_st *stream);
  * capture, where allocation calls are not permitted.  pq_gemv's tensor-core
  * path (batch >= 5) takes a small per-call buffer from a stream-ordered pool;
  * this entry runs that same kernel with the buffer in a fixed device array
- * instead (3,735,552 bytes, part of the library image: every GPU that loads
+ * instead (3,743,744 bytes, part of the library image: every GPU that loads
  * the library holds it until the process exits).
  *
- * Same arguments, layouts and accuracy as pq_gemv; limits: fmt must be PQ_Q4_K
- * (PQ_ERR_KERNEL otherwise) and k <= 16384 (PQ_ERR_SIZE otherwise); any
- * batch >= 1 (chunks of 16, run one after another on `stream`).
+ * Same arguments, layouts and accuracy bar as pq_gemv, but it runs the
+ * tensor-core kernel at every batch, 1-4 included (where pq_gemv mostly
+ * runs other kernels), so its result equals pq_gemv_kernel(...,
+ * PQ_KERNEL_TC) bit for bit.  Limits: fmt must be PQ_Q4_K (PQ_ERR_KERNEL
+ * otherwise) and k <= 16384 (PQ_ERR_SIZE otherwise); any batch >= 1 (chunks
+ * of 16, run one after another on `stream`).
  * Shared state: all calls in the process use the one array per GPU, which
  * keeps the last call's contents; each call writes every byte of it that it
  * later reads, so nothing needs clearing, but calls that overlap on the GPU
  * (different streams, or different threads) race on it and must be ordered
  * by the caller.  The first call on a device looks up the array's device
  * address (a one-time set-up with that device current); make that first call
- * before any stream capture.
+ * before any stream capture.  The address is looked up once per device
+ * ordinal, in the device's primary context (the one the CUDA runtime uses);
+ * calls made under another context, or after cudaDeviceReset, are not
+ * supported.
  */
 int pq_gemv_noalloc(pq_fmt fmt, const void *w_blocks, int n_out, int k,
                     const float *x, int batch, float *y, struct CUstream_st *stream);

@@ -8,11 +8,15 @@
 //
 // Exactness: a tile entry is the integer sc_j*q (q in 0..15, sc_j in 0..63,
 // so <= 945), exactly representable in fp16; x enters as two fp16 columns
-// (x_hi = fp16(x), x_lo = fp16(x - x_hi)), so every product is exact in the
-// f32 accumulator and only accumulation rounds.  The sub-block mins enter
-// through a second, K=16 product of the 6-bit mins with the fp16 hi/lo sums of
-// x over each 32-element sub-block.  Per super-block and row the epilogue forms
-// y += d*(A.x) - dmin*(m.XS) in f32.
+// (x_hi = fp16(x'), x_lo = fp16(x' - x_hi)) of x' = 2^e * x, where the power
+// of two e is chosen per super-block and column so that max|x'| lies in
+// [2^9, 2^10): every x' and every sum of 32 of them fits fp16's range, for
+// any finite x.  Every product is exact in the f32 accumulator and only
+// accumulation rounds.  The sub-block mins enter through a second, K=16
+// product of the 6-bit mins with the fp16 hi/lo sums of x' over each
+// 32-element sub-block.  Per super-block, row and column the epilogue forms
+// y += 2^-e * (d*(A.x') - dmin*(m.XS')) in f32 (multiplying by 2^-e is
+// exact).
 //
 // Work split: the (128-row tile, super-block) items of the matrix, in
 // tile-major order, are cut into one contiguous, equal-sized range per CTA
@@ -76,10 +80,14 @@ constexpr int kMaxGrid = 160;                 // CTAs at most (partial-sum slots
 // x image of one super-block for NBP columns (N' = 2*NBP MMA columns, the hi
 // parts then the lo parts): N' x 256 fp16, K-major 8x8 core matrices, 8-row
 // groups 4096 bytes apart; then the mins operand N' x 16 fp16 (K = j < 8: the
-// hi or lo part of the sum of x over sub-block j; K = 8..15: zero), 8-row
-// groups 256 bytes apart.
+// hi or lo part of the sum of x' over sub-block j; K = 8..15: zero), 8-row
+// groups 256 bytes apart; then 128 bytes holding, per column, the f32 factor
+// 2^-e that undoes the column's scale.
 template <int NBP> __host__ __device__ constexpr int xmain_bytes() { return 2 * NBP * 256 * 2; }
-template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xmain_bytes<NBP>() + 2 * NBP * 16 * 2; }
+template <int NBP> __host__ __device__ constexpr int xmins_bytes() { return 2 * NBP * 16 * 2; }
+template <int NBP> __host__ __device__ constexpr int xscale_off() { return xmain_bytes<NBP>() + xmins_bytes<NBP>(); }
+template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xscale_off<NBP>() + 128; }
+static_assert(16 * 4 <= 128, "one f32 factor per column fits the scale area");
 template <int NBP> __host__ __device__ constexpr int raw_stages() { return NBP == 16 ? 6 : 8; }
 template <int NBP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NBP>(); }
 template <int NBP> __host__ __device__ constexpr int smem_bytes() { return raw_stages<NBP>() * stage_bytes<NBP>() + 1024; }
@@ -115,6 +123,21 @@ __host__ __device__ constexpr int kmaj_off(int n, int K, int sbo) {
 // kernel launch, so that the weights the main kernel starts streaming at once
 // are complete even when the previous kernel wrote them; the main kernel waits
 // for this one only before its first x tile.
+//
+// Scale of column b: with E the binary exponent of m = max|x| over the
+// super-block's 256 values of the column (m in [2^E, 2^(E+1))), x' = 2^e * x
+// with e = 9 - E, capped at 126 so that 2^e and 2^-e are normal f32 numbers
+// (a cap that only applies when m < 2^-117); e = 0 when m is 0, inf or NaN
+// (non-finite values then reach y as they would unscaled).  Scaling by a power
+// of two is exact, so x' = x_hi + x_lo holds x to a relative 2^-21 plus an
+// absolute 2^-25 in scaled units, i.e. about 2^-34 of the column's maximum.
+__device__ __forceinline__ int tc_scale_exponent(uint32_t max_abs_bits) {
+    const int eb = (int)(max_abs_bits >> 23);           // biased exponent; 0 for zero and subnormals
+    if (max_abs_bits == 0u || eb == 255) return 0;
+    const int e = 9 - ((eb > 0 ? eb : 1) - 127);
+    return e < 126 ? e : 126;
+}
+
 template <int NBP>
 __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, int k, int nb_cols,
                                                  uint8_t *__restrict__ img) {
@@ -125,46 +148,71 @@ __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, in
     uint8_t *tile = img + (size_t)sb * btile_bytes<NBP>();
     __half *out = reinterpret_cast<__half *>(tile);
     __half *om = reinterpret_cast<__half *>(tile + xmain_bytes<NBP>());
+    float *undo = reinterpret_cast<float *>(tile + xscale_off<NBP>());
+    __shared__ uint32_t wmax[8][NBP];
+    __shared__ float mult[NBP];
     __shared__ float xs[NBP][8];
-    const int t = threadIdx.x;
-    // sub-block sums, fixed order (thread per (column, sub-block), 8 vector loads)
-    if (t < NBP * 8) {
-        const int b = t / 8, j = t % 8;
-        float s = 0.f;
-        if (b < nb_cols) {
-            const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)b * k + sb * 256 + 32 * j);
-            float4 v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldg(xb + i);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s = s + v[i].x + v[i].y + v[i].z + v[i].w;
-        }
-        xs[b][j] = s;
-    }
-    __syncthreads();
-    // mins operand: K = j < 8 holds the sums (hi part for n < NBP, lo part after), K = 8..15 zero
-    for (int i = t; i < NP * 16; i += 256) {
-        const int n = i / 16, K = i % 16;
-        float v = 0.f;
-        if (K < 8) {
-            const float s = xs[n % NBP][K];
-            const __half hi = __float2half_rn(s);
-            v = n < NBP ? __half2float(hi) : __half2float(__float2half_rn(s - __half2float(hi)));
-        }
-        om[kmaj_off(n, K, 256) / 2] = __float2half_rn(v);
-    }
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     // main part: thread t = K index; all column loads in flight together
     const int K = t;
     const int pos = kpos(K / 8, K % 8);
     float v[NBP];
 #pragma unroll
     for (int b = 0; b < NBP; ++b) v[b] = b < nb_cols ? __ldg(x + (size_t)b * k + sb * 256 + pos) : 0.f;
+    // sub-block sums: thread (column, sub-block) for t < NBP * 8, 8 vector loads
+    const int sbc = t / 8, sbj = t % 8;
+    float4 sv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < NBP * 8 && sbc < nb_cols) {
+        const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)sbc * k + sb * 256 + 32 * sbj);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sv[i] = __ldg(xb + i);
+    }
+    // max |x| per column: the bit patterns of non-negative floats order like
+    // their values (NaN above inf), so an integer reduction gives it
 #pragma unroll
     for (int b = 0; b < NBP; ++b) {
-        const __half hi = __float2half_rn(v[b]);
-        const __half lo = __float2half_rn(v[b] - __half2float(hi));
+        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(v[b]) & 0x7fffffffu);
+        if (lane == 0) wmax[warp][b] = m;
+    }
+    __syncthreads();
+    if (t < NBP) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = max(m, wmax[w][t]);
+        const int e = tc_scale_exponent(m);
+        mult[t] = __uint_as_float((uint32_t)(127 + e) << 23);    // 2^e
+        undo[t] = __uint_as_float((uint32_t)(127 - e) << 23);    // 2^-e
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) {
+        const float s = v[b] * mult[b];
+        const __half hi = __float2half_rn(s);
+        const __half lo = __float2half_rn(s - __half2float(hi));
         out[kmaj_off(b, K, 4096) / 2] = hi;
         out[kmaj_off(NBP + b, K, 4096) / 2] = lo;
+    }
+    if (t < NBP * 8) {
+        // fixed order; |x'| < 2^10, so |sum| < 2^15 stays in fp16's range
+        const float m = mult[sbc];
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = s + sv[i].x * m + sv[i].y * m + sv[i].z * m + sv[i].w * m;
+        xs[sbc][sbj] = s;
+    }
+    __syncthreads();
+    // mins operand: K = j < 8 holds the sums (hi part for n < NBP, lo part after), K = 8..15 zero
+    for (int i = t; i < NP * 16; i += 256) {
+        const int n = i / 16, Kk = i % 16;
+        float val = 0.f;
+        if (Kk < 8) {
+            const float s = xs[n % NBP][Kk];
+            const __half hi = __float2half_rn(s);
+            val = n < NBP ? __half2float(hi) : __half2float(__float2half_rn(s - __half2float(hi)));
+        }
+        om[kmaj_off(n, Kk, 256) / 2] = __float2half_rn(val);
     }
 }
 
@@ -430,31 +478,44 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!dead && !mbar_wait(&item_done[buf], par)) dead = true;
             tc_fence_after();
             const uint32_t dd = *reinterpret_cast<const uint32_t *>(st + r * 144);
+            // lane b < NBP keeps column b's factor 2^-e (read before the stage is freed)
+            const float undo = *reinterpret_cast<const float *>(st + RAW_BYTES + xscale_off<NBP>() + 4 * (lane % NBP));
             __syncwarp();
             if (lane == 0) mbar_arrive(&raw_empty[slot]);
             const float d = h2f(dd), dmin = h2f(dd >> 16);
             // the super-block's three accumulators (two halves of the products,
-            // the mins product), each with hi and lo x columns
+            // the mins product), each with hi and lo x columns, in scaled units
+            float v[NBP];
 #pragma unroll
             for (int part = 0; part < 3; ++part) {
                 const uint32_t taddr = row_taddr + (uint32_t)((3 * buf + part) * NP);
                 const float sc = part < 2 ? d : -dmin;
                 if constexpr (NP == 32) {
-                    uint32_t t[32];
-                    tmem_ld32(taddr, t);
-                    tmem_ld_wait(t);
+                    // hi columns, then lo columns: 16 registers at a time (the
+                    // 800-thread block leaves 72 registers per thread)
 #pragma unroll
-                    for (int b = 0; b < NBP; ++b)
-                        yacc[b] = fmaf(sc, __uint_as_float(t[b]) + __uint_as_float(t[NBP + b]), yacc[b]);
+                    for (int hl = 0; hl < 2; ++hl) {
+                        uint32_t t[16];
+                        tmem_ld16(taddr + (uint32_t)(16 * hl), t);
+                        tmem_ld_wait(t);
+#pragma unroll
+                        for (int b = 0; b < NBP; ++b)
+                            v[b] = (part == 0 && hl == 0) ? sc * __uint_as_float(t[b])
+                                                          : fmaf(sc, __uint_as_float(t[b]), v[b]);
+                    }
                 } else {
                     uint32_t t[16];
                     tmem_ld16(taddr, t);
                     tmem_ld_wait(t);
 #pragma unroll
-                    for (int b = 0; b < NBP; ++b)
-                        yacc[b] = fmaf(sc, __uint_as_float(t[b]) + __uint_as_float(t[NBP + b]), yacc[b]);
+                    for (int b = 0; b < NBP; ++b) {
+                        const float pr = __uint_as_float(t[b]) + __uint_as_float(t[NBP + b]);
+                        v[b] = part == 0 ? sc * pr : fmaf(sc, pr, v[b]);
+                    }
                 }
             }
+#pragma unroll
+            for (int b = 0; b < NBP; ++b) yacc[b] = fmaf(v[b], __shfl_sync(0xffffffffu, undo, b), yacc[b]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -721,14 +782,14 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
 
 // Fixed scratch for the allocation-free entry point (pq_gemv_noalloc): x image
 // for k up to kNoAllocMaxK at up to 16 columns and split-K partial sums for up
-// to kMaxGrid CTAs: 3,735,552 bytes.  Every GPU that loads
+// to kMaxGrid CTAs: 3,743,744 bytes.  Every GPU that loads
 // this library keeps it until the process exits.  In host code the name is
 // only a stand-in for the device array; its device address comes from
 // cudaGetSymbolAddress, once per device.
 constexpr int kNoAllocMaxK = 16384;
 constexpr size_t kNoAllocScratchBytes =
     (size_t)(kNoAllocMaxK / 256) * (size_t)btile_bytes<16>() + (size_t)kMaxGrid * 2 * 16 * TM * 4;
-static_assert(kNoAllocScratchBytes == 3735552, "stated size");
+static_assert(kNoAllocScratchBytes == 3743744, "stated size");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 uint8_t *noalloc_scratch_ptr() {

@@ -17,6 +17,10 @@ Generators (numpy PCG64 via ``default_rng``):
   the fp16 scale fields, which get finite positive values from a stated
   range: every bit pattern of the packed scales, mins and codes occurs, so
   decoders see all of them.
+* ``special_scale_records``  the same, but the scale fields (fp16 d/dmin, or
+  the f32 row scales of the per-row formats) take every IEEE class: positive
+  and negative normals, subnormals, signed zeros and, at a stated rate,
+  infinities and NaNs (quiet and signalling, random payloads).
 
 Byte offsets of the fp16 fields (the only layout facts used here):
 Q8_0 d @0; Q4_K d @0, dmin @2; Q6_K d @208; Q5_K d @0, dmin @2; Q3_K d @108;
@@ -111,4 +115,59 @@ def random_records(fmt: str, n_out: int, k: int, seed: int,
     elif fmt == "q2_k":
         rec[:, 80:82] = _f16_field(g, nblk, *d_range)
         rec[:, 82:84] = _f16_field(g, nblk, *dmin_range)
+    return rec.reshape(-1)
+
+
+# fp16 / f32 scale fields of each record format: (offset, kind) per block, or
+# the per-row f32 scales of the per-row formats
+_SCALE_FIELDS = {"q8_0": (0,), "q4_k": (0, 2), "q6_k": (208,), "q5_k": (0, 2),
+                 "q3_k": (108,), "q2_k": (80, 82)}
+
+
+def _f16_class_bits(g: np.random.Generator, n: int, nonfinite: float) -> np.ndarray:
+    """n fp16 bit patterns: finite classes (normal with exponent field 1..11,
+    i.e. |v| in [2^-14, 2^-3), subnormal, zero; either sign) and, with
+    probability `nonfinite`, +-inf or a NaN."""
+    sign = g.integers(0, 2, n).astype(np.uint16) << 15
+    cls = g.choice(3, size=n, p=[0.7, 0.2, 0.1])                # normal, subnormal, zero
+    exp = np.where(cls == 0, g.integers(1, 12, n), 0).astype(np.uint16)
+    man = np.where(cls == 2, 0, g.integers(0, 1024, n)).astype(np.uint16)
+    man = np.where((cls == 1) & (man == 0), 1, man).astype(np.uint16)
+    bits = sign | (exp << 10) | man
+    bad = g.random(n) < nonfinite
+    nan = g.random(n) < 0.5
+    payload = g.integers(1, 1024, n).astype(np.uint16)
+    special = sign | np.uint16(0x7C00) | np.where(nan, payload, 0).astype(np.uint16)
+    return np.where(bad, special, bits).astype(np.uint16)
+
+
+def _f32_class_bits(g: np.random.Generator, n: int, nonfinite: float) -> np.ndarray:
+    sign = g.integers(0, 2, n).astype(np.uint32) << 31
+    cls = g.choice(3, size=n, p=[0.7, 0.2, 0.1])
+    exp = np.where(cls == 0, g.integers(100, 121, n), 0).astype(np.uint32)
+    man = np.where(cls == 2, 0, g.integers(0, 1 << 23, n)).astype(np.uint32)
+    man = np.where((cls == 1) & (man == 0), 1, man).astype(np.uint32)
+    bits = sign | (exp << 23) | man
+    bad = g.random(n) < nonfinite
+    nan = g.random(n) < 0.5
+    payload = g.integers(1, 1 << 23, n).astype(np.uint32)
+    special = sign | np.uint32(0x7F800000) | np.where(nan, payload, 0).astype(np.uint32)
+    return np.where(bad, special, bits).astype(np.uint32)
+
+
+def special_scale_records(fmt: str, n_out: int, k: int, seed: int, nonfinite: float = 0.05) -> np.ndarray:
+    """Uniform random bytes whose scale fields take every IEEE class; each
+    scale field is non-finite with probability `nonfinite`."""
+    g = rng(seed)
+    if fmt in ("i8_row", "i4_row"):
+        buf = random_records(fmt, n_out, k, seed)
+        nq = n_out * k if fmt == "i8_row" else n_out * k // 2
+        soff = (nq + 15) // 16 * 16
+        buf[soff: soff + 4 * n_out] = _f32_class_bits(g, n_out, nonfinite).astype("<u4").view(np.uint8)
+        return buf
+    qk, bb = BLOCK[fmt]
+    nblk = n_out * (k // qk)
+    rec = random_records(fmt, n_out, k, seed).reshape(nblk, bb).copy()
+    for off in _SCALE_FIELDS[fmt]:
+        rec[:, off:off + 2] = _f16_class_bits(g, nblk, nonfinite).astype("<u2").view(np.uint8).reshape(nblk, 2)
     return rec.reshape(-1)

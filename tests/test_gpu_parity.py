@@ -9,13 +9,10 @@ import pytest
 
 import oracle
 import quantized_weight_mat_gb300 as pq
+from gpuio import dev, guard_intact, out_buf, run_gemv
 from pqcases import tolerance_ok, weights, x_for
 
 pytestmark = pytest.mark.gpu
-
-GUARD = 64
-SENTINEL = np.float32(np.frombuffer(np.uint32(0x7fc0beef).tobytes(), dtype=np.float32)[0])
-
 
 @pytest.fixture(scope="module", autouse=True)
 def setup(cuda_ok):
@@ -23,37 +20,6 @@ def setup(cuda_ok):
     build.build()
     import torch
     torch.cuda.init()
-
-
-def dev(a):
-    import torch
-    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-
-def out_buf(n):
-    import torch
-    t = torch.empty(n + GUARD, dtype=torch.float32, device="cuda")
-    t.fill_(float(SENTINEL))
-    return t
-
-
-def guard_intact(t, n):
-    g = t[n:].cpu().numpy().view(np.uint32)
-    return bool(np.all(g == np.uint32(0x7fc0beef)))
-
-
-def run_gemv(fmt, w, n_out, k, x, kernel="auto"):
-    import torch
-    batch = x.shape[0]
-    wd, xd = dev(w), dev(x)
-    y = out_buf(batch * n_out)
-    st = pq.pq_gemv_kernel(fmt, wd, n_out, k, xd, batch, y, kernel=kernel, check=False)
-    torch.cuda.synchronize()
-    if st == pq.PQ_ERR_KERNEL:
-        return None
-    assert st == 0, pq.pq_strerror(st)
-    assert guard_intact(y, batch * n_out)
-    return y[: batch * n_out].cpu().numpy().reshape(batch, n_out)
 
 
 # ------------------------------------------------------------------ dequant

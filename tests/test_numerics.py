@@ -5,11 +5,14 @@
    - 1024*sc for low nibbles and (1024+16q)*(sc/16) - 64*sc for high nibbles.
    Every operand is an exact fp16 value and the exact result sc*q <= 945 is
    an fp16 integer, so the single rounding of the fused operation is exact.
-2. Tensor-core x operand: x = x_hi + x_lo with x_hi = fp16(x) and x_lo =
-   fp16(x - x_hi) leaves a residual of at most 2^-21 |x| + 2^-25 (x_lo turns
-   subnormal below 2^-14, where fp16 has a fixed step of 2^-24), and it
-   holds only for |x| < 65520, above which x_hi overflows; every product
-   (sc*q) * x_hi and (sc*q) * x_lo is exact in the f32 accumulator.
+2. Tensor-core x operand: x' = x_hi + x_lo with x_hi = fp16(x') and x_lo =
+   fp16(x' - x_hi) leaves a residual of at most 2^-21 |x'| + 2^-25 (x_lo turns
+   subnormal below 2^-14, where fp16 has a fixed step of 2^-24); every
+   product (sc*q) * x_hi and (sc*q) * x_lo is exact in the f32 accumulator.
+   The pair alone overflows at |x'| >= 65520, so x' = 2^e * x is first scaled
+   per super-block and column by a power of two chosen from the column's
+   maximum: every x' and every sum of 32 of them then stays inside fp16's
+   range for any finite x, and 2^e and 2^-e are normal f32 numbers.
 3. Batch-1 x limbs: per 256 values, x ~= u*(254*xh + xl) with int8 limbs
    made by the 1.5*2^23 round-to-nearest shift.  Both limbs stay in
    [-127, 127] without any clamp (the kernel relies on it), and the error is
@@ -17,6 +20,7 @@
 The emulation rounds each step exactly as the kernel does: fused operations
 are computed exactly with rationals and rounded once to f32.
 """
+import zlib
 from fractions import Fraction
 
 import numpy as np
@@ -86,13 +90,102 @@ def test_x_hi_lo_split_residual_and_exact_products():
 
 @pytest.mark.filterwarnings("ignore::RuntimeWarning")
 def test_x_hi_lo_range_limits():
-    # the largest x the pair holds, and the first one it cannot
+    # the largest value the bare pair holds, and the first one it cannot: the
+    # reason x is scaled before the split
     assert np.isfinite(np.float16(np.float32(65519.0)))
     assert np.isinf(np.float16(np.float32(65520.0)))
     # below the smallest fp16 subnormal (2^-24) half-way point, x is lost
     tiny = np.float32(2.0 ** -26)
     hi = np.float16(tiny)
     assert float(hi) == 0.0 and float(np.float16(tiny - np.float32(hi))) == 0.0
+
+
+def tc_scale_exponent(max_abs_bits: int) -> int:
+    """The tensor-core x prep's choice of e from the bits of max|x| (sign
+    cleared): e = 9 - E for max|x| in [2^E, 2^(E+1)), at most 126; 0 for a
+    zero, infinite or NaN maximum."""
+    eb = max_abs_bits >> 23
+    if max_abs_bits == 0 or eb == 255:
+        return 0
+    return min(9 - (max(eb, 1) - 127), 126)
+
+
+def pow2_f32(e: int) -> np.float32:
+    """2^e built from its bit pattern, as the kernel does (e + 127 in 1..254)."""
+    assert 1 <= e + 127 <= 254
+    return np.array([(e + 127) << 23], dtype=np.uint32).view(np.float32)[0]
+
+
+def tc_columns(case: str, g: np.random.Generator) -> np.ndarray:
+    if case == "normal":
+        return g.normal(0, 1, 256)
+    if case == "huge":
+        return g.normal(0, 1, 256) * 1e30
+    if case == "large":
+        return g.uniform(-1e6, 1e6, 256)
+    if case == "tiny":
+        return g.normal(0, 1e-30, 256)
+    if case == "denormal":
+        return g.normal(0, 1e-39, 256)
+    if case == "wide":
+        return g.normal(0, 1, 256) * 10.0 ** g.uniform(-30, 30, 256)
+    if case == "spike":
+        v = g.normal(0, 1e-3, 256)
+        v[g.integers(0, 256)] = 3.0e38
+        return v
+    if case == "max":
+        return np.full(256, 3.4e38) * g.choice([-1, 1], 256)
+    if case == "zero":
+        return np.zeros(256)
+    raise ValueError(case)
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("case", ["normal", "huge", "large", "tiny", "denormal", "wide", "spike", "max", "zero"])
+def test_tc_x_scale_keeps_the_pair_and_sums_in_range(case):
+    g = np.random.default_rng(zlib.crc32(case.encode()))
+    for _ in range(8):
+        v = tc_columns(case, g).astype(np.float32)
+        m = int((v.view(np.uint32) & np.uint32(0x7FFFFFFF)).max())
+        e = tc_scale_exponent(m)
+        mult, undo = pow2_f32(e), pow2_f32(-e)
+        assert float(mult) * float(undo) == 1.0                       # both normal, exact inverses
+        xs = (v * mult).astype(np.float32)
+        amax = float(np.max(np.abs(xs)))
+        assert amax < 2.0 ** 10
+        if m and 1 <= (m >> 23) and 9 - ((m >> 23) - 127) <= 126:
+            assert amax >= 2.0 ** 9                                   # no cap: the max lands in [2^9, 2^10)
+        # scaling by 2^e is exact wherever the result stays a normal f32
+        normal = np.abs(xs) >= np.float32(2.0 ** -126)
+        assert np.array_equal((xs[normal].astype(np.float64) / float(mult)), v[normal].astype(np.float64))
+        hi = xs.astype(np.float16)
+        lo = (xs - hi.astype(np.float32)).astype(np.float16)
+        assert np.all(np.isfinite(hi)) and np.all(np.isfinite(lo))
+        for x, h, l in zip(xs[:64], hi[:64], lo[:64]):
+            res = abs(Fraction(float(x)) - Fraction(float(h)) - Fraction(float(l)))
+            assert res <= Fraction(abs(float(x))) / 2 ** 21 + Fraction(1, 2 ** 25)
+        # the eight 32-value sub-block sums (fixed order, f32) and their pairs
+        for j in range(8):
+            s = np.float32(0.0)
+            for val in xs[32 * j:32 * j + 32]:
+                s = np.float32(s + val)
+            assert abs(float(s)) < 2.0 ** 15 < 65504.0
+            sh = np.float16(s)
+            assert np.isfinite(sh) and np.isfinite(np.float16(s - np.float32(sh)))
+
+
+def test_tc_x_scale_exponent_edges():
+    bits = lambda f: int(np.float32(f).view(np.uint32))
+    assert tc_scale_exponent(bits(1.0)) == 9             # 1 -> 512
+    assert tc_scale_exponent(bits(1023.9)) == 0          # already in [2^9, 2^10)
+    assert tc_scale_exponent(bits(512.0)) == 0
+    assert tc_scale_exponent(bits(1024.0)) == -1
+    assert tc_scale_exponent(bits(3.4e38)) == 9 - 127
+    assert tc_scale_exponent(bits(1e-38)) == 126         # capped: 2^126 and 2^-126 stay normal
+    assert tc_scale_exponent(1) == 126                   # smallest subnormal
+    assert tc_scale_exponent(0) == 0
+    assert tc_scale_exponent(0x7F800000) == 0            # inf: no scaling
+    assert tc_scale_exponent(0x7FC00000) == 0            # NaN: no scaling
 
 
 # ------------------------------------------------------------------ 3
