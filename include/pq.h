@@ -113,6 +113,39 @@ int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k,
             const float *x, int batch, float *y, struct CUstream_st *stream);
 
 /*
+ * Mat-vec with the bias add fused into the store (the PESTI README,
+ * "Conformance", lists a bias on the QKV projections):
+ *   y[b][r] = sum_i w(r, i) * x[b][i] + bias[r]
+ *   bias  device f32 [n_out], 4-byte aligned, read only; must not overlap y.
+ * Other arguments, layouts, errors and the accuracy bar as pq_gemv (the bias
+ * is added in f32 to the f32 sum).  The batch-1 kernel (Q4_K, Q6_K) and the
+ * tensor-core kernel add it at their final store; the other kernels store y
+ * and one small kernel adds the bias after them.
+ */
+int pq_gemv_bias(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
+                 const float *bias, float *y, struct CUstream_st *stream);
+
+/*
+ * SwiGLU on a fused gate+up matrix (the PESTI README, "Conformance": the MLP
+ * multiplies the sigmoid-based silu of the gate projection by the up
+ * projection):
+ *   h[b][j] = silu(g) * u,  g = sum_i w(j, i) * x[b][i],
+ *                           u = sum_i w(n_ff + j, i) * x[b][i],
+ *   silu(z) = z / (1 + e^-z)
+ *   w_blocks  2 * n_ff rows in the layout above: the n_ff gate rows, then the
+ *             n_ff up rows; 16-byte aligned, read only.
+ *   h         device f32 [batch][n_ff] row-major, 4-byte aligned, fully
+ *             overwritten; must not overlap w_blocks or x.
+ * Accuracy: within 2e-3 * RMS(h) + 1e-6 of silu(g) * u on the exact sums.
+ * The batch-1 kernel (Q4_K, Q6_K) reduces each gate row and its up row in
+ * the same warp and stores only h; the tensor-core kernel pairs gate and up
+ * tiles in its finishing kernel; the other kernels write the 2 * n_ff sums to
+ * pool memory and one small kernel forms h.  Status codes as pq_gemv.
+ */
+int pq_gemv_swiglu(pq_fmt fmt, const void *w_blocks, int n_ff, int k, const float *x, int batch,
+                   float *h, struct CUstream_st *stream);
+
+/*
  * out[r][i] = w(r, i) as f32, row-major [n_out][k], bit-identical to the
  * layout rules above (one f32 rounding for Q4_K's final subtraction and for
  * PQ_I8_ROW's product; every other step is exact).

@@ -28,7 +28,8 @@ LIB_PATH = os.environ.get("PQ_LIB_PATH") or os.path.join(
     os.path.dirname(os.path.abspath(__file__)), "libpq.so")
 EXPORTS = ("pq_gemv", "pq_dequant", "pq_weight_bytes", "pq_strerror",
            "pq_gemv_kernel", "pq_gemv_choice", "pq_gemv_launches", "pq_wait_timeouts",
-           "pq_set_weight_prefetch", "pq_gemv_noalloc", "pq_selftest_wait_timeout")
+           "pq_set_weight_prefetch", "pq_gemv_noalloc", "pq_selftest_wait_timeout",
+           "pq_gemv_bias", "pq_gemv_swiglu")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,10 @@ def lib() -> ctypes.CDLL:
             L.pq_selftest_wait_timeout.restype = i32
             L.pq_gemv_noalloc.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
             L.pq_gemv_noalloc.restype = i32
+            L.pq_gemv_bias.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp, vp]
+            L.pq_gemv_bias.restype = i32
+            L.pq_gemv_swiglu.argtypes = [i32, vp, i32, i32, vp, i32, vp, vp]
+            L.pq_gemv_swiglu.restype = i32
             L.pq_set_weight_prefetch.argtypes = [i32]
             L.pq_set_weight_prefetch.restype = i32
             _lib = L
@@ -121,6 +126,26 @@ def pq_gemv_kernel(fmt, w_blocks, n_out: int, k: int, x, batch: int, y, stream=N
                               int(batch), _addr(y), _stream(stream), kid)
     if check and st:
         raise PQError(st, "pq_gemv_kernel")
+    return st
+
+
+def pq_gemv_bias(fmt, w_blocks, n_out: int, k: int, x, batch: int, bias, y, stream=None,
+                 check: bool = True) -> int:
+    """y = W x + bias (bias [n_out], fused into the store where the kernel allows)."""
+    st = lib().pq_gemv_bias(_fmt(fmt), _addr(w_blocks), int(n_out), int(k), _addr(x), int(batch),
+                            _addr(bias), _addr(y), _stream(stream))
+    if check and st:
+        raise PQError(st, "pq_gemv_bias")
+    return st
+
+
+def pq_gemv_swiglu(fmt, w_blocks, n_ff: int, k: int, x, batch: int, h, stream=None,
+                   check: bool = True) -> int:
+    """h = silu(W_gate x) * (W_up x) for a fused gate+up W of 2 * n_ff rows (gate rows first)."""
+    st = lib().pq_gemv_swiglu(_fmt(fmt), _addr(w_blocks), int(n_ff), int(k), _addr(x), int(batch),
+                              _addr(h), _stream(stream))
+    if check and st:
+        raise PQError(st, "pq_gemv_swiglu")
     return st
 
 

@@ -396,6 +396,19 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 // weights too, unless the caller has declared weights static
 // (pq_set_weight_prefetch), in which case the producer starts streaming them
 // while the previous kernel finishes.
+//
+// x is read with ordinary loads by the consumer warps as soon as that wait
+// returns.  Data requested by an SM returns roughly in request order, so a
+// load of x issued behind the whole ring's worth of weight copies would wait
+// for all of them (several microseconds at this SM's share of the HBM
+// bandwidth).  Until the consumers have converted x, the producer therefore
+// keeps at most kXWindow stages in flight (issued, not landed); after that
+// only the ring depth limits it.  Measured per-CTA timelines (%globaltimer)
+// of 14336x4096 launched back to back: x ready 2.8 us after the wait returned
+// with the whole ring in flight ahead of it, about 1.2 us with this limit;
+// per launch 8.15 -> 7.12 us (window 2; 7.4 us with 3, 7.9 us with 4).  The
+// producer polls the consumers' signal with mbarrier.test_wait: try_wait may
+// suspend the thread, which delayed the first weight copies.
 #ifndef PQ_ROWS_CW
 #define PQ_ROWS_CW 8
 #endif
@@ -411,6 +424,10 @@ constexpr int RPG = 2;                       // rows per row group per stage
 constexpr int THREADS = (CW + 1) * 32;
 constexpr int MAX_STAGES = 8;
 constexpr int kStatic = 512;                 // reserve for the kernel's static shared memory (barriers)
+#ifndef PQ_X_WINDOW
+#define PQ_X_WINDOW 2
+#endif
+constexpr int kXWindow = PQ_X_WINDOW;        // stages in flight at most until x is converted
 
 struct Params {
     const uint8_t *w;
@@ -424,33 +441,34 @@ struct Params {
     int nstages;
     int rows_cap;   // max rows of one CTA (partials buffer, G > 1)
     int early_w;    // stream weights before waiting on the previous kernel
-    int xstage;     // x through a shared-memory copy (see x_stage_bytes)
+    int n_ff;       // SwiGLU: pairs (the matrix has 2 * n_ff rows, gate rows first)
+    const float *bias;   // bias epilogue: bias[n_out]
 };
 
 inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
-
-// With p.xstage, x arrives as an f32 copy in shared memory, fetched with one
-// bulk copy issued ahead of the weight stream (so that it does not queue
-// behind the CTA's weight copies), and is converted to the limb image from
-// there.  Without it the consumer warps read x from global memory.
-__host__ __device__ inline int x_stage_bytes(int64_t k, bool staged) { return staged ? (int)(4 * k) : 0; }
 
 inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
 
 // Stage plan for (k, n_out, grid) with super-blocks of `block_bytes`; false
 // when this kernel cannot take the shape (rows must be whole multiples of
 // 16 bytes for the bulk copy).
-inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, bool staged, Params &p) {
+// With `swiglu` the CTA's items are (gate, up) row pairs: a stage holds NG
+// gate rows, then the NG up rows of the same pairs, and n_out is 2 * pairs.
+inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p, bool swiglu = false) {
     if (k % 256 || grid < 1 || ((k / 256) * block_bytes) % 16) return false;
     const int G = segments(k);
     if (G < 1 || G > CW) return false;
     p.G = G;
     p.NG = CW / G;
     p.RS = RPG * p.NG;
-    p.rows_cap = (int)((n_out + grid - 1) / grid);
+    if (swiglu) {
+        const int64_t pairs_cap = (n_out / 2 + grid - 1) / grid;
+        p.rows_cap = (int)((pairs_cap + p.NG - 1) / p.NG * p.RS);   // stage-relative rows
+    } else {
+        p.rows_cap = (int)((n_out + grid - 1) / grid);
+    }
     const int64_t stage = (int64_t)p.RS * (k / 256) * block_bytes;
-    p.xstage = staged ? 1 : 0;
-    const int64_t avail = kRowsSmem - kStatic - x_stage_bytes(k, staged) - x_image_bytes(k, 1) - red_bytes(p);
+    const int64_t avail = kRowsSmem - kStatic - x_image_bytes(k, 1) - red_bytes(p);
     int64_t ns = avail / stage;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
     p.nstages = (int)ns;
@@ -650,20 +668,27 @@ struct Q6K {
 };
 
 // Rows gi and gi+NG of one stage (lane base address s); CHECK handles a
-// partial last stage.
+// partial last stage (v0, v1: whether each row is present).
 template <class F, bool CHECK>
 __device__ __forceinline__ void two_rows(float &p0, float &p1, uint32_t s, uint32_t rA0, uint32_t rA1,
-                                         int gi, int NG, int n, const typename F::X &X, int hf) {
+                                         bool v0, bool v1, const typename F::X &X, int hf) {
     if (!CHECK) {
         p0 = F::dot(s + rA0, X, hf);
         p1 = F::dot(s + rA1, X, hf);
     } else {
-        p0 = gi < n ? F::dot(s + rA0, X, hf) : 0.f;
-        p1 = gi + NG < n ? F::dot(s + rA1, X, hf) : 0.f;
+        p0 = v0 ? F::dot(s + rA0, X, hf) : 0.f;
+        p1 = v1 ? F::dot(s + rA1, X, hf) : 0.f;
     }
 }
 
-template <class F>
+// Epilogues fused into the store (PESTI README, "Conformance": the QKV
+// projections carry a bias, the MLP multiplies silu of the gate projection by
+// the up projection).
+// silu(z) = z * sigmoid(z) = z / (1 + e^-z), with CUDA's expf; for z below
+// about -88 e^-z is inf and the quotient is -0, the limit.
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+template <class F, int EPI>
 __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
@@ -675,13 +700,16 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     const int S = p.k / 64;
     const uint32_t rowbytes = (uint32_t)nb * (uint32_t)F::kBlockBytes;
     const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
-    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
-    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
-    const int units = (nrows + RS - 1) / RS;
+    constexpr bool SW = EPI == kEpiSwiGLU;
+    // items: rows, or (SwiGLU) row pairs; IPS items per stage
+    const int64_t n_items = SW ? (int64_t)p.n_ff : (int64_t)p.n_out;
+    const int64_t r0 = n_items * blockIdx.x / gridDim.x;
+    const int nrows = (int)(n_items * (blockIdx.x + 1) / gridDim.x - r0);
+    const int IPS = SW ? NG : RS;
+    const int units = (nrows + IPS - 1) / IPS;
     const int NS = p.nstages;
     const uint32_t stage_bytes = (uint32_t)RS * rowbytes;
-    float *xstage = reinterpret_cast<float *>(smem + (size_t)NS * stage_bytes);
-    uint8_t *ximg = smem + (size_t)NS * stage_bytes + x_stage_bytes(p.k, p.xstage);
+    uint8_t *ximg = smem + (size_t)NS * stage_bytes;
     uint8_t *xmeta = ximg + 2 * p.k;
     float *red = reinterpret_cast<float *>(xmeta + S * 16);
     const uint32_t ring_s = smem_u32(smem);
@@ -700,30 +728,40 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     if (warp == CW) {
         // ---------------- producer: one contiguous copy per stage ----------------
         if (lane == 0) {
-            // weights that may be read before the previous kernel ends: the
-            // first ring's worth when they are declared static, else none
-            const int early = p.early_w ? (units < NS ? units : NS) : 0;
+            if (!p.early_w) grid_dep_wait();   // the weights may be the previous kernel's output
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
+            const int window = kXWindow < NS ? kXWindow : NS;
+            bool x_in = false;         // the consumers have converted x
+            int landed = 0, lslot = 0; // stages known to have landed; slot of the next one
+            uint32_t lph = 0;
             int slot = 0;
             uint32_t ph = 0;
-            for (int u = 0; u <= units; ++u) {
-                if (u == early) {
-                    // x (the previous kernel's output, if any) goes ahead of
-                    // the rest of the weight stream
-                    grid_dep_wait();
-                    if (p.xstage) {
-                        mbar_arrive_expect_tx(&x_bar, (uint32_t)(4 * p.k));
-                        bulk_g2s(xstage, p.x, (uint32_t)(4 * p.k), &x_bar);
-                    }
-                }
-                if (u == units) break;
-                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
+            bool ok = true;
+            for (int u = 0; u < units && ok; ++u) {
+                const int rows = nrows - u * IPS < IPS ? nrows - u * IPS : IPS;
                 const uint32_t bytes = (uint32_t)rows * rowbytes;
                 if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_g2s_hint(smem + (size_t)slot * stage_bytes, src, bytes, &full_bar[slot], pol);
-                src += (size_t)RS * rowbytes;
+                if (!x_in) x_in = mbar_test_wait(&x_bar, 0);   // poll, never suspend
+                // until x is in, stage u - window must have landed before stage u
+                // is issued (window <= NS: that stage's slot is not re-armed yet)
+                while (!x_in && landed <= u - window) {
+                    if (!mbar_wait(&full_bar[lslot], lph)) { ok = false; break; }
+                    if (++lslot == NS) { lslot = 0; lph ^= 1u; }
+                    ++landed;
+                }
+                if (!ok) break;
+                uint8_t *dst = smem + (size_t)slot * stage_bytes;
+                if constexpr (SW) {
+                    // gate rows to the stage's first half, the same pairs' up rows to the second
+                    mbar_arrive_expect_tx(&full_bar[slot], 2 * bytes);
+                    bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
+                    bulk_g2s_hint(dst + (size_t)NG * rowbytes, src + (size_t)p.n_ff * rowbytes, bytes, &full_bar[slot], pol);
+                } else {
+                    mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                    bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
+                }
+                src += (size_t)IPS * rowbytes;
                 if (++slot == NS) { slot = 0; ph ^= 1u; }
             }
         }
@@ -732,14 +770,10 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
 
     // ---------------- x image (all consumer warps) ----------------
     bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
-    if (p.xstage) {
-        if (!mbar_wait(&x_bar, 0)) dead = true;
-        prep_x_all<true>(xstage, ximg, xmeta, nb, S, warp, CW, lane);
-    } else {
-        grid_dep_wait();
-        prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
-    }
+    grid_dep_wait();     // x may be the previous kernel's output
+    prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
     named_sync(1, CW * 32);
+    if (threadIdx.x == 0) mbar_arrive(&x_bar);   // lifts the producer's in-flight limit
     if (warp >= CA) return;
 
     const int gi = warp / G, seg = warp - gi * G;
@@ -754,6 +788,7 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     const uint32_t rA0 = (uint32_t)gi * rowbytes, rA1 = (uint32_t)(gi + NG) * rowbytes;
     const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
     // the row this lane's reduced value belongs to: 0,1 of stage A, 2,3 of stage B
+    // (SwiGLU: rows gi and gi+NG of a stage are the gate and up rows of pair gi)
     const int my_t = gi + (b3 ? NG : 0);
 
     int slot = 0;
@@ -770,22 +805,23 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
         }
         const uint32_t sA = lane_base + (uint32_t)slotA * stage_bytes;
         const uint32_t sB = lane_base + (uint32_t)slotB * stage_bytes;
-        const int nA = nrows - u * RS < RS ? nrows - u * RS : RS;
-        const int nB = hasB ? (nrows - (u + 1) * RS < RS ? nrows - (u + 1) * RS : RS) : 0;
+        // items (rows, or pairs) in stages A and B
+        const int nA = nrows - u * IPS < IPS ? nrows - u * IPS : IPS;
+        const int nB = hasB ? (nrows - (u + 1) * IPS < IPS ? nrows - (u + 1) * IPS : IPS) : 0;
         float pr[4];
         // stage A: wait, compute its two rows, hand the slot back; then stage B
         if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
-        if (nA == RS)
-            two_rows<F, false>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
+        if (nA == IPS)
+            two_rows<F, false>(pr[0], pr[1], sA, rA0, rA1, true, true, X, hf);
         else
-            two_rows<F, true>(pr[0], pr[1], sA, rA0, rA1, gi, NG, nA, X, hf);
+            two_rows<F, true>(pr[0], pr[1], sA, rA0, rA1, gi < nA, SW ? gi < nA : gi + NG < nA, X, hf);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slotA]);
         if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
-        if (nB == RS)
-            two_rows<F, false>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+        if (nB == IPS)
+            two_rows<F, false>(pr[2], pr[3], sB, rA0, rA1, true, true, X, hf);
         else
-            two_rows<F, true>(pr[2], pr[3], sB, rA0, rA1, gi, NG, nB, X, hf);
+            two_rows<F, true>(pr[2], pr[3], sB, rA0, rA1, gi < nB, SW ? gi < nB : gi + NG < nB, X, hf);
         __syncwarp();
         if (lane == 0 && hasB) mbar_arrive(&empty_bar[slotB]);
         // transposed reduction of the four rows: lanes 0-7 end with row 0,
@@ -797,44 +833,63 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
         v += __shfl_xor_sync(0xffffffffu, v, 4);
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if ((lane & 7) == 0) {
-            const int n_here = b4 ? nB : nA;
-            if (my_t < n_here) {
-                const int row = (u + (b4 ? 1 : 0)) * RS + my_t;     // relative to r0
-                if (G == 1)
-                    p.y[r0 + row] = v;
-                else
+        const int n_here = b4 ? nB : nA;
+        if constexpr (SW) {
+            const float up = __shfl_down_sync(0xffffffffu, v, 8);   // lanes 0 and 16: the pair's up row
+            if ((lane & 15) == 0 && gi < n_here) {
+                if (G == 1) {
+                    p.y[r0 + (u + (b4 ? 1 : 0)) * NG + gi] = silu(v) * up;
+                } else {
+                    const int row = (u + (b4 ? 1 : 0)) * RS + gi;    // stage-relative gate row
                     red[row * G + seg] = v;
+                    red[(row + NG) * G + seg] = up;
+                }
             }
+        } else if ((lane & 7) == 0 && my_t < n_here) {
+            const int row = (u + (b4 ? 1 : 0)) * RS + my_t;     // relative to r0
+            if (G == 1)
+                p.y[r0 + row] = EPI == kEpiBias ? v + p.bias[r0 + row] : v;
+            else
+                red[row * G + seg] = v;
         }
     }
     if (G > 1) {
+        // partial sums of the G segments of each row, added in segment order
         named_sync(2, CA * 32);
         for (int i = warp * 32 + lane; i < nrows; i += CA * 32) {
-            float sum = red[i * G];
-            for (int g2 = 1; g2 < G; ++g2) sum += red[i * G + g2];
-            p.y[r0 + i] = sum;
+            if constexpr (SW) {
+                const int row = (i / NG) * RS + i % NG;       // gate row of pair i; its up row is row + NG
+                float g = red[row * G], up = red[(row + NG) * G];
+                for (int g2 = 1; g2 < G; ++g2) {
+                    g += red[row * G + g2];
+                    up += red[(row + NG) * G + g2];
+                }
+                p.y[r0 + i] = silu(g) * up;
+            } else {
+                float sum = red[i * G];
+                for (int g2 = 1; g2 < G; ++g2) sum += red[i * G + g2];
+                p.y[r0 + i] = EPI == kEpiBias ? sum + p.bias[r0 + i] : sum;
+            }
         }
     }
 }
 
-template <class F>
-cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
-                   int grid, cudaStream_t s, int early_w) {
-    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, 0};
-    // x through shared memory unless the weights are prefetched and rows are
-    // short (then the ring depth matters more than where x queues)
-    const bool staged = !early_w || segments(k) > 1;
-    if (!plan(k, n_out, grid, F::kBlockBytes, staged, p)) return cudaErrorInvalidValue;
-    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_stage_bytes(k, staged) +
-                     x_image_bytes(k, 1) + red_bytes(p);
+// One launch over n_out rows (EPI none / bias), or over the 2 * n_ff rows of
+// a fused gate+up matrix writing n_ff SwiGLU outputs (EPI SwiGLU, n_out =
+// 2 * n_ff); grid <= the number of items.
+template <class F, int EPI>
+cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y, int grid,
+                   cudaStream_t s, int early_w, const float *bias) {
+    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, (int)(n_out / 2), bias};
+    if (!plan(k, n_out, grid, F::kBlockBytes, p, EPI == kEpiSwiGLU)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p);
     static PerDeviceOnce configured;
     const cudaError_t ce = configured.run([] {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows<F>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows<F, EPI>);
         if (e != cudaSuccess) return e;
         if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(gemv_rows<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
+        return cudaFuncSetAttribute(gemv_rows<F, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
     });
     if (ce != cudaSuccess) return ce;
     cudaLaunchConfig_t cfg = {};
@@ -847,17 +902,28 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows<F>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows<F, EPI>, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Whether the whole-row kernel takes (fmt, k, n_out) at batch 1.
-inline bool takes(int fmt, int64_t k, int64_t n_out) {
+template <class F>
+cudaError_t launch_epi(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y, int grid,
+                       cudaStream_t s, int early_w, const Epilogue &epi) {
+    if (epi.kind == kEpiSwiGLU) return launch<F, kEpiSwiGLU>(w, n_out, k, x, y, grid, s, early_w, nullptr);
+    if (epi.kind == kEpiBias) return launch<F, kEpiBias>(w, n_out, k, x, y, grid, s, early_w, epi.bias);
+    return launch<F, kEpiNone>(w, n_out, k, x, y, grid, s, early_w, nullptr);
+}
+
+// Whether the whole-row kernel takes (fmt, k, n_out) at batch 1 (n_out = 2 *
+// pairs for the SwiGLU epilogue).
+inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
     Params p{};
     const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
-    const int grid = (int)(n_out < grid_est ? n_out : grid_est);
-    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, true, p);
-    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, true, p);
+    const int64_t items = swiglu ? n_out / 2 : n_out;
+    const int grid = (int)(items < grid_est ? items : grid_est);
+    if (swiglu && (n_out % 2 || items < 1)) return false;
+    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, p, swiglu);
+    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p, swiglu);
     return false;
 }
 }  // namespace rowk
@@ -1291,11 +1357,24 @@ unsigned stream_wait_timeouts(bool reset) {
     return v;
 }
 
+bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kind) {
+    return batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out, kind == kEpiSwiGLU);
+}
+
 bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch) {
     if (batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out)) return true;
     if (fmt != PQ_Q4_K || batch < 1 || batch > 4 || n_out < 1) return false;
     if (k % 256 || k > (INT64_C(1) << 20)) return false;
     return plan_stages(k, batch) >= 2;
+}
+
+cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
+                                   cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi) {
+    if (!stream_epilogue_fused(fmt, n_out, k, 1, epi.kind)) return cudaErrorInvalidValue;
+    const int64_t items = epi.kind == kEpiSwiGLU ? n_out / 2 : n_out;
+    const int grid = (int)(items < dev.sm_count ? items : dev.sm_count);
+    if (fmt == PQ_Q4_K) return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
 }
 
 cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
@@ -1304,10 +1383,8 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
     if (!stream_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
     Params p{w, x, y, (long long)ldy, (int)n_out, (int)k, 0};
     const int grid = (int)(n_out < dev.sm_count ? n_out : dev.sm_count);
-    if (batch == 1 && fmt == PQ_Q4_K && rowk::takes(fmt, k, n_out))
-        return rowk::launch<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch());
-    if (batch == 1 && fmt == PQ_Q6_K && rowk::takes(fmt, k, n_out))
-        return rowk::launch<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch());
+    if (batch == 1 && (fmt == PQ_Q4_K || fmt == PQ_Q6_K) && rowk::takes(fmt, k, n_out))
+        return launch_gemv_stream_epi(fmt, w, n_out, k, x, y, s, dev, Epilogue{});
     if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
         return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);
     switch (batch) {

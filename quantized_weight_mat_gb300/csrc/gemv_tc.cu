@@ -340,7 +340,19 @@ struct TcParams {
     int n_out;
     int k;
     int nb_cols;
+    const float *bias;         // bias epilogue: bias[n_out], else null
+    // SwiGLU epilogue (n_ff > 0): tile 2i is rows [128i, 128i+128) of the gate
+    // half, tile 2i+1 the same rows of the up half (rows n_ff + ...); every
+    // tile's sums go to ytmp [tiles][TM][NBP] or to the partial sums, and a
+    // finishing kernel forms h = silu(gate) * up
+    int n_ff;
+    float *ytmp;
 };
+
+// First matrix row of tile t (see TcParams).
+__host__ __device__ __forceinline__ long long tile_row0(int t, int n_ff) {
+    return n_ff > 0 ? (long long)(t & 1) * n_ff + (long long)(t >> 1) * TM : (long long)t * TM;
+}
 
 // First work item of CTA c when `total` items are split over `grid` CTAs, and
 // the CTA that owns item i (the largest c with item_begin(c) <= i).
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!mbar_wait(&raw_empty[slot], ph ^ 1u)) break;
                 uint8_t *st = ring + slot * STAGE;
                 mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)STAGE);
-                tma_load_2d(st, &wmap, sb * 144, tile * TM, &raw_full[slot]);
+                tma_load_2d(st, &wmap, sb * 144, (int)tile_row0(tile, p.n_ff), &raw_full[slot]);
                 // the weights were complete before the x-prep kernel let this kernel
                 // launch; the x image is that kernel's output: wait for it once,
                 // before its first use
@@ -525,11 +537,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const long long t0i = (long long)tile * nb;
                 const int cf = item_owner(t0i, p.total, grid), cl = item_owner(t0i + nb - 1, p.total, grid);
                 const int row = tile * TM + r;
-                if (cf == cl) {
+                if (cf == cl && p.n_ff > 0) {
+                    // SwiGLU: the finishing kernel pairs this tile with its partner
+                    float4 *mine = reinterpret_cast<float4 *>(p.ytmp + ((size_t)tile * TM + r) * NBP);
+#pragma unroll
+                    for (int b4 = 0; b4 < NBP / 4; ++b4)
+                        mine[b4] = make_float4(yacc[4 * b4], yacc[4 * b4 + 1], yacc[4 * b4 + 2], yacc[4 * b4 + 3]);
+                } else if (cf == cl) {
                     if (row < p.n_out) {
+                        const float bias = p.bias ? p.bias[row] : 0.f;
 #pragma unroll
                         for (int b = 0; b < NBP; ++b)
-                            if (b < p.nb_cols) p.y[(size_t)b * p.ldy + row] = yacc[b];
+                            if (b < p.nb_cols) p.y[(size_t)b * p.ldy + row] = p.bias ? yacc[b] + bias : yacc[b];
                     }
                 } else {
                     // split tile: this CTA's part, added up by the finishing kernel
@@ -630,7 +649,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 // resident beside it and waits for the main grid to complete.
 template <int NBP>
 __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partials, float *__restrict__ y,
-                                               long long ldy, long long total, int nb, int n_out, int nb_cols) {
+                                               long long ldy, long long total, int nb, int n_out, int nb_cols,
+                                               const float *__restrict__ bias) {
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int grid = (int)gridDim.x, c = (int)blockIdx.x;
@@ -671,9 +691,66 @@ __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partia
         }
     }
     if (row < n_out) {
+        const float bv = bias ? bias[row] : 0.f;
 #pragma unroll
         for (int b = 0; b < NBP; ++b)
-            if (b < nb_cols) y[(size_t)b * ldy + row] = sum[b];
+            if (b < nb_cols) y[(size_t)b * ldy + row] = bias ? sum[b] + bv : sum[b];
+    }
+}
+
+// The sums of row r of tile t for all NBP columns: from ytmp when one CTA
+// computed the whole tile, else its CTAs' partial sums added in CTA order.
+template <int NBP>
+__device__ __forceinline__ void tile_sums(float (&sum)[NBP], int t, int r, const float *__restrict__ partials,
+                                          const float *__restrict__ ytmp, long long total, int nb, int grid) {
+    const long long t0 = (long long)t * nb;
+    const int cf = item_owner(t0, total, grid), cl = item_owner(t0 + nb - 1, total, grid);
+    if (cf == cl) {
+        const float4 *v = reinterpret_cast<const float4 *>(ytmp + ((size_t)t * TM + r) * NBP);
+#pragma unroll
+        for (int b4 = 0; b4 < NBP / 4; ++b4) {
+            const float4 q = v[b4];
+            sum[4 * b4] = q.x; sum[4 * b4 + 1] = q.y; sum[4 * b4 + 2] = q.z; sum[4 * b4 + 3] = q.w;
+        }
+        return;
+    }
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) sum[b] = 0.f;
+    for (int cc = cf; cc <= cl; ++cc) {
+        const int side = t == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
+        const float4 *part = reinterpret_cast<const float4 *>(partials + ((size_t)(cc * 2 + side) * TM + r) * NBP);
+#pragma unroll
+        for (int b4 = 0; b4 < NBP / 4; ++b4) {
+            const float4 q = part[b4];
+            sum[4 * b4] += q.x; sum[4 * b4 + 1] += q.y; sum[4 * b4 + 2] += q.z; sum[4 * b4 + 3] += q.w;
+        }
+    }
+}
+
+// silu(z) = z * sigmoid(z) = z / (1 + e^-z) with CUDA's expf (PESTI README,
+// "Conformance": the MLP multiplies silu of the gate projection by the up
+// projection).
+__device__ __forceinline__ float silu_tc(float z) { return z / (1.0f + expf(-z)); }
+
+// SwiGLU finish: block i forms h[b][128i + r] = silu(gate) * up from tiles 2i
+// (gate rows) and 2i+1 (up rows).  Launched after the main kernel with
+// programmatic dependent launch, like tc_finish.
+template <int NBP>
+__global__ void __launch_bounds__(TM) tc_finish_swiglu(const float *__restrict__ partials,
+                                                      const float *__restrict__ ytmp, float *__restrict__ h,
+                                                      long long ldh, long long total, int nb, int grid, int n_ff,
+                                                      int nb_cols) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int i = (int)blockIdx.x, r = threadIdx.x;
+    float g[NBP], u[NBP];
+    tile_sums<NBP>(g, 2 * i, r, partials, ytmp, total, nb, grid);
+    tile_sums<NBP>(u, 2 * i + 1, r, partials, ytmp, total, nb, grid);
+    const int j = i * TM + r;
+    if (j < n_ff) {
+#pragma unroll
+        for (int b = 0; b < NBP; ++b)
+            if (b < nb_cols) h[(size_t)b * ldh + j] = silu_tc(g[b]) * u[b];
     }
 }
 
@@ -713,8 +790,14 @@ EncodeTiled encode_fn() {
 // finishing kernel (about four super-blocks' time per call); that is chosen
 // when it costs each CTA at most five super-blocks more than an even split
 // (14336x4096: 16 instead of 12 super-blocks per CTA).
-int tc_grid(int64_t n_out, int64_t k, const DeviceInfo &dev) {
-    const long long ntiles = (long long)((n_out + TM - 1) / TM), nb = k / 256;
+// Row tiles of a call: 128-row tiles of the matrix, or for the SwiGLU
+// epilogue a gate tile and an up tile per 128 pairs.
+long long tc_tiles(int64_t n_out, const Epilogue &epi) {
+    return epi.kind == kEpiSwiGLU ? 2 * ((n_out / 2 + TM - 1) / TM) : (n_out + TM - 1) / TM;
+}
+
+int tc_grid(int64_t n_out, int64_t k, const DeviceInfo &dev, const Epilogue &epi = Epilogue{}) {
+    const long long ntiles = tc_tiles(n_out, epi), nb = k / 256;
     const long long total = ntiles * nb;
     long long g = dev.sm_count < kMaxGrid ? dev.sm_count : kMaxGrid;
     if (g > total) g = total;
@@ -723,12 +806,21 @@ int tc_grid(int64_t n_out, int64_t k, const DeviceInfo &dev) {
     return (int)g;
 }
 
+// Scratch of one call: x image, split-K partial sums, and for the SwiGLU
+// epilogue the whole tiles' sums [tiles][TM][NBP].
+template <int NBP> size_t scratch_bytes_epi(int64_t n_out, int64_t k, int grid, const Epilogue &epi) {
+    return scratch_bytes<NBP>(k, grid) + (epi.kind == kEpiSwiGLU ? (size_t)tc_tiles(n_out, epi) * TM * NBP * 4 : 0);
+}
+
 template <int NBP>
 cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch, float *y,
-                       int64_t ldy, cudaStream_t s, int grid, uint8_t *scratch) {
+                       int64_t ldy, cudaStream_t s, int grid, uint8_t *scratch, const Epilogue &epi = Epilogue{}) {
     const int nb = (int)(k / 256);
     uint8_t *img = scratch;
     float *partials = reinterpret_cast<float *>(scratch + scratch_img_bytes<NBP>(k));
+    float *ytmp = reinterpret_cast<float *>(scratch + scratch_bytes<NBP>(k, grid));
+    const bool swiglu = epi.kind == kEpiSwiGLU;
+    const int n_ff = swiglu ? (int)(n_out / 2) : 0;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -759,9 +851,10 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
         return cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
     });
     if (e != cudaSuccess) return e;
-    const long long ntiles = (n_out + TM - 1) / TM;
+    const long long ntiles = tc_tiles(n_out, epi);
     const long long total = ntiles * nb;
-    TcParams p{img, y, partials, (long long)ldy, total, (int)n_out, (int)k, batch};
+    TcParams p{img, y, partials, (long long)ldy, total, (int)n_out, (int)k, batch,
+               epi.kind == kEpiBias ? epi.bias : nullptr, n_ff, swiglu ? ytmp : nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
@@ -771,12 +864,19 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
     if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess || !any_split(total, nb, grid)) return e;
-    cfg.gridDim = dim3(grid);
+    if (e != cudaSuccess) return e;
     cfg.blockDim = dim3(TM);
     cfg.dynamicSmemBytes = 0;
+    if (swiglu) {
+        cfg.gridDim = dim3((unsigned)(ntiles / 2));
+        e = cudaLaunchKernelEx(&cfg, tc_finish_swiglu<NBP>, (const float *)partials, (const float *)ytmp, y,
+                               (long long)ldy, total, nb, grid, n_ff, batch);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    if (!any_split(total, nb, grid)) return e;
+    cfg.gridDim = dim3(grid);
     e = cudaLaunchKernelEx(&cfg, tc_finish<NBP>, (const float *)partials, y, (long long)ldy, total, nb, (int)n_out,
-                           batch);
+                           batch, p.bias);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -834,17 +934,18 @@ bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch) {
 }
 
 cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
-                           float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev) {
+                           float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi) {
     if (!tc_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
-    const int grid = tc_grid(n_out, k, dev);
-    const size_t bytes = batch <= 8 ? scratch_bytes<8>(k, grid) : scratch_bytes<16>(k, grid);
+    if (epi.kind == kEpiSwiGLU && (n_out % 2 || n_out < 2)) return cudaErrorInvalidValue;
+    const int grid = tc_grid(n_out, k, dev, epi);
+    const size_t bytes = batch <= 8 ? scratch_bytes_epi<8>(n_out, k, grid, epi) : scratch_bytes_epi<16>(n_out, k, grid, epi);
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
     void *scratch = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, pool, s);
     if (e != cudaSuccess) return e;
-    e = batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch)
-                   : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch);
+    e = batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi)
+                   : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi);
     const cudaError_t f = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : f;
 }

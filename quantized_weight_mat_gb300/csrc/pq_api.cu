@@ -164,6 +164,56 @@ int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &
     return PQ_OK;
 }
 
+// Mat-vec with an optional epilogue.  The kernel choice is pq_gemv's for the
+// n_out x k matrix (for SwiGLU the fused 2 * n_ff-row matrix); the batch-1
+// whole-row kernel and the tensor-core kernel fuse the epilogue into their
+// stores, the others run it as a small kernel afterwards (SwiGLU through a
+// pool buffer of batch x n_out outputs).
+int gemv_epi_impl(int fmt, const void *w_blocks, int n_out, int k, const float *x, int batch, float *y,
+                  cudaStream_t stream, const Epilogue &epi) {
+    const DeviceInfo *dev = nullptr;
+    int st = check_device(&dev);
+    if (st) return st;
+    const bool sw = epi.kind == kEpiSwiGLU;
+    const int64_t ldy = sw ? n_out / 2 : n_out;
+    const uint8_t *w = static_cast<const uint8_t *>(w_blocks);
+    st = for_each_chunk(fmt, n_out, k, batch, PQ_KERNEL_AUTO, [](int, int, int) { return PQ_OK; });
+    if (st) return st;
+    return for_each_chunk(fmt, n_out, k, batch, PQ_KERNEL_AUTO, [&](int kern, int b0, int nb) {
+        const float *xb = x + (int64_t)b0 * k;
+        float *yb = y + (int64_t)b0 * ldy;
+        cudaError_t e;
+        if (kern == PQ_KERNEL_TC) {
+            e = launch_gemv_tc(fmt, w, n_out, k, xb, nb, yb, ldy, stream, *dev, epi);
+        } else if (kern == PQ_KERNEL_STREAM && stream_epilogue_fused(fmt, n_out, k, nb, epi.kind)) {
+            e = launch_gemv_stream_epi(fmt, w, n_out, k, xb, yb, stream, *dev, epi);
+        } else {
+            // plain mat-vec, then the epilogue kernel
+            float *out = yb;
+            void *tmp = nullptr;
+            if (sw) {
+                cudaMemPool_t pool = scratch_pool();
+                if (!pool) return PQ_ERR_LAUNCH;
+                if (cudaMallocFromPoolAsync(&tmp, (size_t)nb * n_out * 4, pool, stream) != cudaSuccess)
+                    return PQ_ERR_LAUNCH;
+                out = static_cast<float *>(tmp);
+            }
+            if (kern == PQ_KERNEL_STREAM)
+                e = launch_gemv_stream(fmt, w, n_out, k, xb, nb, out, n_out, stream, *dev);
+            else
+                e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, out, n_out, stream);
+            if (e == cudaSuccess)
+                e = sw ? launch_swiglu_rows(out, n_out / 2, nb, yb, ldy, stream)
+                       : launch_add_bias(yb, epi.bias, n_out, ldy, nb, stream);
+            if (tmp) {
+                const cudaError_t f = cudaFreeAsync(tmp, stream);
+                if (e == cudaSuccess) e = f;
+            }
+        }
+        return e == cudaSuccess ? PQ_OK : PQ_ERR_LAUNCH;
+    });
+}
+
 int gemv_impl(int fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
               float *y, cudaStream_t stream, int kernel) {
     int st = check_gemv(fmt, w_blocks, n_out, k, x, batch, y);
@@ -221,6 +271,38 @@ int pq_gemv(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x, 
 int pq_gemv_kernel(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x,
                    int batch, float *y, struct CUstream_st *stream, int kernel) {
     return gemv_impl((int)fmt, w_blocks, n_out, k, x, batch, y, stream, kernel);
+}
+
+int pq_gemv_bias(pq_fmt fmt, const void *w_blocks, int n_out, int k, const float *x, int batch,
+                 const float *bias, float *y, struct CUstream_st *stream) {
+    int st = check_gemv((int)fmt, w_blocks, n_out, k, x, batch, y);
+    if (st) return st;
+    if (!bias) return PQ_ERR_ARG;
+    if ((uintptr_t)bias % 4) return PQ_ERR_ALIGN;
+    if (overlaps(y, 4 * (int64_t)batch * n_out, bias, 4 * (int64_t)n_out)) return PQ_ERR_ARG;
+    Epilogue epi;
+    epi.kind = kEpiBias;
+    epi.bias = bias;
+    return gemv_epi_impl((int)fmt, w_blocks, n_out, k, x, batch, y, stream, epi);
+}
+
+int pq_gemv_swiglu(pq_fmt fmt, const void *w_blocks, int n_ff, int k, const float *x, int batch, float *h,
+                   struct CUstream_st *stream) {
+    if (!valid_fmt((int)fmt)) return PQ_ERR_FMT;
+    if (!w_blocks || !x || !h || n_ff <= 0 || k <= 0 || batch <= 0) return PQ_ERR_ARG;
+    if (n_ff > 0x3fffffff) return PQ_ERR_SIZE;
+    const int n_out = 2 * n_ff;
+    int st = check_common((int)fmt, w_blocks, n_out, k);
+    if (st) return st;
+    if ((int64_t)batch * n_out > (INT64_C(1) << 40) || (int64_t)batch * k > (INT64_C(1) << 40)) return PQ_ERR_SIZE;
+    if ((uintptr_t)x % 16 || (uintptr_t)h % 4) return PQ_ERR_ALIGN;
+    const int64_t hbytes = 4 * (int64_t)batch * n_ff;
+    if (overlaps(h, hbytes, w_blocks, weight_bytes64((int)fmt, n_out, k)) ||
+        overlaps(h, hbytes, x, 4 * (int64_t)batch * k))
+        return PQ_ERR_ARG;
+    Epilogue epi;
+    epi.kind = kEpiSwiGLU;
+    return gemv_epi_impl((int)fmt, w_blocks, n_out, k, x, batch, h, stream, epi);
 }
 
 int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch) {

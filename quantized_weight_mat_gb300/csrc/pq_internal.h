@@ -53,6 +53,17 @@ const DeviceInfo *device_info();
 // memory taken with cudaMallocFromPoolAsync, kept for reuse); null on failure.
 cudaMemPool_t scratch_pool();
 
+// Epilogue applied to the mat-vec outputs before they are stored.
+//   kEpiBias:   y[b][r] = (W x_b)[r] + bias[r]
+//   kEpiSwiGLU: W is a fused gate+up matrix of n_out = 2 * n_ff rows (gate
+//               rows first); h[b][j] = silu((W x_b)[j]) * (W x_b)[n_ff + j],
+//               stored as [batch][n_ff]
+constexpr int kEpiNone = 0, kEpiBias = 1, kEpiSwiGLU = 2;
+struct Epilogue {
+    int kind = kEpiNone;
+    const float *bias = nullptr;
+};
+
 // Launchers: arguments already validated; return cudaError_t of the launch.
 cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, float *out,
                            cudaStream_t s);
@@ -67,18 +78,32 @@ bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch);
 cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                                const float *x, int batch, float *y, int64_t ldy,
                                cudaStream_t s, const DeviceInfo &dev);
+// The batch-1 whole-row kernel with the epilogue fused into its stores
+// (Q4_K and Q6_K); `stream_epilogue_fused` says whether it takes the case.
+bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kind);
+cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
+                                   cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi);
 
 // Tensor-core kernel (tcgen05): Q4_K, batch chunks of 8 or 16.
 bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch);
+// The epilogue is fused: the bias is added at the final store, SwiGLU pairs
+// gate and up tiles in the finishing kernel (y is then h, [batch][n_out / 2]
+// with row stride ldy).
 cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                            const float *x, int batch, float *y, int64_t ldy,
-                           cudaStream_t s, const DeviceInfo &dev);
+                           cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi = Epilogue{});
 
 // Allocation-free variant of the tensor-core kernel: the x image lives in a
 // fixed device array instead of pool memory (k <= noalloc_max_k(), batch <= 16).
 int noalloc_max_k();
 cudaError_t launch_gemv_tc_noalloc(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
                                    float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev);
+
+// Stand-alone epilogue kernels (epilogue.cu) for kernels without a fused one:
+// y[b][r] += bias[r]; h[b][j] = silu(g[b][j]) * g[b][n_ff + j] with g
+// [batch][2 n_ff].
+cudaError_t launch_add_bias(float *y, const float *bias, int64_t n_out, int64_t ldy, int batch, cudaStream_t s);
+cudaError_t launch_swiglu_rows(const float *g, int64_t n_ff, int batch, float *h, int64_t ldh, cudaStream_t s);
 
 // Process-wide: may kernels read weights before the preceding kernel on the
 // stream has finished (set by pq_set_weight_prefetch)?
