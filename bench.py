@@ -173,8 +173,17 @@ CONFIGS = [
     ("Q6_K LM head 128256x4096, batch 1", "q6_k", 128256, 4096, 1),
 ] + [(f"Q4_K {n}x{k}, batch {b}", "q4_k", n, k, b)
      for (n, k) in ((14336, 4096), (4096, 14336)) for b in (1, 2, 4, 8, 16)
-] + [(f"{f.upper()} 14336x4096, batch 1 (generic kernel)", f, 14336, 4096, 1)
-     for f in ("q5_k", "q3_k", "q2_k", "i4_row")]
+] + [(f"Q6_K LM head 128256x4096, batch {b}", "q6_k", 128256, 4096, b) for b in (2, 4, 8)
+] + [("Q8_0 4096x4096, batch 1", "q8_0", 4096, 4096, 1),
+     ("Q8_0 14336x4096, batch 1", "q8_0", 14336, 4096, 1),
+     ("I8_ROW 14336x4096, batch 1", "i8_row", 14336, 4096, 1),
+     ("I8_ROW 4096x4096, batch 1", "i8_row", 4096, 4096, 1),
+] + [(f"{f.upper()} 14336x4096, batch 1", f, 14336, 4096, 1)
+     for f in ("q5_k", "q3_k", "q2_k", "i4_row")
+] + [("Q4_K QKV 6144x4096 with bias, batch 1", "q4_k", 6144, 4096, 1, "bias"),
+     ("Q4_K gate+up 28672x4096 with SwiGLU, batch 1", "q4_k", 28672, 4096, 1, "swiglu"),
+     ("Q4_K gate+up 28672x4096 with SwiGLU, batch 8", "q4_k", 28672, 4096, 8, "swiglu"),
+     ("Q4_K gate+up 28672x4096, batch 8", "q4_k", 28672, 4096, 8)]
 
 
 def per_config(pq, dev, peak, l2_bytes):
@@ -183,22 +192,33 @@ def per_config(pq, dev, peak, l2_bytes):
     events around one replay.  Returns one record per workload."""
     import torch
     out = []
-    for name, fmt, n, k, b in CONFIGS:
+    for name, fmt, n, k, b, *epi in CONFIGS:
+        epi = epi[0] if epi else None
         nbytes = synth.weight_bytes(fmt, n, k)
         copies = max(2, -(-2 * l2_bytes // nbytes))
         base = torch.from_numpy(synth.random_records(fmt, n, k, seed=11)).to(dev)
         W = [base] + [base.clone() for _ in range(copies - 1)]
         x = torch.from_numpy(synth.normal_x(b, k, seed=12)).to(dev)
         y = torch.empty(b * n, dtype=torch.float32, device=dev)
+        bias = torch.zeros(n, dtype=torch.float32, device=dev)
         launches = max(20, min(400, int(4e8 // nbytes)))
+
+        def call(i, stream=None):
+            if epi == "bias":
+                pq.pq_gemv_bias(fmt, W[i % copies], n, k, x, b, bias, y, stream)
+            elif epi == "swiglu":
+                pq.pq_gemv_swiglu(fmt, W[i % copies], n // 2, k, x, b, y, stream)
+            else:
+                pq.pq_gemv(fmt, W[i % copies], n, k, x, b, y, stream)
+
         for i in range(3):
-            pq.pq_gemv(fmt, W[i % copies], n, k, x, b, y)
+            call(i)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             cur = torch.cuda.current_stream()
             for i in range(launches):
-                pq.pq_gemv(fmt, W[i % copies], n, k, x, b, y, cur)
+                call(i, cur)
         g.replay()
         torch.cuda.synchronize()
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -349,6 +369,37 @@ def run_ours(args):
     torch.cuda.synchronize()
     ms = timed(args.steps)
     dom_ms = dominant_alone(args.dominant_launches)
+
+    # the same layer with the epilogues fused (PESTI README, "Conformance"):
+    # QKV with its bias, O, gate+up with SwiGLU writing h (14336 values), and
+    # the down projection reading h; same weights and bytes per step
+    qkv_bias = torch.from_numpy(np.random.default_rng(9).normal(0.0, 0.5, SET[0][1]).astype(np.float32)).to(dev)
+    H = torch.empty(FFN, dtype=torch.float32, device=dev)
+
+    def fused_body(count):
+        cur = torch.cuda.current_stream()
+        for s in range(count):
+            ws = W[s % L]
+            pq.pq_gemv_bias(FMT, ws[0], SET[0][1], SET[0][2], X[0], 1, qkv_bias, Y[0], cur)
+            pq.pq_gemv(FMT, ws[1], SET[1][1], SET[1][2], X[1], 1, Y[1], cur)
+            pq.pq_gemv_swiglu(FMT, ws[2], FFN, SET[2][2], X[2], 1, H, cur)
+            pq.pq_gemv(FMT, ws[3], SET[3][1], SET[3][2], H, 1, Y[3], cur)
+
+    fused_body(min(L, args.warmup))
+    torch.cuda.synchronize()
+    fused_steps = min(args.steps, args.graph_steps)
+    gF = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gF):
+        fused_body(fused_steps)
+    gF.replay()
+    torch.cuda.synchronize()
+    fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.record()
+    gF.replay()
+    fb.record()
+    torch.cuda.synchronize()
+    fused_us = fa.elapsed_time(fb) * 1e3 / fused_steps
+    del gF
     # the same steps as plain stream launches (no graph), for comparison
     stream_steps = min(args.steps, 400)
     torch.cuda.synchronize()
@@ -392,6 +443,10 @@ def run_ours(args):
         "hbm_frac": round(gbs / world / peak, 4),
         "hbm_frac_nominal_8000": round(gbs / world / NOMINAL_HBM_GBS, 4),
         "us_per_set_stream_launches": round(1e3 * stream_ms / stream_steps, 3),
+        "fused_epilogue_set": {"us_per_set": round(fused_us, 3),
+                               "workload": "QKV 6144x4096 + bias, O 4096x4096, gate+up 28672x4096 with SwiGLU "
+                                           "(h of 14336), down 4096x14336 reading h; batch 1, CUDA graph",
+                               "weight_GBs": round(set_bytes() / (fused_us * 1e-6) / 1e9, 1)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,

@@ -443,18 +443,28 @@ struct Params {
     int early_w;    // stream weights before waiting on the previous kernel
     int n_ff;       // SwiGLU: pairs (the matrix has 2 * n_ff rows, gate rows first)
     const float *bias;   // bias epilogue: bias[n_out]
+    const float *rscale; // per-row formats: the f32 row scales, rscale[n_out]
+    int epi;        // kEpiNone, kEpiBias or kEpiSwiGLU
 };
 
 inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
 
-inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
+__host__ __device__ inline int red_bytes(const Params &p) { return p.G > 1 ? (p.rows_cap * p.G * 4 + 15) / 16 * 16 : 0; }
+// Row scales of a per-row format, copied to shared memory once per CTA (for
+// SwiGLU the gate and the up rows' scales of every pair), then the CTA's
+// slice of the bias for the bias epilogue.
+__host__ __device__ inline int rsc_bytes(const Params &p, bool row_scaled, bool swiglu) {
+    return row_scaled ? ((swiglu ? 2 : 1) * p.rows_cap * 4 + 15) / 16 * 16 : 0;
+}
+inline int bias_bytes(const Params &p, bool bias) { return bias ? (p.rows_cap * 4 + 15) / 16 * 16 : 0; }
 
 // Stage plan for (k, n_out, grid) with super-blocks of `block_bytes`; false
 // when this kernel cannot take the shape (rows must be whole multiples of
 // 16 bytes for the bulk copy).
 // With `swiglu` the CTA's items are (gate, up) row pairs: a stage holds NG
 // gate rows, then the NG up rows of the same pairs, and n_out is 2 * pairs.
-inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p, bool swiglu = false) {
+inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p, bool swiglu = false,
+                 bool row_scaled = false, bool bias = false) {
     if (k % 256 || grid < 1 || ((k / 256) * block_bytes) % 16) return false;
     const int G = segments(k);
     if (G < 1 || G > CW) return false;
@@ -468,7 +478,8 @@ inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p,
         p.rows_cap = (int)((n_out + grid - 1) / grid);
     }
     const int64_t stage = (int64_t)p.RS * (k / 256) * block_bytes;
-    const int64_t avail = kRowsSmem - kStatic - x_image_bytes(k, 1) - red_bytes(p);
+    const int64_t avail = kRowsSmem - kStatic - x_image_bytes(k, 1) - red_bytes(p) - rsc_bytes(p, row_scaled, swiglu) -
+                          bias_bytes(p, bias);
     int64_t ns = avail / stage;
     if (ns > MAX_STAGES) ns = MAX_STAGES;
     p.nstages = (int)ns;
@@ -522,6 +533,7 @@ __device__ __forceinline__ void load_x_parts(uint32_t (&xh)[4][8], uint32_t (&xl
 // Q4_K: lane owns sub-blocks 4h..4h+3 (chunks 2h, 2h+1) of its super-block.
 struct Q4K {
     static constexpr int kBlockBytes = 144;
+    static constexpr bool kRowScaled = false;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the 4 sub-blocks (32 positions each)
         int xs[4];                     // sum of X = 254*xh + xl per sub-block
@@ -581,6 +593,7 @@ struct Q4K {
 // since row and stage sizes are multiples of 16 bytes).
 struct Q6K {
     static constexpr int kBlockBytes = 210;
+    static constexpr bool kRowScaled = false;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-position parts t = 0..3
         int xs[8];                     // sum of X over the 8 sub-blocks of 16
@@ -667,6 +680,110 @@ struct Q6K {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Q8_0: eight 34-byte blocks (d, 32 int8 codes) make one 272-byte group of 256
+// weights; the lane owns blocks 4h..4h+3 of its group (136 bytes at an 8-byte
+// boundary).  Blocks 4h and 4h+2 start 2 bytes past a word boundary, so their
+// codes are realigned with one byte permute per word.
+struct Q80 {
+    static constexpr int kBlockBytes = 272;
+    static constexpr bool kRowScaled = false;
+    struct X {
+        uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-weight blocks
+        float u;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        int xs32[4];
+        load_x_parts(R.xh, R.xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
+        if (!valid) R.u = 0.f;
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint32_t a = blk + 136u * (uint32_t)hf;
+        uint32_t w[34];
+#pragma unroll
+        for (int j = 0; j < 17; ++j) {
+            uint2 v;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a + 8u * (uint32_t)j));
+            w[2 * j] = v.x;
+            w[2 * j + 1] = v.y;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            // block t at byte 34t of the lane's range: d, then 32 codes
+            const int wd = (34 * t) / 4;              // word holding d
+            const bool odd = (t & 1) != 0;            // d in the high half, codes word-aligned
+            const uint32_t dbits = odd ? (w[wd] >> 16) : w[wd];
+            int dh = 0, dl = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t q = odd ? w[wd + 1 + i] : __byte_perm(w[wd + i], w[wd + i + 1], 0x5432u);
+                dh = dp4a_ss(q, R.xh[t][i], dh);
+                dl = dp4a_ss(q, R.xl[t][i], dl);
+            }
+            // |254 dh + dl| < 2^28: exact in 32-bit integers
+            acc = fmaf(h2f(dbits), (float)(254 * dh + dl), acc);
+        }
+        return R.u * acc;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Per-row int8: a row is k int8 codes; the lane owns 128 codes (16-byte
+// aligned) of its 256-weight group.  Lanes' ranges are 128 bytes apart, so
+// all of them would read the same shared-memory banks at each step: lane l
+// reads its eight 16-byte chunks in the rotated order c' = (c + l) mod 8, with
+// its x limbs loaded in the same order.  The row's f32 scale multiplies the
+// reduced sum.
+struct I8R {
+    static constexpr int kBlockBytes = 256;
+    static constexpr bool kRowScaled = true;
+    struct X {
+        uint32_t xh[8][4], xl[8][4];   // limbs of chunk (c + lane) mod 8, 16 positions each
+        float u;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        uint32_t xh[4][8], xl[4][8];
+        int xs32[4];
+        load_x_parts(xh, xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
+        if (!valid) R.u = 0.f;
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int m = (c + lane) & 7;          // chunk m: part m/2, words 4(m%2)..4(m%2)+3
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // select without dynamic register indexing
+                uint32_t h = 0, l = 0;
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm)
+                    if (mm == m) { h = xh[mm >> 1][4 * (mm & 1) + i]; l = xl[mm >> 1][4 * (mm & 1) + i]; }
+                R.xh[c][i] = h;
+                R.xl[c][i] = l;
+            }
+        }
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint32_t a = blk + 128u * (uint32_t)hf;
+        const uint32_t lane = threadIdx.x & 31u;
+        int dh = 0, dl = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 q = lds(a + 16u * ((c + lane) & 7u));
+            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dh = dp4a_ss(qw[i], R.xh[c][i], dh);
+                dl = dp4a_ss(qw[i], R.xl[c][i], dl);
+            }
+        }
+        // |dh|, |dl| <= 128 * 128 * 127 < 2^21: 254 dh + dl is exact in 32 bits
+        return R.u * (float)(254 * dh + dl);
+    }
+};
+
 // Rows gi and gi+NG of one stage (lane base address s); CHECK handles a
 // partial last stage (v0, v1: whether each row is present).
 template <class F, bool CHECK>
@@ -688,7 +805,13 @@ __device__ __forceinline__ void two_rows(float &p0, float &p1, uint32_t s, uint3
 // about -88 e^-z is inf and the quotient is -0, the limit.
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-template <class F, int EPI>
+// Two instances per format: RT = false has no epilogue at compile time (the
+// plain mat-vec), RT = true takes the epilogue as a run-time parameter and
+// serves both the bias and SwiGLU, so a decode step that mixes them runs two
+// codes, not three.  Three template instances of this large kernel cycling
+// in one step measured 3 us per step slower (instruction fetch); one
+// run-time instance for everything 0.4 us slower on the plain step.
+template <class F, bool RT>
 __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
@@ -700,7 +823,7 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     const int S = p.k / 64;
     const uint32_t rowbytes = (uint32_t)nb * (uint32_t)F::kBlockBytes;
     const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
-    constexpr bool SW = EPI == kEpiSwiGLU;
+    const bool SW = RT && p.epi == kEpiSwiGLU, BIAS = RT && p.epi == kEpiBias;
     // items: rows, or (SwiGLU) row pairs; IPS items per stage
     const int64_t n_items = SW ? (int64_t)p.n_ff : (int64_t)p.n_out;
     const int64_t r0 = n_items * blockIdx.x / gridDim.x;
@@ -712,6 +835,8 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     uint8_t *ximg = smem + (size_t)NS * stage_bytes;
     uint8_t *xmeta = ximg + 2 * p.k;
     float *red = reinterpret_cast<float *>(xmeta + S * 16);
+    float *rsc = red + red_bytes(p) / 4;      // row scales (per-row formats): rows, then (SwiGLU) up rows
+    float *bsm = rsc + rsc_bytes(p, F::kRowScaled, SW) / 4;   // bias slice (bias epilogue)
     const uint32_t ring_s = smem_u32(smem);
 
     if (threadIdx.x == 0) {
@@ -752,7 +877,7 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
                 }
                 if (!ok) break;
                 uint8_t *dst = smem + (size_t)slot * stage_bytes;
-                if constexpr (SW) {
+                if (SW) {
                     // gate rows to the stage's first half, the same pairs' up rows to the second
                     mbar_arrive_expect_tx(&full_bar[slot], 2 * bytes);
                     bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
@@ -771,7 +896,35 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
     // ---------------- x image (all consumer warps) ----------------
     bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
     grid_dep_wait();     // x may be the previous kernel's output
+    // the CTA's row scales and bias slice: the first values' loads are issued
+    // with x's and stored to shared memory after the x conversion
+    const bool kVec = F::kRowScaled || BIAS;
+    float v0 = 0.f, v1 = 0.f;
+    const int i0v = threadIdx.x;
+    if (kVec) {
+        if (i0v < nrows) {
+            v0 = F::kRowScaled ? __ldg(p.rscale + r0 + i0v) : __ldg(p.bias + r0 + i0v);
+            if (F::kRowScaled && SW) v1 = __ldg(p.rscale + p.n_ff + r0 + i0v);
+        }
+    }
     prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
+    if (kVec) {
+        float *dst = F::kRowScaled ? rsc : bsm;
+        if (i0v < nrows) {
+            dst[i0v] = v0;
+            if (F::kRowScaled && SW) rsc[p.rows_cap + i0v] = v1;
+        }
+        for (int i = i0v + CW * 32; i < nrows; i += CW * 32) {
+            if constexpr (F::kRowScaled) {
+                rsc[i] = __ldg(p.rscale + r0 + i);
+                if (SW) rsc[p.rows_cap + i] = __ldg(p.rscale + p.n_ff + r0 + i);
+            } else {
+                bsm[i] = __ldg(p.bias + r0 + i);
+            }
+        }
+        if (F::kRowScaled && BIAS)
+            for (int i = i0v; i < nrows; i += CW * 32) bsm[i] = __ldg(p.bias + r0 + i);
+    }
     named_sync(1, CW * 32);
     if (threadIdx.x == 0) mbar_arrive(&x_bar);   // lifts the producer's in-flight limit
     if (warp >= CA) return;
@@ -834,11 +987,15 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
         v += __shfl_xor_sync(0xffffffffu, v, 2);
         v += __shfl_xor_sync(0xffffffffu, v, 1);
         const int n_here = b4 ? nB : nA;
-        if constexpr (SW) {
+        if (SW) {
             const float up = __shfl_down_sync(0xffffffffu, v, 8);   // lanes 0 and 16: the pair's up row
             if ((lane & 15) == 0 && gi < n_here) {
                 if (G == 1) {
-                    p.y[r0 + (u + (b4 ? 1 : 0)) * NG + gi] = silu(v) * up;
+                    const int pair = (u + (b4 ? 1 : 0)) * NG + gi;    // relative to r0
+                    if constexpr (F::kRowScaled)
+                        p.y[r0 + pair] = silu(v * rsc[pair]) * (up * rsc[p.rows_cap + pair]);
+                    else
+                        p.y[r0 + pair] = silu(v) * up;
                 } else {
                     const int row = (u + (b4 ? 1 : 0)) * RS + gi;    // stage-relative gate row
                     red[row * G + seg] = v;
@@ -847,49 +1004,60 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
             }
         } else if ((lane & 7) == 0 && my_t < n_here) {
             const int row = (u + (b4 ? 1 : 0)) * RS + my_t;     // relative to r0
-            if (G == 1)
-                p.y[r0 + row] = EPI == kEpiBias ? v + p.bias[r0 + row] : v;
-            else
+            if (G == 1) {
+                const float yv = F::kRowScaled ? v * rsc[row] : v;
+                p.y[r0 + row] = BIAS ? yv + bsm[row] : yv;
+            } else {
                 red[row * G + seg] = v;
+            }
         }
     }
     if (G > 1) {
         // partial sums of the G segments of each row, added in segment order
         named_sync(2, CA * 32);
         for (int i = warp * 32 + lane; i < nrows; i += CA * 32) {
-            if constexpr (SW) {
+            if (SW) {
                 const int row = (i / NG) * RS + i % NG;       // gate row of pair i; its up row is row + NG
                 float g = red[row * G], up = red[(row + NG) * G];
                 for (int g2 = 1; g2 < G; ++g2) {
                     g += red[row * G + g2];
                     up += red[(row + NG) * G + g2];
                 }
+                if constexpr (F::kRowScaled) {
+                    g *= rsc[i];
+                    up *= rsc[p.rows_cap + i];
+                }
                 p.y[r0 + i] = silu(g) * up;
             } else {
                 float sum = red[i * G];
                 for (int g2 = 1; g2 < G; ++g2) sum += red[i * G + g2];
-                p.y[r0 + i] = EPI == kEpiBias ? sum + p.bias[r0 + i] : sum;
+                if constexpr (F::kRowScaled) sum *= rsc[i];
+                p.y[r0 + i] = BIAS ? sum + bsm[i] : sum;
             }
         }
     }
 }
 
-// One launch over n_out rows (EPI none / bias), or over the 2 * n_ff rows of
-// a fused gate+up matrix writing n_ff SwiGLU outputs (EPI SwiGLU, n_out =
+// One launch over n_out rows (no epilogue or bias), or over the 2 * n_ff rows
+// of a fused gate+up matrix writing n_ff SwiGLU outputs (n_out =
 // 2 * n_ff); grid <= the number of items.
-template <class F, int EPI>
+template <class F>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y, int grid,
-                   cudaStream_t s, int early_w, const float *bias) {
-    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, (int)(n_out / 2), bias};
-    if (!plan(k, n_out, grid, F::kBlockBytes, p, EPI == kEpiSwiGLU)) return cudaErrorInvalidValue;
-    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p);
-    static PerDeviceOnce configured;
-    const cudaError_t ce = configured.run([] {
+                   cudaStream_t s, int early_w, const float *bias, int epi_kind) {
+    const float *rscale = F::kRowScaled ? reinterpret_cast<const float *>(w + i8row_scale_offset(n_out, k)) : nullptr;
+    Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, (int)(n_out / 2), bias, rscale, epi_kind};
+    if (!plan(k, n_out, grid, F::kBlockBytes, p, epi_kind == kEpiSwiGLU, F::kRowScaled, epi_kind == kEpiBias))
+        return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p) +
+                     rsc_bytes(p, F::kRowScaled, epi_kind == kEpiSwiGLU) + bias_bytes(p, epi_kind == kEpiBias);
+    auto kern = epi_kind == kEpiNone ? gemv_rows<F, false> : gemv_rows<F, true>;
+    static PerDeviceOnce configured[2];
+    const cudaError_t ce = configured[epi_kind == kEpiNone ? 0 : 1].run([kern] {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_rows<F, EPI>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
         if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(gemv_rows<F, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem - kStatic);
     });
     if (ce != cudaSuccess) return ce;
     cudaLaunchConfig_t cfg = {};
@@ -902,16 +1070,14 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows<F, EPI>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <class F>
 cudaError_t launch_epi(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y, int grid,
                        cudaStream_t s, int early_w, const Epilogue &epi) {
-    if (epi.kind == kEpiSwiGLU) return launch<F, kEpiSwiGLU>(w, n_out, k, x, y, grid, s, early_w, nullptr);
-    if (epi.kind == kEpiBias) return launch<F, kEpiBias>(w, n_out, k, x, y, grid, s, early_w, epi.bias);
-    return launch<F, kEpiNone>(w, n_out, k, x, y, grid, s, early_w, nullptr);
+    return launch<F>(w, n_out, k, x, y, grid, s, early_w, epi.kind == kEpiBias ? epi.bias : nullptr, epi.kind);
 }
 
 // Whether the whole-row kernel takes (fmt, k, n_out) at batch 1 (n_out = 2 *
@@ -924,6 +1090,8 @@ inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
     if (swiglu && (n_out % 2 || items < 1)) return false;
     if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, p, swiglu);
     if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p, swiglu);
+    if (fmt == PQ_Q8_0) return k % 256 == 0 && plan(k, n_out, grid, Q80::kBlockBytes, p, swiglu);
+    if (fmt == PQ_I8_ROW) return k % 256 == 0 && plan(k, n_out, grid, I8R::kBlockBytes, p, swiglu, true);
     return false;
 }
 }  // namespace rowk
@@ -1373,8 +1541,12 @@ cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int
     if (!stream_epilogue_fused(fmt, n_out, k, 1, epi.kind)) return cudaErrorInvalidValue;
     const int64_t items = epi.kind == kEpiSwiGLU ? n_out / 2 : n_out;
     const int grid = (int)(items < dev.sm_count ? items : dev.sm_count);
-    if (fmt == PQ_Q4_K) return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
-    return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    switch (fmt) {
+    case PQ_Q4_K: return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q6_K: return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q8_0: return rowk::launch_epi<rowk::Q80>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    default: return rowk::launch_epi<rowk::I8R>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    }
 }
 
 cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
@@ -1383,7 +1555,7 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
     if (!stream_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
     Params p{w, x, y, (long long)ldy, (int)n_out, (int)k, 0};
     const int grid = (int)(n_out < dev.sm_count ? n_out : dev.sm_count);
-    if (batch == 1 && (fmt == PQ_Q4_K || fmt == PQ_Q6_K) && rowk::takes(fmt, k, n_out))
+    if (batch == 1 && rowk::takes(fmt, k, n_out))
         return launch_gemv_stream_epi(fmt, w, n_out, k, x, y, s, dev, Epilogue{});
     if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
         return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);

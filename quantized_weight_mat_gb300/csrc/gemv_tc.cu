@@ -699,7 +699,8 @@ __global__ void __launch_bounds__(TM) tc_finish(const float *__restrict__ partia
 }
 
 // The sums of row r of tile t for all NBP columns: from ytmp when one CTA
-// computed the whole tile, else its CTAs' partial sums added in CTA order.
+// computed the whole tile, else its CTAs' partial sums added in CTA order
+// (the loads of up to four parts in flight at a time).
 template <int NBP>
 __device__ __forceinline__ void tile_sums(float (&sum)[NBP], int t, int r, const float *__restrict__ partials,
                                           const float *__restrict__ ytmp, long long total, int nb, int grid) {
@@ -716,13 +717,27 @@ __device__ __forceinline__ void tile_sums(float (&sum)[NBP], int t, int r, const
     }
 #pragma unroll
     for (int b = 0; b < NBP; ++b) sum[b] = 0.f;
-    for (int cc = cf; cc <= cl; ++cc) {
-        const int side = t == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
-        const float4 *part = reinterpret_cast<const float4 *>(partials + ((size_t)(cc * 2 + side) * TM + r) * NBP);
+    for (int c0 = cf; c0 <= cl; c0 += 4) {
+        float4 v[4][NBP / 4];
 #pragma unroll
-        for (int b4 = 0; b4 < NBP / 4; ++b4) {
-            const float4 q = part[b4];
-            sum[4 * b4] += q.x; sum[4 * b4 + 1] += q.y; sum[4 * b4 + 2] += q.z; sum[4 * b4 + 3] += q.w;
+        for (int u = 0; u < 4; ++u) {
+            const int cc = c0 + u;
+            if (cc <= cl) {
+                const int side = t == (int)(item_begin(cc, total, grid) / nb) ? 0 : 1;
+                const float4 *part = reinterpret_cast<const float4 *>(partials + ((size_t)(cc * 2 + side) * TM + r) * NBP);
+#pragma unroll
+                for (int b4 = 0; b4 < NBP / 4; ++b4) v[u][b4] = part[b4];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (c0 + u <= cl) {
+#pragma unroll
+                for (int b4 = 0; b4 < NBP / 4; ++b4) {
+                    sum[4 * b4] += v[u][b4].x; sum[4 * b4 + 1] += v[u][b4].y;
+                    sum[4 * b4 + 2] += v[u][b4].z; sum[4 * b4 + 3] += v[u][b4].w;
+                }
+            }
         }
     }
 }
@@ -736,21 +751,28 @@ __device__ __forceinline__ float silu_tc(float z) { return z / (1.0f + expf(-z))
 // (gate rows) and 2i+1 (up rows).  Launched after the main kernel with
 // programmatic dependent launch, like tc_finish.
 template <int NBP>
-__global__ void __launch_bounds__(TM) tc_finish_swiglu(const float *__restrict__ partials,
+__global__ void __launch_bounds__(2 * TM) tc_finish_swiglu(const float *__restrict__ partials,
                                                       const float *__restrict__ ytmp, float *__restrict__ h,
                                                       long long ldh, long long total, int nb, int grid, int n_ff,
                                                       int nb_cols) {
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int i = (int)blockIdx.x, r = threadIdx.x;
-    float g[NBP], u[NBP];
-    tile_sums<NBP>(g, 2 * i, r, partials, ytmp, total, nb, grid);
-    tile_sums<NBP>(u, 2 * i + 1, r, partials, ytmp, total, nb, grid);
+    // threads 0..127 sum the gate tile's row r, threads 128..255 the up tile's;
+    // the up sums reach the gate thread through shared memory
+    __shared__ float up_s[TM][NBP + 1];
+    const int i = (int)blockIdx.x, r = threadIdx.x % TM, half = threadIdx.x / TM;
+    float v[NBP];
+    tile_sums<NBP>(v, 2 * i + half, r, partials, ytmp, total, nb, grid);
+    if (half) {
+#pragma unroll
+        for (int b = 0; b < NBP; ++b) up_s[r][b] = v[b];
+    }
+    __syncthreads();
     const int j = i * TM + r;
-    if (j < n_ff) {
+    if (!half && j < n_ff) {
 #pragma unroll
         for (int b = 0; b < NBP; ++b)
-            if (b < nb_cols) h[(size_t)b * ldh + j] = silu_tc(g[b]) * u[b];
+            if (b < nb_cols) h[(size_t)b * ldh + j] = silu_tc(v[b]) * up_s[r][b];
     }
 }
 
@@ -869,6 +891,7 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     cfg.dynamicSmemBytes = 0;
     if (swiglu) {
         cfg.gridDim = dim3((unsigned)(ntiles / 2));
+        cfg.blockDim = dim3(2 * TM);
         e = cudaLaunchKernelEx(&cfg, tc_finish_swiglu<NBP>, (const float *)partials, (const float *)ytmp, y,
                                (long long)ldy, total, nb, grid, n_ff, batch);
         return e != cudaSuccess ? e : cudaGetLastError();

@@ -135,10 +135,10 @@ int choose(int fmt, int64_t n_out, int64_t k, int nb) {
     const bool tc_pays = nb >= 5 || (nb >= 3 && k >= 8192) || (nb == 4 && n_out * k >= (INT64_C(1) << 25));
     if (tc_pays && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
     if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
-    // Q6_K has a streaming kernel for one column only; one launch per column
-    // still beats the generic kernel (LM head 128256x4096: 2 x 65 us against
-    // 301 us at batch 2)
-    if (fmt == PQ_Q6_K && stream_supported(fmt, n_out, k, 1)) return PQ_KERNEL_STREAM;
+    // Q6_K, Q8_0 and per-row int8 have a streaming kernel for one column only;
+    // one launch per column still beats the generic kernel (Q6_K LM head
+    // 128256x4096: 2 x 65 us against 301 us at batch 2)
+    if (fmt != PQ_Q4_K && stream_supported(fmt, n_out, k, 1)) return PQ_KERNEL_STREAM;
     return PQ_KERNEL_GENERIC;
 }
 
@@ -201,7 +201,7 @@ int gemv_epi_impl(int fmt, const void *w_blocks, int n_out, int k, const float *
             if (kern == PQ_KERNEL_STREAM)
                 e = launch_gemv_stream(fmt, w, n_out, k, xb, nb, out, n_out, stream, *dev);
             else
-                e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, out, n_out, stream);
+                e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, out, n_out, stream, dev->sm_count);
             if (e == cudaSuccess)
                 e = sw ? launch_swiglu_rows(out, n_out / 2, nb, yb, ldy, stream)
                        : launch_add_bias(yb, epi.bias, n_out, ldy, nb, stream);
@@ -234,7 +234,7 @@ int gemv_impl(int fmt, const void *w_blocks, int n_out, int k, const float *x, i
         else if (kern == PQ_KERNEL_STREAM)
             e = launch_gemv_stream(fmt, w, n_out, k, xb, nb, yb, n_out, stream, *dev);
         else
-            e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, yb, n_out, stream);
+            e = launch_gemv_generic(fmt, w, n_out, k, xb, nb, yb, n_out, stream, dev->sm_count);
         return e == cudaSuccess ? PQ_OK : PQ_ERR_LAUNCH;
     });
 }

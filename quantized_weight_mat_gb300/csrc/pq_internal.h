@@ -70,7 +70,7 @@ cudaError_t launch_dequant(int fmt, const uint8_t *w, int64_t n_out, int64_t k, 
 
 cudaError_t launch_gemv_generic(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                                 const float *x, int batch, float *y, int64_t ldy,
-                                cudaStream_t s);
+                                cudaStream_t s, int sm_count);
 
 // Streaming kernel (bulk-copy ring).  `supported` reports whether it can run
 // this case; the launcher handles batch <= 4.

@@ -106,8 +106,8 @@ def test_kernel_choice_table():
             assert c in (pq.KERNEL_GENERIC, pq.KERNEL_STREAM, pq.KERNEL_TC)
             n = pq.pq_gemv_launches(fmt, 4096, k, b)
             # slices of up to 16 (tensor core) or 4 columns, or one column at a
-            # time for a one-column streaming kernel (Q6_K)
-            assert (b + 15) // 16 <= n <= (b if fmt == "q6_k" else (b + 3) // 4)
+            # time for a one-column streaming kernel (Q6_K, Q8_0, per-row int8)
+            assert (b + 15) // 16 <= n <= (b if fmt != "q4_k" else (b + 3) // 4)
 
 
 def test_generic_only_formats_take_the_generic_kernel():
@@ -160,3 +160,11 @@ def test_q4_k_dispatch_matches_the_measured_winners():
     # the Q6_K head streams one column at a time at any batch
     assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 4)] == [S, S, S]
     assert pq.pq_gemv_launches("q6_k", 128256, 4096, 4) == 4
+    # so do Q8_0 and per-row int8 when k is a multiple of 256 (whole-row
+    # kernel); other k take the generic kernel
+    for fmt in ("q8_0", "i8_row"):
+        assert [pq.pq_gemv_choice(fmt, 14336, 4096, b) for b in (1, 2, 4, 16)] == [S, S, S, S]
+        assert pq.pq_gemv_launches(fmt, 14336, 4096, 4) == 4
+        assert pq.pq_gemv_launches(fmt, 14336, 4096, 17) == 17
+    assert pq.pq_gemv_choice("q8_0", 896, 896, 1) == pq.KERNEL_GENERIC
+    assert pq.pq_gemv_choice("i8_row", 4096, 100, 1) == pq.KERNEL_GENERIC
