@@ -532,6 +532,7 @@ __device__ __forceinline__ void load_x_parts(uint32_t (&xh)[4][8], uint32_t (&xl
 // ---------------------------------------------------------------------------
 // Q4_K: lane owns sub-blocks 4h..4h+3 (chunks 2h, 2h+1) of its super-block.
 struct Q4K {
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 144;
     static constexpr bool kRowScaled = false;
     struct X {
@@ -592,6 +593,7 @@ struct Q4K {
 // words and realigns them with one byte permute each (selector fixed per lane,
 // since row and stage sizes are multiples of 16 bytes).
 struct Q6K {
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 210;
     static constexpr bool kRowScaled = false;
     struct X {
@@ -686,6 +688,7 @@ struct Q6K {
 // boundary).  Blocks 4h and 4h+2 start 2 bytes past a word boundary, so their
 // codes are realigned with one byte permute per word.
 struct Q80 {
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 272;
     static constexpr bool kRowScaled = false;
     struct X {
@@ -739,6 +742,7 @@ struct Q80 {
 struct I8R {
     static constexpr int kBlockBytes = 256;
     static constexpr bool kRowScaled = true;
+    static int64_t scale_offset(int64_t n_out, int64_t k) { return i8row_scale_offset(n_out, k); }
     struct X {
         uint32_t xh[8][4], xl[8][4];   // limbs of chunk (c + lane) mod 8, 16 positions each
         float u;
@@ -781,6 +785,134 @@ struct I8R {
         }
         // |dh|, |dl| <= 128 * 128 * 127 < 2^21: 254 dh + dl is exact in 32 bits
         return R.u * (float)(254 * dh + dl);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Q5_K: Q4_K's layout plus 32 bytes of fifth bits (qh at byte 16, qs at 48):
+// weight 64c + 32h + l takes bit 2c + h of qh[l] as 16.  The lane owns
+// sub-blocks 4hf..4hf+3 as in Q4_K; each code byte gets its fifth bit OR'ed
+// into bit 4, and the integer dot products run on 5-bit codes.
+struct Q5K {
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
+    static constexpr int kBlockBytes = 176;
+    static constexpr bool kRowScaled = false;
+    struct X {
+        uint32_t xh[4][8], xl[4][8];
+        int xs[4];
+        float u;
+        uint32_t mA, mB, qoff, hsh;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        load_x_parts(R.xh, R.xl, R.xs, R.u, ximg, xmeta, S, kbc, hf);
+        if (!valid) R.u = 0.f;
+        R.mA = hf ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+        R.mB = hf ? 0x30303030u : 0u;
+        R.qoff = 48u + 64u * (uint32_t)hf;
+        R.hsh = 4u * (uint32_t)hf;
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint4 hd = lds(blk);
+        const uint4 ha = lds(blk + 16u), hb = lds(blk + 32u);
+        const uint4 qa = lds(blk + R.qoff), qb = lds(blk + R.qoff + 16);
+        const uint4 qc = lds(blk + R.qoff + 32), qd = lds(blk + R.qoff + 48);
+        const uint32_t w0[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const uint32_t w1[8] = {qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
+        const uint32_t qh[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+        const uint32_t sc4 = ((hf ? hd.w : hd.y) & R.mA) | ((hd.y >> 2) & R.mB);
+        const uint32_t m4 = ((hf ? (hd.w >> 4) : hd.z) & R.mA) | ((hd.z >> 2) & R.mB);
+        int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0, dh2 = 0, dl2 = 0, dh3 = 0, dl3 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // bits 4hf..4hf+3 of each qh byte are the fifth bits of the lane's four sub-blocks
+            const uint32_t hb4 = qh[i] >> R.hsh;
+            const uint32_t c0 = (w0[i] & 0x0F0F0F0Fu) | ((hb4 << 4) & 0x10101010u);
+            const uint32_t c1 = ((w0[i] >> 4) & 0x0F0F0F0Fu) | ((hb4 << 3) & 0x10101010u);
+            const uint32_t c2 = (w1[i] & 0x0F0F0F0Fu) | ((hb4 << 2) & 0x10101010u);
+            const uint32_t c3 = ((w1[i] >> 4) & 0x0F0F0F0Fu) | ((hb4 << 1) & 0x10101010u);
+            dh0 = dp4a_us(c0, R.xh[0][i], dh0);
+            dl0 = dp4a_us(c0, R.xl[0][i], dl0);
+            dh1 = dp4a_us(c1, R.xh[1][i], dh1);
+            dl1 = dp4a_us(c1, R.xl[1][i], dl1);
+            dh2 = dp4a_us(c2, R.xh[2][i], dh2);
+            dl2 = dp4a_us(c2, R.xl[2][i], dl2);
+            dh3 = dp4a_us(c3, R.xh[3][i], dh3);
+            dl3 = dp4a_us(c3, R.xl[3][i], dl3);
+        }
+        const int s0 = byte_of(sc4, 0), s1 = byte_of(sc4, 1), s2 = byte_of(sc4, 2), s3 = byte_of(sc4, 3);
+        const int H = s0 * dh0 + s1 * dh1 + s2 * dh2 + s3 * dh3;        // |H| < 2^25
+        const int L = s0 * dl0 + s1 * dl1 + s2 * dl2 + s3 * dl3;
+        const int M = byte_of(m4, 0) * R.xs[0] + byte_of(m4, 1) * R.xs[1] +
+                      byte_of(m4, 2) * R.xs[2] + byte_of(m4, 3) * R.xs[3];
+        const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+        return R.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Per-row int4: a row is k/2 bytes, weight 2i in the low nibble of byte i;
+// the lane owns 128 weights (64 bytes).  XOR with 0x88 turns each two's-
+// complement code q into q + 8 (0..15), so the integer dot products run on
+// unsigned codes and 8 * (sum of x) is subtracted; low nibbles meet the even
+// positions' x limbs and high nibbles (kept in place, 16 (q + 8)) the odd
+// ones, split apart once at load.  As for per-row int8 the lanes' ranges
+// would share banks, so lane l reads its four 16-byte chunks in the order
+// (c + l/2) mod 4.  The row's f32 scale multiplies the reduced sum.
+struct I4R {
+    static constexpr int kBlockBytes = 128;
+    static constexpr bool kRowScaled = true;
+    static int64_t scale_offset(int64_t n_out, int64_t k) { return i4row_scale_offset(n_out, k); }
+    struct X {
+        uint32_t eh[4][4], el[4][4], oh[4][4], ol[4][4];   // chunk (c + lane/2) mod 4: even / odd limbs
+        int xs;                                          // sum of 254 xh + xl over the lane's 128 positions
+        float u;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        uint32_t xh[4][8], xl[4][8];
+        int xs32[4];
+        load_x_parts(xh, xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
+        if (!valid) R.u = 0.f;
+        R.xs = xs32[0] + xs32[1] + xs32[2] + xs32[3];
+        const int rot = (threadIdx.x & 31) >> 1;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int m = (c + rot) & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t ah = 0, bh = 0, al = 0, bl = 0;
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm)
+                    if (mm == m) { ah = xh[mm][2 * i]; bh = xh[mm][2 * i + 1]; al = xl[mm][2 * i]; bl = xl[mm][2 * i + 1]; }
+                R.eh[c][i] = __byte_perm(ah, bh, 0x6420u);
+                R.oh[c][i] = __byte_perm(ah, bh, 0x7531u);
+                R.el[c][i] = __byte_perm(al, bl, 0x6420u);
+                R.ol[c][i] = __byte_perm(al, bl, 0x7531u);
+            }
+        }
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint32_t a = blk + 64u * (uint32_t)hf;
+        const uint32_t rot = (threadIdx.x & 31u) >> 1;
+        int eh = 0, el = 0, oh = 0, ol = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 q = lds(a + 16u * ((c + rot) & 3u));
+            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = (qw[i] ^ 0x88888888u) & 0x0F0F0F0Fu;     // q + 8 of even weights
+                const uint32_t hi = (qw[i] ^ 0x88888888u) & 0xF0F0F0F0u;     // 16 (q + 8) of odd weights
+                eh = dp4a_us(lo, R.eh[c][i], eh);
+                el = dp4a_us(lo, R.el[c][i], el);
+                oh = dp4a_us(hi, R.oh[c][i], oh);
+                ol = dp4a_us(hi, R.ol[c][i], ol);
+            }
+        }
+        // 16 * sum (q + 8) X, exact in 32 bits (|.| < 2^22), then minus 16 * 8 * sum X
+        const float h16 = (float)(16 * eh + oh), l16 = (float)(16 * el + ol);
+        return R.u * 0.0625f * (fmaf(254.0f, h16, l16) - 128.0f * (float)R.xs);
     }
 };
 
@@ -1044,7 +1176,7 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
 template <class F>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y, int grid,
                    cudaStream_t s, int early_w, const float *bias, int epi_kind) {
-    const float *rscale = F::kRowScaled ? reinterpret_cast<const float *>(w + i8row_scale_offset(n_out, k)) : nullptr;
+    const float *rscale = F::kRowScaled ? reinterpret_cast<const float *>(w + F::scale_offset(n_out, k)) : nullptr;
     Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, (int)(n_out / 2), bias, rscale, epi_kind};
     if (!plan(k, n_out, grid, F::kBlockBytes, p, epi_kind == kEpiSwiGLU, F::kRowScaled, epi_kind == kEpiBias))
         return cudaErrorInvalidValue;
@@ -1092,6 +1224,8 @@ inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
     if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p, swiglu);
     if (fmt == PQ_Q8_0) return k % 256 == 0 && plan(k, n_out, grid, Q80::kBlockBytes, p, swiglu);
     if (fmt == PQ_I8_ROW) return k % 256 == 0 && plan(k, n_out, grid, I8R::kBlockBytes, p, swiglu, true);
+    if (fmt == PQ_Q5_K) return plan(k, n_out, grid, Q5K::kBlockBytes, p, swiglu);
+    if (fmt == PQ_I4_ROW) return k % 256 == 0 && plan(k, n_out, grid, I4R::kBlockBytes, p, swiglu, true);
     return false;
 }
 }  // namespace rowk
@@ -1545,6 +1679,8 @@ cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int
     case PQ_Q4_K: return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q6_K: return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q8_0: return rowk::launch_epi<rowk::Q80>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q5_K: return rowk::launch_epi<rowk::Q5K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_I4_ROW: return rowk::launch_epi<rowk::I4R>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     default: return rowk::launch_epi<rowk::I8R>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     }
 }
