@@ -916,6 +916,166 @@ struct I4R {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Q2_K (84 bytes: 16 scale/min bytes, 64 bytes of 2-bit codes, f16 d, dmin):
+// weight 128n + 32j + l takes bits 2j, 2j+1 of qs[32n + l]; its group of 16
+// (i / 16) has scale = low nibble, min = high nibble of scales[i / 16].  The
+// lane owns half n = hf: codes qs[32hf..32hf+31], groups 8hf..8hf+7.  Blocks
+// are 4-byte aligned, so every read is a 32-bit word.
+struct Q2K {
+    static constexpr int kBlockBytes = 84;
+    static constexpr bool kRowScaled = false;
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
+    struct X {
+        uint32_t xh[4][8], xl[4][8];
+        int xs[8];          // sum of 254 xh + xl over each group of 16
+        float u;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t) {
+        int xs32[4];
+        load_x_parts(R.xh, R.xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            int sh = 0, sl = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                sh = dp4a_ss(R.xh[g >> 1][4 * (g & 1) + i], 0x01010101u, sh);
+                sl = dp4a_ss(R.xl[g >> 1][4 * (g & 1) + i], 0x01010101u, sl);
+            }
+            R.xs[g] = 254 * sh + sl;
+        }
+        if (!valid) R.u = 0.f;
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = lds32(blk + 16u + 32u * (uint32_t)hf + 4u * (uint32_t)i);
+        const uint32_t s0 = lds32(blk + 8u * (uint32_t)hf), s1 = lds32(blk + 8u * (uint32_t)hf + 4u);
+        const uint32_t dd = lds32(blk + 80u);
+        int H = 0, L = 0, M = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            // groups 2t (words 0-3) and 2t+1 (words 4-7) of part t
+            int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t c0 = (q[i] >> (2 * t)) & 0x03030303u;
+                const uint32_t c1 = (q[4 + i] >> (2 * t)) & 0x03030303u;
+                dh0 = dp4a_us(c0, R.xh[t][i], dh0);
+                dl0 = dp4a_us(c0, R.xl[t][i], dl0);
+                dh1 = dp4a_us(c1, R.xh[t][4 + i], dh1);
+                dl1 = dp4a_us(c1, R.xl[t][4 + i], dl1);
+            }
+            const uint32_t sw = t < 2 ? s0 : s1;
+            const int g0 = byte_of(sw, 2 * (t & 1)), g1 = byte_of(sw, 2 * (t & 1) + 1);
+            H += (g0 & 15) * dh0 + (g1 & 15) * dh1;
+            L += (g0 & 15) * dl0 + (g1 & 15) * dl1;
+            M += (g0 >> 4) * R.xs[2 * t] + (g1 >> 4) * R.xs[2 * t + 1];
+        }
+        const float d = h2f(dd), dmin = h2f(dd >> 16);
+        return R.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Q3_K (110 bytes: hmask[32], 64 bytes of 2-bit codes, 12 bytes of sixteen
+// signed 6-bit scales, f16 d): weight 128n + 32j + l takes bits 2j, 2j+1 of
+// qs[32n + l] as a code and bit 4n + j of hmask[l] as its high bit, value =
+// code - 4 when that bit is clear, code when set; group i / 16 has scale
+// (low nibble of byte s (s < 8) or high nibble of byte s - 8, with bits
+// 2(s/4), 2(s/4)+1 of byte 8 + s % 4 on top) - 32.  The lane owns half n =
+// hf; code | high << 2 = value + 4 (0..7) feeds the dot products and 4 * (sum
+// of x) per group is subtracted.  Blocks may start 2 bytes past a word
+// boundary: the lane reads aligned words and realigns each with one permute.
+struct Q3K {
+    static constexpr int kBlockBytes = 110;
+    static constexpr bool kRowScaled = false;
+    static int64_t scale_offset(int64_t, int64_t) { return 0; }
+    struct X {
+        uint32_t xh[4][8], xl[4][8];
+        int xs[8];          // sum of 254 xh + xl over each group of 16
+        float u;
+        uint32_t delta, sel, dsh;
+    };
+    static __device__ __forceinline__ void load(X &R, const uint8_t *ximg, const uint8_t *xmeta, int S,
+                                                int kbc, int hf, bool valid, uint32_t lane_base) {
+        int xs32[4];
+        load_x_parts(R.xh, R.xl, xs32, R.u, ximg, xmeta, S, kbc, hf);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            int sh = 0, sl = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                sh = dp4a_ss(R.xh[g >> 1][4 * (g & 1) + i], 0x01010101u, sh);
+                sl = dp4a_ss(R.xl[g >> 1][4 * (g & 1) + i], 0x01010101u, sl);
+            }
+            R.xs[g] = 254 * sh + sl;
+        }
+        if (!valid) R.u = 0.f;
+        R.delta = lane_base & 2u;
+        R.sel = R.delta ? 0x5432u : 0x3210u;
+        R.dsh = R.delta ? 16u : 0u;
+    }
+    static __device__ __forceinline__ float dot(uint32_t blk, const X &R, int hf) {
+        const uint32_t a = blk - R.delta;
+        uint32_t hm[8], q[8], sc[3];
+        {
+            uint32_t w[9];
+#pragma unroll
+            for (int j = 0; j < 9; ++j) w[j] = lds32(a + 4u * (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hm[j] = __byte_perm(w[j], w[j + 1], R.sel) >> (4u * (uint32_t)hf);
+        }
+        {
+            uint32_t w[9];
+#pragma unroll
+            for (int j = 0; j < 9; ++j) w[j] = lds32(a + 32u + 32u * (uint32_t)hf + 4u * (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = __byte_perm(w[j], w[j + 1], R.sel);
+        }
+        uint32_t dw;
+        {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = lds32(a + 96u + 4u * (uint32_t)j);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) sc[j] = __byte_perm(w[j], w[j + 1], R.sel);
+            dw = lds32(a + 108u) >> R.dsh;
+        }
+        // signed scales of the lane's groups g = 0..7 (absolute 8hf + g)
+        const uint32_t lo = hf ? ((sc[0] >> 4) & 0x0F0F0F0Fu) : (sc[0] & 0x0F0F0F0Fu);
+        const uint32_t lo2 = hf ? ((sc[1] >> 4) & 0x0F0F0F0Fu) : (sc[1] & 0x0F0F0F0Fu);
+        const uint32_t hi = sc[2] >> (4u * (uint32_t)hf);       // bits 2(g/4) + 4hf of byte g % 4
+        int H = 0, L = 0, M = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t c0 = ((q[i] >> (2 * t)) & 0x03030303u) | (((hm[i] >> t) & 0x01010101u) << 2);
+                const uint32_t c1 = ((q[4 + i] >> (2 * t)) & 0x03030303u) | (((hm[4 + i] >> t) & 0x01010101u) << 2);
+                dh0 = dp4a_us(c0, R.xh[t][i], dh0);
+                dl0 = dp4a_us(c0, R.xl[t][i], dl0);
+                dh1 = dp4a_us(c1, R.xh[t][4 + i], dh1);
+                dl1 = dp4a_us(c1, R.xl[t][4 + i], dl1);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int g = 2 * t + e;
+                const int lo4 = byte_of(g < 4 ? lo : lo2, g & 3);
+                const int hi2 = (byte_of(hi, g & 3) >> (2 * (g >> 2))) & 3;
+                const int scg = (lo4 | (hi2 << 4)) - 32;
+                H += scg * (e ? dh1 : dh0);
+                L += scg * (e ? dl1 : dl0);
+                M += scg * R.xs[g];
+            }
+        }
+        // sum of value * X = sum of (value + 4) * X - 4 * sum of X, per group
+        return R.u * h2f(dw) * (fmaf(254.0f, (float)H, (float)L) - 4.0f * (float)M);
+    }
+};
+
 // Rows gi and gi+NG of one stage (lane base address s); CHECK handles a
 // partial last stage (v0, v1: whether each row is present).
 template <class F, bool CHECK>
@@ -1226,6 +1386,8 @@ inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
     if (fmt == PQ_I8_ROW) return k % 256 == 0 && plan(k, n_out, grid, I8R::kBlockBytes, p, swiglu, true);
     if (fmt == PQ_Q5_K) return plan(k, n_out, grid, Q5K::kBlockBytes, p, swiglu);
     if (fmt == PQ_I4_ROW) return k % 256 == 0 && plan(k, n_out, grid, I4R::kBlockBytes, p, swiglu, true);
+    if (fmt == PQ_Q2_K) return plan(k, n_out, grid, Q2K::kBlockBytes, p, swiglu);
+    if (fmt == PQ_Q3_K) return plan(k, n_out, grid, Q3K::kBlockBytes, p, swiglu);
     return false;
 }
 }  // namespace rowk
@@ -1681,6 +1843,8 @@ cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int
     case PQ_Q8_0: return rowk::launch_epi<rowk::Q80>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q5_K: return rowk::launch_epi<rowk::Q5K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_I4_ROW: return rowk::launch_epi<rowk::I4R>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q2_K: return rowk::launch_epi<rowk::Q2K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q3_K: return rowk::launch_epi<rowk::Q3K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     default: return rowk::launch_epi<rowk::I8R>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     }
 }

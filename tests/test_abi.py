@@ -110,24 +110,21 @@ def test_kernel_choice_table():
             assert (b + 15) // 16 <= n <= (b if fmt != "q4_k" else (b + 3) // 4)
 
 
-def test_generic_only_formats_take_the_generic_kernel():
-    # Q3_K / Q2_K run on the generic kernel at every batch, 4 columns a launch
-    for fmt in ("q3_k", "q2_k"):
-        assert pq.pq_gemv_choice(fmt, 4096, 100, 1) == pq.PQ_ERR_K
-        for b in (1, 2, 4, 5, 16, 17):
-            assert pq.pq_gemv_choice(fmt, 4096, 4096, b) == pq.KERNEL_GENERIC
-            assert pq.pq_gemv_launches(fmt, 4096, 4096, b) == (b + 3) // 4
-
-
-def test_q5_k_and_int4_rows_stream_one_column_at_a_time():
-    # Q5_K and per-row int4 (k a multiple of 256) take the whole-row kernel,
-    # one launch per column; per-row int4 with other k the generic kernel
-    S = pq.KERNEL_STREAM
-    for fmt in ("q5_k", "i4_row"):
+def test_k_family_and_int4_rows_stream_one_column_at_a_time():
+    # Q5_K, Q3_K, Q2_K and per-row int4 take the whole-row kernel, one launch
+    # per column, when a row is a whole number of 16-byte units (Q3_K: k a
+    # multiple of 2048, Q2_K of 1024); other k take the generic kernel, 4
+    # columns a launch
+    S, G = pq.KERNEL_STREAM, pq.KERNEL_GENERIC
+    for fmt in ("q5_k", "q3_k", "q2_k", "i4_row"):
         for b in (1, 2, 4, 5, 16, 17):
             assert pq.pq_gemv_choice(fmt, 4096, 4096, b) == S
             assert pq.pq_gemv_launches(fmt, 4096, 4096, b) == b
-    assert pq.pq_gemv_choice("i4_row", 4096, 100, 1) == pq.KERNEL_GENERIC
+    for fmt, k in (("q3_k", 1024), ("q2_k", 768), ("i4_row", 100)):
+        for b in (1, 5):
+            assert pq.pq_gemv_choice(fmt, 4096, k, b) == G
+            assert pq.pq_gemv_launches(fmt, 4096, k, b) == (b + 3) // 4
+    assert pq.pq_gemv_choice("q2_k", 4096, 100, 1) == pq.PQ_ERR_K
     assert pq.pq_gemv_choice("i4_row", 4096, 101, 1) == pq.PQ_ERR_K
 
 
