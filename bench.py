@@ -183,7 +183,9 @@ CONFIGS = [
 ] + [("Q4_K QKV 6144x4096 with bias, batch 1", "q4_k", 6144, 4096, 1, "bias"),
      ("Q4_K gate+up 28672x4096 with SwiGLU, batch 1", "q4_k", 28672, 4096, 1, "swiglu"),
      ("Q4_K gate+up 28672x4096 with SwiGLU, batch 8", "q4_k", 28672, 4096, 8, "swiglu"),
-     ("Q4_K gate+up 28672x4096, batch 8", "q4_k", 28672, 4096, 8)]
+     ("Q4_K gate+up 28672x4096, batch 8", "q4_k", 28672, 4096, 8),
+     ("Q4_K 14336x4096, batch 32 (prompt width)", "q4_k", 14336, 4096, 32),
+     ("Q4_K 4096x14336, batch 32 (prompt width)", "q4_k", 4096, 14336, 32)]
 
 
 def per_config(pq, dev, peak, l2_bytes):

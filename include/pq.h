@@ -95,7 +95,9 @@ typedef enum {
  *   x         device f32 [batch][k] row-major, 16-byte aligned.  Read only.
  *   y         device f32 [batch][n_out] row-major; fully overwritten (not
  *             accumulated into).  Must not overlap w_blocks or x.
- *   batch     >= 1.  Batches above 16 are processed in chunks of at most 16.
+ *   batch     >= 1.  Batches above 32 are processed in chunks of at most 32
+ *             (the tensor-core kernel takes up to 32 columns per pass over
+ *             W; the CUDA-core kernels up to 4, or one).
  *
  * Accuracy: partial sums are accumulated in f32; the result agrees with the
  * exact dot product of the decoded f32 weights within
@@ -168,7 +170,7 @@ const char *pq_strerror(int status);
  *   PQ_KERNEL_GENERIC  warp-per-row kernel, any format / shape / batch
  *   PQ_KERNEL_STREAM   bulk-copy ring + integer dot products (Q4_K at
  *                      batch 1-4, Q6_K at batch 1)
- *   PQ_KERNEL_TC       tcgen05 tensor-core kernel (Q4_K, batch 1-16, k a
+ *   PQ_KERNEL_TC       tcgen05 tensor-core kernel (Q4_K, batch 1-32, k a
  *                      multiple of 256 up to 65536; pq_gemv chooses it at
  *                      batch >= 5, and at batch 3-4 for long rows or large
  *                      matrices)
@@ -189,7 +191,7 @@ int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch);
 
 /*
  * Number of batch slices one pq_gemv call with these arguments runs (slices
- * of up to 16 columns for the tensor-core kernel, up to 4 otherwise), each
+ * of up to 32 columns for the tensor-core kernel, up to 4 or 1 otherwise), each
  * with one kernel choice.  A slice is one launch of its kernel, plus, for the
  * tensor-core and the batch-2 long-row kernels, one small x-conversion launch
  * before it, and for the tensor-core kernel one split-K finishing launch after

@@ -66,15 +66,20 @@ constexpr int RAW_BYTES = TM * 144;           // one super-block column of a til
 #define PQ_TC_ABUFS 2
 #endif
 constexpr int A_BUFS = PQ_TC_ABUFS;           // super-blocks in flight between decoders, MMA and epilogue
-constexpr int A_SLOTS = 4 * A_BUFS;           // 64-weight slots
 constexpr int TMEM_COLS = 512;
-constexpr int A_COL = TMEM_COLS - 32 * A_SLOTS;   // TMEM column of A slot 0 (32 columns per slot)
-constexpr int AMIN_COL = A_COL - 8 * A_BUFS;       // mins operand of buffer b: 8 columns at AMIN_COL + 8b
 constexpr int DEC_WARPS = 16, EPI_WARPS = 4;
 constexpr int PRODUCER_WARP = DEC_WARPS + EPI_WARPS;
 constexpr int MMA_WARP = PRODUCER_WARP + 1;   // MMA_WARP + 2*buf + half: see the issuer role
-constexpr int MMA_WARPS = 2 * A_BUFS;
-constexpr int THREADS = (MMA_WARP + MMA_WARPS) * 32;
+
+// Per column count: the 32-column kernel keeps one super-block in flight (its
+// three 64-column accumulators and A slots fill the 512 TMEM columns), the
+// others two.
+template <int NBP> __host__ __device__ constexpr int tc_abufs() { return NBP == 32 ? 1 : A_BUFS; }
+template <int NBP> __host__ __device__ constexpr int tc_threads() { return (MMA_WARP + 2 * tc_abufs<NBP>()) * 32; }
+// TMEM column of A slot 0 (32 columns per 64-weight slot, four slots per
+// buffer) and of the mins operand of buffer b (8 columns at tc_amin_col + 8b)
+template <int NBP> __host__ __device__ constexpr int tc_a_col() { return TMEM_COLS - 32 * 4 * tc_abufs<NBP>(); }
+template <int NBP> __host__ __device__ constexpr int tc_amin_col() { return tc_a_col<NBP>() - 8 * tc_abufs<NBP>(); }
 constexpr int kMaxGrid = 160;                 // CTAs at most (partial-sum slots are sized for it)
 
 // x image of one super-block for NBP columns (N' = 2*NBP MMA columns, the hi
@@ -88,10 +93,12 @@ template <int NBP> __host__ __device__ constexpr int xmins_bytes() { return 2 * 
 template <int NBP> __host__ __device__ constexpr int xscale_off() { return xmain_bytes<NBP>() + xmins_bytes<NBP>(); }
 template <int NBP> __host__ __device__ constexpr int btile_bytes() { return xscale_off<NBP>() + 128; }
 static_assert(16 * 4 <= 128, "one f32 factor per column fits the scale area");
-template <int NBP> __host__ __device__ constexpr int raw_stages() { return NBP == 16 ? 6 : 8; }
+template <int NBP> __host__ __device__ constexpr int raw_stages() { return NBP == 32 ? 4 : NBP == 16 ? 6 : 8; }
 template <int NBP> __host__ __device__ constexpr int stage_bytes() { return RAW_BYTES + btile_bytes<NBP>(); }
 template <int NBP> __host__ __device__ constexpr int smem_bytes() { return raw_stages<NBP>() * stage_bytes<NBP>() + 1024; }
-static_assert(stage_bytes<8>() % 128 == 0 && stage_bytes<16>() % 128 == 0, "stage alignment");
+static_assert(stage_bytes<8>() % 128 == 0 && stage_bytes<16>() % 128 == 0 && stage_bytes<32>() % 128 == 0,
+              "stage alignment");
+static_assert(smem_bytes<32>() <= 227 * 1024 && smem_bytes<16>() <= 227 * 1024, "shared memory per CTA");
 
 // Scratch of one call: x image, then partial sums [grid][2][TM][NBP] (slot
 // 2c: CTA c's first tile, 2c+1: its last tile, when split).
@@ -362,14 +369,16 @@ __device__ __forceinline__ int item_owner(long long i, long long total, int grid
 }
 
 template <int NBP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(tc_threads<NBP>(), 1)
     gemv_tc_q4_k(const __grid_constant__ CUtensorMap wmap, TcParams p) {
     constexpr int NP = 2 * NBP;
     constexpr int NSR = raw_stages<NBP>();
     constexpr int STAGE = stage_bytes<NBP>();
     constexpr uint32_t IDESC = instr_desc(TM, NP);
+    constexpr int A_BUFS = tc_abufs<NBP>();
+    constexpr int A_COL = tc_a_col<NBP>(), AMIN_COL = tc_amin_col<NBP>();
     static_assert(3 * A_BUFS * NP <= AMIN_COL, "accumulators below the A operands");
-    static_assert(A_COL + 32 * A_SLOTS <= TMEM_COLS, "A slots fit in the allocation");
+    static_assert(A_COL + 32 * 4 * A_BUFS <= TMEM_COLS, "A slots fit in the allocation");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
@@ -497,25 +506,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float d = h2f(dd), dmin = h2f(dd >> 16);
             // the super-block's three accumulators (two halves of the products,
             // the mins product), each with hi and lo x columns, in scaled units
-            float v[NBP];
+            if constexpr (NBP == 8) {
+                float v[NBP];
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {
-                const uint32_t taddr = row_taddr + (uint32_t)((3 * buf + part) * NP);
-                const float sc = part < 2 ? d : -dmin;
-                if constexpr (NP == 32) {
-                    // hi columns, then lo columns: 16 registers at a time (the
-                    // 800-thread block leaves 72 registers per thread)
-#pragma unroll
-                    for (int hl = 0; hl < 2; ++hl) {
-                        uint32_t t[16];
-                        tmem_ld16(taddr + (uint32_t)(16 * hl), t);
-                        tmem_ld_wait(t);
-#pragma unroll
-                        for (int b = 0; b < NBP; ++b)
-                            v[b] = (part == 0 && hl == 0) ? sc * __uint_as_float(t[b])
-                                                          : fmaf(sc, __uint_as_float(t[b]), v[b]);
-                    }
-                } else {
+                for (int part = 0; part < 3; ++part) {
+                    const uint32_t taddr = row_taddr + (uint32_t)((3 * buf + part) * NP);
+                    const float sc = part < 2 ? d : -dmin;
                     uint32_t t[16];
                     tmem_ld16(taddr, t);
                     tmem_ld_wait(t);
@@ -525,9 +521,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                         v[b] = part == 0 ? sc * pr : fmaf(sc, pr, v[b]);
                     }
                 }
-            }
 #pragma unroll
-            for (int b = 0; b < NBP; ++b) yacc[b] = fmaf(v[b], __shfl_sync(0xffffffffu, undo, b), yacc[b]);
+                for (int b = 0; b < NBP; ++b) yacc[b] = fmaf(v[b], __shfl_sync(0xffffffffu, undo, b), yacc[b]);
+            } else {
+                // 16 columns at a time: their hi columns, then their lo
+                // columns, 16 registers each (the 800- and 736-thread blocks
+                // leave 72 and 80 registers per thread)
+#pragma unroll
+                for (int grp = 0; grp < NBP / 16; ++grp) {
+                    float v[16];
+#pragma unroll
+                    for (int part = 0; part < 3; ++part) {
+                        const uint32_t taddr = row_taddr + (uint32_t)((3 * buf + part) * NP + 16 * grp);
+                        const float sc = part < 2 ? d : -dmin;
+#pragma unroll
+                        for (int hl = 0; hl < 2; ++hl) {
+                            uint32_t t[16];
+                            tmem_ld16(taddr + (uint32_t)(NBP * hl), t);
+                            tmem_ld_wait(t);
+#pragma unroll
+                            for (int b = 0; b < 16; ++b)
+                                v[b] = (part == 0 && hl == 0) ? sc * __uint_as_float(t[b])
+                                                              : fmaf(sc, __uint_as_float(t[b]), v[b]);
+                        }
+                    }
+#pragma unroll
+                    for (int b = 0; b < 16; ++b)
+                        yacc[16 * grp + b] = fmaf(v[b], __shfl_sync(0xffffffffu, undo, 16 * grp + b), yacc[16 * grp + b]);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -872,6 +894,7 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     e = configured.run([] {
         return cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
     });
+    static_assert(tc_threads<NBP>() <= 1024, "block size");
     if (e != cudaSuccess) return e;
     const long long ntiles = tc_tiles(n_out, epi);
     const long long total = ntiles * nb;
@@ -879,7 +902,7 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
                epi.kind == kEpiBias ? epi.bias : nullptr, n_ff, swiglu ? ytmp : nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(tc_threads<NBP>());
     cfg.dynamicSmemBytes = (size_t)smem_bytes<NBP>();
     cfg.stream = s;
     cfg.attrs = attr;
@@ -933,7 +956,7 @@ int noalloc_max_k() { return kNoAllocMaxK; }
 
 cudaError_t launch_gemv_tc_noalloc(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
                                    float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev) {
-    if (!tc_supported(PQ_Q4_K, n_out, k, batch) || k > kNoAllocMaxK) return cudaErrorInvalidValue;
+    if (!tc_supported(PQ_Q4_K, n_out, k, batch) || batch > 16 || k > kNoAllocMaxK) return cudaErrorInvalidValue;
     uint8_t *scratch = noalloc_scratch_ptr();
     if (!scratch) return cudaErrorInvalidSymbol;
     const int grid = tc_grid(n_out, k, dev);
@@ -952,7 +975,7 @@ unsigned tc_wait_timeouts(bool reset) {
 }
 
 bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch) {
-    return fmt == PQ_Q4_K && batch >= 1 && batch <= 16 && n_out >= 1 && k % 256 == 0 && k >= 256 &&
+    return fmt == PQ_Q4_K && batch >= 1 && batch <= 32 && n_out >= 1 && k % 256 == 0 && k >= 256 &&
            k <= 65536;
 }
 
@@ -961,14 +984,17 @@ cudaError_t launch_gemv_tc(int fmt, const uint8_t *w, int64_t n_out, int64_t k, 
     if (!tc_supported(fmt, n_out, k, batch)) return cudaErrorInvalidValue;
     if (epi.kind == kEpiSwiGLU && (n_out % 2 || n_out < 2)) return cudaErrorInvalidValue;
     const int grid = tc_grid(n_out, k, dev, epi);
-    const size_t bytes = batch <= 8 ? scratch_bytes_epi<8>(n_out, k, grid, epi) : scratch_bytes_epi<16>(n_out, k, grid, epi);
+    const size_t bytes = batch <= 8    ? scratch_bytes_epi<8>(n_out, k, grid, epi)
+                         : batch <= 16 ? scratch_bytes_epi<16>(n_out, k, grid, epi)
+                                       : scratch_bytes_epi<32>(n_out, k, grid, epi);
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
     void *scratch = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&scratch, bytes, pool, s);
     if (e != cudaSuccess) return e;
-    e = batch <= 8 ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi)
-                   : launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi);
+    e = batch <= 8    ? launch_nbp<8>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi)
+        : batch <= 16 ? launch_nbp<16>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi)
+                      : launch_nbp<32>(w, n_out, k, x, batch, y, ldy, s, grid, (uint8_t *)scratch, epi);
     const cudaError_t f = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : f;
 }

@@ -142,13 +142,14 @@ int choose(int fmt, int64_t n_out, int64_t k, int nb) {
     return PQ_KERNEL_GENERIC;
 }
 
-// Chunking of the batch: chunks of up to 16 columns; a chunk that no
+// Chunking of the batch: chunks of up to 32 columns (the tensor-core kernel
+// takes 1-32: one pass over W for a 32-row prompt); a chunk that no
 // tensor-core kernel takes is split further into chunks of up to 4, and into
-// single columns for a streaming kernel that only takes one (Q6_K).
+// single columns for a streaming kernel that only takes one.
 template <class F>
 int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &&f) {
     for (int b0 = 0; b0 < batch;) {
-        int nb = batch - b0 < 16 ? batch - b0 : 16;
+        int nb = batch - b0 < 32 ? batch - b0 : 32;
         int kern = forced >= 0 ? forced : choose(fmt, n_out, k, nb);
         if (kern != PQ_KERNEL_TC && nb > 4) nb = 4;
         // a streaming kernel that takes one column at a time runs column by column
@@ -309,7 +310,7 @@ int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch) {
     int st = check_common((int)fmt, (const void *)16, n_out, k);
     if (st) return st;
     if (batch <= 0) return PQ_ERR_ARG;
-    return choose((int)fmt, n_out, k, batch < 16 ? batch : 16);
+    return choose((int)fmt, n_out, k, batch < 32 ? batch : 32);
 }
 
 int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch) {

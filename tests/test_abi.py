@@ -105,9 +105,9 @@ def test_kernel_choice_table():
             c = pq.pq_gemv_choice(fmt, 4096, k, b)
             assert c in (pq.KERNEL_GENERIC, pq.KERNEL_STREAM, pq.KERNEL_TC)
             n = pq.pq_gemv_launches(fmt, 4096, k, b)
-            # slices of up to 16 (tensor core) or 4 columns, or one column at a
+            # slices of up to 32 (tensor core) or 4 columns, or one column at a
             # time for a one-column streaming kernel (Q6_K, Q8_0, per-row int8)
-            assert (b + 15) // 16 <= n <= (b if fmt != "q4_k" else (b + 3) // 4)
+            assert (b + 31) // 32 <= n <= (b if fmt != "q4_k" else (b + 3) // 4)
 
 
 def test_k_family_and_int4_rows_stream_one_column_at_a_time():
@@ -165,6 +165,10 @@ def test_q4_k_dispatch_matches_the_measured_winners():
     for (n, k), want in table.items():
         got = [pq.pq_gemv_choice("q4_k", n, k, b) for b in (1, 2, 3, 4, 5, 8, 16)]
         assert got == want, (n, k, got)
+    # prompt width: up to 32 columns in one tensor-core pass over W
+    for b, launches in ((17, 1), (32, 1), (33, 2), (64, 2), (65, 3)):
+        assert pq.pq_gemv_choice("q4_k", 14336, 4096, b) == T
+        assert pq.pq_gemv_launches("q4_k", 14336, 4096, b) == launches
     # the Q6_K head streams one column at a time at any batch
     assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 4)] == [S, S, S]
     assert pq.pq_gemv_launches("q6_k", 128256, 4096, 4) == 4

@@ -69,7 +69,7 @@ GEMV_SHAPES = {
 CASES = [(f, n, k) for f, shapes in GEMV_SHAPES.items() for (n, k) in shapes]
 
 
-@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16, 17])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 16, 17, 24, 32, 33, 40])
 @pytest.mark.parametrize("kernel", ["auto", "generic", "stream", "tc"])
 @pytest.mark.parametrize("fmt,n_out,k", CASES)
 def test_gemv_parity(fmt, n_out, k, kernel, batch):
@@ -164,6 +164,13 @@ def test_workload_q6_k_output_head():
 @pytest.mark.parametrize("batch", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("n_out,k,j", [(14336, 4096, 0), (4096, 14336, 1)])
 def test_workload_small_batch(n_out, k, j, batch):
+    full_case("q4_k", n_out, k, batch, 50 + 2 * j, 51 + 2 * j)
+
+
+@pytest.mark.parametrize("batch", [32, 64])
+@pytest.mark.parametrize("n_out,k,j", [(14336, 4096, 0), (4096, 14336, 1)])
+def test_workload_prompt_width(n_out, k, j, batch):
+    # 32-row prompt-width mat-vec (one tensor-core pass over W per 32 columns)
     full_case("q4_k", n_out, k, batch, 50 + 2 * j, 51 + 2 * j)
 
 
