@@ -54,7 +54,7 @@ NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 # kernel from one ncu capture, keyed by the sha256 of the kernel source it was
 # taken on (code only, comments removed); any edit of that code makes the
 # figure stale (reported as null).
-NCU_TRAFFIC = {"f3c237399babbd6c": 66_157_568}
+NCU_TRAFFIC = {"f3c237399babbd6c": 66_157_568, "e7a438cff78acc04": 66_132_736}
 
 
 def set_bytes():
