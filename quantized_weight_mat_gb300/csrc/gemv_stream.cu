@@ -1809,6 +1809,351 @@ inline bool takes(int64_t k, int64_t n_out, int batch) {
 }
 }  // namespace rowsnb
 
+// ---------------------------------------------------------------------------
+// Q6_K at batch 2-4: the whole-row kernel for several columns, so that the
+// 210-byte super-blocks (GGUF Q6_K; PESTI README, "What This Is") stream once
+// per call instead of once per column.
+//
+// Lane (h, t, j) of a super-block's eight lanes owns 32 weights: the 16
+// positions 16j..16j+15 of the runs t and t+2 of half h (run t of half h is
+// weights 128h + 32t .. +31).  Both runs take their low four bits from the
+// same 16 ql bytes (low and high nibbles) and their high two bits from the
+// same 16 qh bytes (bit pairs t and t+2), and each run's 16 positions share
+// one signed 8-bit scale, so a lane reads 32 bytes and two scales per row.
+// Its x limbs (four 16-byte groups per column of the image prep_x_nb writes)
+// stay in registers: 16 words per column.  Per row and column: 16 dp4a on
+// the unsigned 6-bit codes, then
+//   y += u * d * (sc_a * (254*H_a + L_a - 32*XS_a) + sc_b * (...)_b)
+// with XS the run's sum of 254*xh + xl (the code offset of 32), made once
+// per call.  A warp covers four super-blocks; G warps a row (partials added
+// in shared memory in segment order); four rows per iteration are reduced by
+// one transposed shuffle tree.  Rows must be whole multiples of 16 bytes
+// (k a multiple of 2048).
+namespace rows6 {
+// consumer warps: 16 at two columns (544 threads: 96 registers each), 15 at
+// four (512 threads: 128 registers, which the four columns' 72 limb words need)
+template <int NB> constexpr int cw() { return NB == 2 ? 16 : 15; }
+template <int NB> constexpr int threads() { return (cw<NB>() + 1) * 32; }
+constexpr int MAX_STAGES = 8;
+constexpr int kStatic = 512;
+constexpr int LPB = 8;                       // lanes per super-block
+constexpr int KW = 32 / LPB;                 // super-blocks per warp
+constexpr int BB = 210;                      // bytes per super-block
+using rowsnb::Params;
+using rowsnb::col_bytes;
+
+inline int segments(int64_t k) { return (int)((k / 256 + KW - 1) / KW); }
+template <int NB> inline int red_bytes(const Params &p) {
+    return p.G > 1 ? (p.rows_cap * p.G * NB * 4 + 15) / 16 * 16 : 0;
+}
+
+template <int NB> inline bool plan(int64_t k, int64_t n_out, int grid, Params &p) {
+    if (k % 2048 || grid < 1 || n_out < 1) return false;
+    const int G = segments(k);
+    if (G < 1 || G > cw<NB>()) return false;
+    p.G = G;
+    p.NG = cw<NB>() / G;
+    p.RS = 2 * p.NG;
+    p.rows_cap = (int)((n_out + grid - 1) / grid);
+    const int64_t stage = (int64_t)p.RS * (k / 256) * BB;
+    const int64_t avail = kSmemBudget - kStatic - (int64_t)NB * col_bytes(k) - rows6::red_bytes<NB>(p);
+    int64_t ns = avail / stage;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    p.nstages = (int)ns;
+    return ns >= 2;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(threads<NB>(), 1) gemv_q6_k_nb(Params p) {
+    constexpr int CW = cw<NB>();
+    constexpr int V = 4 * NB;                // values per lane per iteration (4 rows x NB columns)
+    constexpr int LOGV = NB == 2 ? 3 : 4;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
+    __shared__ __align__(8) uint64_t x_bar;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.k / 256;
+    const int S = p.k / 64;
+    const int CB = col_bytes(p.k);
+    const uint32_t rowbytes = (uint32_t)nb * (uint32_t)BB;
+    const int G = p.G, NG = p.NG, RS = p.RS, CA = G * NG;
+    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
+    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
+    const int units = (nrows + RS - 1) / RS;
+    const int NS = p.nstages;
+    const uint32_t stage_bytes = (uint32_t)RS * rowbytes;
+    uint8_t *ximg = smem + (size_t)NS * stage_bytes;            // NB columns of CB bytes
+    float *red = reinterpret_cast<float *>(ximg + (size_t)NB * CB);
+    const uint32_t ring_s = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], CA);
+        }
+        mbar_init(&x_bar, 1);
+        fence_mbar_init();
+    }
+    rowk::grid_dep_launch();
+    __syncthreads();
+
+    if (warp == CW) {
+        // ---------------- producer: one contiguous copy per stage ----------------
+        if (lane == 0) {
+            // the first ring's worth of weights, then (after prep_x_nb) the x image
+            const int early = units < NS ? units : NS;
+            const uint64_t pol = make_evict_first_policy();
+            const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
+            int slot = 0;
+            uint32_t ph = 0;
+            for (int u = 0; u <= units; ++u) {
+                if (u == early) {
+                    rowk::grid_dep_wait();
+                    mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
+                    bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                }
+                if (u == units) break;
+                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
+                const uint32_t bytes = (uint32_t)rows * rowbytes;
+                if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_g2s_hint(smem + (size_t)slot * stage_bytes, src, bytes, &full_bar[slot], pol);
+                src += (size_t)RS * rowbytes;
+                if (++slot == NS) { slot = 0; ph ^= 1u; }
+            }
+        }
+        return;
+    }
+
+    if (warp >= CA) return;
+    bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
+    if (!mbar_wait(&x_bar, 0)) dead = true;
+
+    const int gi = warp / G, seg = warp - gi * G;
+    const int part = lane % LPB;
+    const int h = part >> 2, t = (part >> 1) & 1, j = part & 1;
+    // a warp takes four blocks of one parity (segment pair sp covers blocks
+    // 8sp..8sp+7): blocks 2 apart start 420 bytes apart, one bank group
+    // further, so the 32 lanes' word loads fall in 32 different banks
+    const int kb = 8 * (seg >> 1) + 2 * (lane / LPB) + (seg & 1);
+    const bool valid = kb < nb;
+    const int kbc = valid ? kb : nb - 1;       // idle lanes read a real block, weight 0
+    const int sl = 4 * kbc + 2 * h;            // image slice of run t (run t + 2: sl + 1)
+    const int ga = 2 * t + j;                  // 16-byte group of the run's xh (xl: ga + 4)
+
+    uint32_t xah[NB][4], xal[NB][4], xbh[NB][4], xbl[NB][4];
+    int nxa[NB], nxb[NB];                      // -32 * XS of the two runs
+    float u[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const uint8_t *img = ximg + (size_t)b * CB;
+        const uint4 ah = *reinterpret_cast<const uint4 *>(img + (ga * S + sl) * 16);
+        const uint4 al = *reinterpret_cast<const uint4 *>(img + ((ga + 4) * S + sl) * 16);
+        const uint4 bh = *reinterpret_cast<const uint4 *>(img + (ga * S + sl + 1) * 16);
+        const uint4 bl = *reinterpret_cast<const uint4 *>(img + ((ga + 4) * S + sl + 1) * 16);
+        xah[b][0] = ah.x; xah[b][1] = ah.y; xah[b][2] = ah.z; xah[b][3] = ah.w;
+        xal[b][0] = al.x; xal[b][1] = al.y; xal[b][2] = al.z; xal[b][3] = al.w;
+        xbh[b][0] = bh.x; xbh[b][1] = bh.y; xbh[b][2] = bh.z; xbh[b][3] = bh.w;
+        xbl[b][0] = bl.x; xbl[b][1] = bl.y; xbl[b][2] = bl.z; xbl[b][3] = bl.w;
+        int sah = 0, sal = 0, sbh = 0, sbl = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sah = dp4a_ss(xah[b][i], 0x01010101u, sah);
+            sal = dp4a_ss(xal[b][i], 0x01010101u, sal);
+            sbh = dp4a_ss(xbh[b][i], 0x01010101u, sbh);
+            sbl = dp4a_ss(xbl[b][i], 0x01010101u, sbl);
+        }
+        nxa[b] = -32 * (254 * sah + sal);
+        nxb[b] = -32 * (254 * sbh + sbl);
+        const uint8_t *meta = img + 2 * p.k;
+        u[b] = valid ? *reinterpret_cast<const float *>(meta + sl * 16 + 8) : 0.f;
+    }
+
+    // the block starts 2-byte aligned: word loads from the aligned address
+    // below it, realigned with one byte permute per word
+    const uint32_t blk0 = ring_s + (uint32_t)kbc * (uint32_t)BB;
+    const uint32_t delta = blk0 & 2u;
+    const uint32_t sel = delta ? 0x5432u : 0x3210u;
+    const uint32_t dsh = delta ? 16u : 0u;
+    const uint32_t lane_a = blk0 - delta;
+    const uint32_t oql = (uint32_t)(64 * h + 32 * t + 16 * j);
+    const uint32_t oqh = (uint32_t)(128 + 32 * h + 16 * j);
+    const uint32_t osc = (uint32_t)(192 + 8 * h + 2 * t + j) + delta;
+    const int sa = 4 - 2 * t, sb = 2 * t;
+
+    // products of one row (block at aligned shared address a) with all NB columns
+    auto row_dot = [&](uint32_t a, float (&out)[NB]) {
+        uint32_t ql[4], qh[4];
+        {
+            uint32_t w[5], v[5];
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+                w[i] = rowk::lds32(a + oql + 4u * (uint32_t)i);
+                v[i] = rowk::lds32(a + oqh + 4u * (uint32_t)i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ql[i] = __byte_perm(w[i], w[i + 1], sel);
+                qh[i] = __byte_perm(v[i], v[i + 1], sel);
+            }
+        }
+        int sc_a, sc_b;
+        asm volatile("ld.shared.s8 %0, [%1];" : "=r"(sc_a) : "r"(a + osc));
+        asm volatile("ld.shared.s8 %0, [%1];" : "=r"(sc_b) : "r"(a + osc + 4u));
+        const float d = h2f(rowk::lds32(a + 208u) >> dsh);
+        const float dsa = d * (float)sc_a, dsb = d * (float)sc_b;
+        uint32_t qa[4], qb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qa[i] = (ql[i] & 0x0F0F0F0Fu) | ((qh[i] << sa) & 0x30303030u);
+            qb[i] = ((ql[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> sb) & 0x30303030u);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            int Ha = 0, La = nxa[b], Hb = 0, Lb = nxb[b];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Ha = dp4a_us(qa[i], xah[b][i], Ha);
+                La = dp4a_us(qa[i], xal[b][i], La);
+                Hb = dp4a_us(qb[i], xbh[b][i], Hb);
+                Lb = dp4a_us(qb[i], xbl[b][i], Lb);
+            }
+            // |254 H + L| < 2^26: exact in int32
+            const int Da = 254 * Ha + La, Db = 254 * Hb + Lb;
+            out[b] = u[b] * fmaf(dsa, (float)Da, dsb * (float)Db);
+        }
+    };
+
+    const uint32_t rA0 = (uint32_t)gi * rowbytes, rA1 = (uint32_t)(gi + NG) * rowbytes;
+    constexpr int SHIFT = 5 - LOGV;                    // lane >> SHIFT = value index after the tree
+    const int my_v = lane >> SHIFT;
+    const int my_t = my_v / NB, my_b = my_v % NB;      // row slot (0,1 stage A; 2,3 stage B), column
+    const int my_rowoff = gi + ((my_t & 1) ? NG : 0);
+
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int uu = 0; uu < units; uu += 2) {
+        const bool hasB = uu + 1 < units;
+        const int slotA = slot;
+        const uint32_t phA = ph;
+        if (++slot == NS) { slot = 0; ph ^= 1u; }
+        const int slotB = slot;
+        const uint32_t phB = ph;
+        if (hasB) {
+            if (++slot == NS) { slot = 0; ph ^= 1u; }
+        }
+        const int nA = nrows - uu * RS < RS ? nrows - uu * RS : RS;
+        const int nB = hasB ? (nrows - (uu + 1) * RS < RS ? nrows - (uu + 1) * RS : RS) : 0;
+        float v[V];
+        float tmp[NB];
+        if (!dead && !mbar_wait(&full_bar[slotA], phA)) dead = true;
+        {
+            const uint32_t sA = lane_a + (uint32_t)slotA * stage_bytes;
+            row_dot(sA + rA0, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[b] = gi < nA ? tmp[b] : 0.f;
+            row_dot(sA + rA1, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[NB + b] = gi + NG < nA ? tmp[b] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slotA]);
+        if (hasB && !dead && !mbar_wait(&full_bar[slotB], phB)) dead = true;
+        {
+            const uint32_t sB = lane_a + (uint32_t)slotB * stage_bytes;
+            row_dot(sB + rA0, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[2 * NB + b] = gi < nB ? tmp[b] : 0.f;
+            row_dot(sB + rA1, tmp);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[3 * NB + b] = gi + NG < nB ? tmp[b] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0 && hasB) mbar_arrive(&empty_bar[slotB]);
+        const float tot = rowsnb::transposed_sum<V, LOGV>(v, lane);
+        if ((lane & ((1 << SHIFT) - 1)) == 0 && my_b < p.nb_cols) {
+            const int n_here = my_t >= 2 ? nB : nA;
+            if (my_rowoff < n_here) {
+                const int row = (uu + (my_t >= 2 ? 1 : 0)) * RS + my_rowoff;   // relative to r0
+                if (G == 1)
+                    p.y[(size_t)my_b * p.ldy + r0 + row] = tot;
+                else
+                    red[((size_t)row * G + seg) * NB + my_b] = tot;
+            }
+        }
+    }
+    if (G > 1) {
+        named_sync(2, CA * 32);
+        for (int i = warp * 32 + lane; i < nrows * NB; i += CA * 32) {
+            const int row = i / NB, b = i % NB;
+            if (b >= p.nb_cols) continue;
+            float sum = red[((size_t)row * G) * NB + b];
+            for (int g2 = 1; g2 < G; ++g2) sum += red[((size_t)row * G + g2) * NB + b];
+            p.y[(size_t)b * p.ldy + r0 + row] = sum;
+        }
+    }
+}
+
+template <int NB>
+cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int nb_cols, float *y, int64_t ldy,
+                   int grid, cudaStream_t s) {
+    Params p{w, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
+    if (!rows6::plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
+    const int smem = p.nstages * p.RS * (int)(k / 256) * BB + NB * col_bytes(k) + rows6::red_bytes<NB>(p);
+    static PerDeviceOnce configured;
+    const cudaError_t ce = configured.run([] {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemv_q6_k_nb<NB>);
+        if (e != cudaSuccess) return e;
+        if (fa.sharedSizeBytes > (size_t)kStatic) return cudaErrorInvalidConfiguration;
+        return cudaFuncSetAttribute(gemv_q6_k_nb<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBudget - kStatic);
+    });
+    if (ce != cudaSuccess) return ce;
+    cudaMemPool_t pool = scratch_pool();
+    if (!pool) return cudaErrorMemoryAllocation;
+    void *img = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&img, (size_t)NB * col_bytes(k), pool, s);
+    if (e != cudaSuccess) return e;
+    p.x_img = static_cast<const uint8_t *>(img);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3((unsigned)((k / 256 + 7) / 8), NB);
+    pcfg.blockDim = dim3(256);
+    pcfg.stream = s;
+    pcfg.attrs = attr;
+    pcfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pcfg, rowsnb::prep_x_nb<NB>, x, (int)k, nb_cols, static_cast<uint8_t *>(img));
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads<NB>());
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_q6_k_nb<NB>, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    const cudaError_t f = cudaFreeAsync(img, s);
+    return e != cudaSuccess ? e : f;
+}
+
+// Whether this kernel runs Q6_K (k, n_out) at `batch` (2-4) columns.
+inline bool takes(int64_t k, int64_t n_out, int batch) {
+    Params p{};
+    const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
+    const int grid = (int)(n_out < grid_est ? n_out : grid_est);
+    if (batch < 2 || batch > 4 || k > (INT64_C(1) << 20)) return false;
+    return batch == 2 ? rows6::plan<2>(k, n_out, grid, p) : rows6::plan<4>(k, n_out, grid, p);
+}
+}  // namespace rows6
+
 }  // namespace
 
 unsigned stream_wait_timeouts(bool reset) {
@@ -1827,6 +2172,7 @@ bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kin
 
 bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch) {
     if (batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out)) return true;
+    if (fmt == PQ_Q6_K && batch >= 2) return rows6::takes(k, n_out, batch);
     if (fmt != PQ_Q4_K || batch < 1 || batch > 4 || n_out < 1) return false;
     if (k % 256 || k > (INT64_C(1) << 20)) return false;
     return plan_stages(k, batch) >= 2;
@@ -1859,6 +2205,9 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
         return launch_gemv_stream_epi(fmt, w, n_out, k, x, y, s, dev, Epilogue{});
     if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
         return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);
+    if (fmt == PQ_Q6_K)
+        return batch == 2 ? rows6::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s)
+                          : rows6::launch<4>(w, n_out, k, x, batch, y, ldy, grid, s);
     switch (batch) {
     case 1: return launch_nb<1>(p, grid, s);
     case 2: return launch_nb<2>(p, grid, s);

@@ -135,9 +135,10 @@ int choose(int fmt, int64_t n_out, int64_t k, int nb) {
     const bool tc_pays = nb >= 5 || (nb >= 3 && k >= 8192) || (nb == 4 && n_out * k >= (INT64_C(1) << 25));
     if (tc_pays && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
     if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
-    // Q6_K, Q8_0 and per-row int8 have a streaming kernel for one column only;
-    // one launch per column still beats the generic kernel (Q6_K LM head
-    // 128256x4096: 2 x 65 us against 301 us at batch 2)
+    // Q8_0, per-row int8 and the rest of the K family have a streaming kernel
+    // for one column only (Q6_K for 1-4); one launch per column still beats
+    // the generic kernel (Q6_K LM head 128256x4096, one column at a time:
+    // 2 x 65 us against 301 us at batch 2)
     if (fmt != PQ_Q4_K && stream_supported(fmt, n_out, k, 1)) return PQ_KERNEL_STREAM;
     return PQ_KERNEL_GENERIC;
 }

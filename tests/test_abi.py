@@ -106,7 +106,7 @@ def test_kernel_choice_table():
             assert c in (pq.KERNEL_GENERIC, pq.KERNEL_STREAM, pq.KERNEL_TC)
             n = pq.pq_gemv_launches(fmt, 4096, k, b)
             # slices of up to 32 (tensor core) or 4 columns, or one column at a
-            # time for a one-column streaming kernel (Q6_K, Q8_0, per-row int8)
+            # time for a one-column streaming kernel (Q8_0, per-row int8)
             assert (b + 31) // 32 <= n <= (b if fmt != "q4_k" else (b + 3) // 4)
 
 
@@ -169,9 +169,13 @@ def test_q4_k_dispatch_matches_the_measured_winners():
     for b, launches in ((17, 1), (32, 1), (33, 2), (64, 2), (65, 3)):
         assert pq.pq_gemv_choice("q4_k", 14336, 4096, b) == T
         assert pq.pq_gemv_launches("q4_k", 14336, 4096, b) == launches
-    # the Q6_K head streams one column at a time at any batch
-    assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 4)] == [S, S, S]
-    assert pq.pq_gemv_launches("q6_k", 128256, 4096, 4) == 4
+    # the Q6_K head streams W once per call for up to 4 columns, in passes of 4
+    assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 3, 4, 8)] == [S] * 5
+    for b, launches in ((1, 1), (2, 1), (3, 1), (4, 1), (5, 2), (8, 2), (16, 4), (17, 5)):
+        assert pq.pq_gemv_launches("q6_k", 128256, 4096, b) == launches
+    # rows that are not whole 16-byte units (k not a multiple of 2048) take
+    # the generic kernel
+    assert pq.pq_gemv_choice("q6_k", 4096, 768, 2) == pq.KERNEL_GENERIC
     # so do Q8_0 and per-row int8 when k is a multiple of 256 (whole-row
     # kernel); other k take the generic kernel
     for fmt in ("q8_0", "i8_row"):

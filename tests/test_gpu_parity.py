@@ -59,7 +59,7 @@ def test_dequant_bit_exact(fmt, n_out, k, kind):
 GEMV_SHAPES = {
     "q8_0": [(1, 32), (7, 96), (129, 896), (300, 4096), (1000, 768)],
     "q4_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (37, 14336)],
-    "q6_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (9, 14336)],
+    "q6_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (9, 14336), (1000, 4096), (2001, 2048)],
     "i8_row": [(1, 1), (7, 13), (129, 100), (300, 4096), (33, 2048), (1000, 768)],
     "q5_k": [(1, 256), (7, 768), (129, 4096), (9, 14336), (1000, 4096)],
     "q3_k": [(1, 256), (7, 768), (129, 4096), (9, 14336), (1000, 2048)],
@@ -157,8 +157,10 @@ def test_workload_decode_layer_set(j, n_out, k):
     full_case("q4_k", n_out, k, 1, 30 + 2 * j, 31 + 2 * j)
 
 
-def test_workload_q6_k_output_head():
-    full_case("q6_k", 128256, 4096, 1, 40, 41)
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 8])
+def test_workload_q6_k_output_head(batch):
+    # batch 2-4: one pass over the 431 MB head for all columns; 8: two passes
+    full_case("q6_k", 128256, 4096, batch, 40, 41)
 
 
 @pytest.mark.parametrize("batch", [1, 2, 4, 8, 16])
