@@ -273,6 +273,92 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// x image for the register-operand kernel (gemv_mma_q4_k): the same scaled
+// hi/lo halves as prep_x_tc, stored in the order the warps load them as
+// mma.sync A fragments.  Per 16-position step s of the super-block and group
+// mt of 8 columns, lane L = 4g + i holds 16 bytes {a0, a1, a2, a3}: column
+// 8mt + g, positions 16s + 4i + {0, 2} (a0 hi, a1 lo) and + {1, 3} (a2 hi, a3
+// lo) -- the K slots 2i, 2i+1 and 2i+8, 2i+9 of the fragment, matching the
+// weights a thread decodes from one 4-byte qs word.  Then per group, lane L:
+// 8 bytes {hi, lo} of the sums over sub-blocks 2i and 2i+1 of column 8mt + g
+// (the mins operand; K slots 8..15 are zero); then the factors 2^-e.  The
+// tile has the size of prep_x_tc's.
+template <int NBP>
+__global__ void __launch_bounds__(256) prep_x_mma(const float *__restrict__ x, int k, int nb_cols,
+                                                  uint8_t *__restrict__ img) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    constexpr int MT = NBP / 8;
+    const int sb = blockIdx.x;
+    uint8_t *tile = img + (size_t)sb * btile_bytes<NBP>();
+    float *undo = reinterpret_cast<float *>(tile + xscale_off<NBP>());
+    __shared__ uint32_t wmax[8][NBP];
+    __shared__ float mult[NBP];
+    __shared__ float xs[NBP][8];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    float v[NBP];
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) v[b] = b < nb_cols ? __ldg(x + (size_t)b * k + sb * 256 + t) : 0.f;
+    const int sbc = t / 8, sbj = t % 8;
+    float4 sv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < NBP * 8 && sbc < nb_cols) {
+        const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)sbc * k + sb * 256 + 32 * sbj);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sv[i] = __ldg(xb + i);
+    }
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(v[b]) & 0x7fffffffu);
+        if (lane == 0) wmax[warp][b] = m;
+    }
+    __syncthreads();
+    if (t < NBP) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = max(m, wmax[w][t]);
+        const int e = tc_scale_exponent(m);
+        mult[t] = __uint_as_float((uint32_t)(127 + e) << 23);    // 2^e
+        undo[t] = __uint_as_float((uint32_t)(127 - e) << 23);    // 2^-e
+    }
+    __syncthreads();
+    // position t: step t/16, lane slot i = (t%16)/4, r = t%4 -> register 0/2
+    // (hi) or 1/3 (lo) for r even/odd, low half for r < 2
+    const int st = t >> 4, i4 = (t >> 2) & 3, r = t & 3;
+    const int hreg = (r & 1) ? 2 : 0, half = r >> 1;
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) {
+        const float sx = v[b] * mult[b];
+        const __half hi = __float2half_rn(sx);
+        const __half lo = __float2half_rn(sx - __half2float(hi));
+        const int L = 4 * (b % 8) + i4;
+        __half *frag = reinterpret_cast<__half *>(tile + ((size_t)(st * MT + b / 8) * 32 + L) * 16);
+        frag[2 * hreg + half] = hi;
+        frag[2 * (hreg + 1) + half] = lo;
+    }
+    if (t < NBP * 8) {
+        const float m = mult[sbc];
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = s + sv[i].x * m + sv[i].y * m + sv[i].z * m + sv[i].w * m;
+        xs[sbc][sbj] = s;
+    }
+    __syncthreads();
+    // mins operand: thread (column b, sub-block j) writes its hi and lo halves
+    if (t < NBP * 8) {
+        const int b = sbc, j = sbj;
+        const float s = xs[b][j];
+        const __half hi = __float2half_rn(s);
+        const __half lo = __float2half_rn(s - __half2float(hi));
+        const int L = 4 * (b % 8) + (j >> 1);
+        __half *frag = reinterpret_cast<__half *>(tile + xmain_bytes<NBP>() + ((size_t)(b / 8) * 32 + L) * 8);
+        frag[j & 1] = hi;
+        frag[2 + (j & 1)] = lo;
+    }
+}
+
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -665,6 +751,254 @@ __global__ void __launch_bounds__(tc_threads<NBP>(), 1)
     }
 }
 
+// ---------------------------------------------------------------- register-operand kernel
+// The same work split, stages and split-K as gemv_tc_q4_k, with the products
+// on mma.sync (m16n8k16, fp16 in, f32 accumulate) fed from registers: the
+// decoded weights never leave the registers of the warp that decodes them
+// (the tensor-memory kernel above writes 64 KB of fp16 per super-block item
+// into tensor memory, and that store bounds it).  A = x (16 rows = hi and lo
+// parts of 8 columns), B = the exact fp16 sc*q of 8 weight rows.
+//
+//   warp 16 producer (as above);
+//   warps 0-15: group q = warp/4 takes items q, q+4, ...; warp w%4 of a group
+//           rows 32(w%4)..+31 of the item's 128-row tile, in four n8 blocks.
+//           Per item: the 256 K of the super-block in 16 steps; each qs word
+//           gives a thread's four weights of two steps (low and high
+//           nibbles), decoded with one LOP3 + one HFMA2 per two weights; one
+//           K=16 product of the mins per n8 block; then, per row and column,
+//           y += 2^-e * (d*(x'.A) - dmin*(XS'.m)) in registers.
+//           At the end of a tile the four groups' sums are added in group
+//           order through shared memory and stored (or written as split-K
+//           parts / SwiGLU halves, as above).
+constexpr int MMA_GROUPS = 4;
+constexpr int MMA_COMPUTE_WARPS = 16;
+constexpr int MMA_THREADS = (MMA_COMPUTE_WARPS + 1) * 32;
+template <int NBP> __host__ __device__ constexpr int mma_stages() { return NBP == 8 ? 7 : 5; }
+template <int NBP> __host__ __device__ constexpr int mma_red_bytes() { return MMA_GROUPS * TM * NBP * 4; }
+template <int NBP> __host__ __device__ constexpr int mma_smem_bytes() {
+    return mma_stages<NBP>() * stage_bytes<NBP>() + mma_red_bytes<NBP>() + 1024;
+}
+static_assert(mma_smem_bytes<8>() <= 227 * 1024 && mma_smem_bytes<16>() <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint4 &a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// byte i (0..3) of v as an exact fp16 value, duplicated in both halves
+__device__ __forceinline__ uint32_t byte_h2(uint32_t v, int i) {
+    // (0x64 << 8 | byte) is the fp16 1024 + byte; subtracting 1024 is exact
+    const uint32_t sel = (uint32_t)i | 0x40u | ((uint32_t)i << 8) | 0x4000u;
+    const uint32_t p = __byte_perm(v, 0x64646464u, sel);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&p), __float2half2_rn(1024.0f));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+// bytes i and i+1 of v as exact fp16 values (low half: byte i)
+__device__ __forceinline__ uint32_t bytes_h2(uint32_t v, int i) {
+    const uint32_t sel = (uint32_t)i | 0x40u | ((uint32_t)(i + 1) << 8) | 0x4000u;
+    const uint32_t p = __byte_perm(v, 0x64646464u, sel);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&p), __float2half2_rn(1024.0f));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+template <int NBP>
+__global__ void __launch_bounds__(MMA_THREADS, 1)
+    gemv_mma_q4_k(const __grid_constant__ CUtensorMap wmap, TcParams p) {
+    constexpr int MT = NBP / 8;
+    constexpr int NSR = mma_stages<NBP>();
+    constexpr int STAGE = stage_bytes<NBP>();
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
+    uint8_t *ring = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    float *red = reinterpret_cast<float *>(ring + NSR * STAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = p.k / 256;
+    const int grid = (int)gridDim.x;
+    const long long i0 = item_begin(blockIdx.x, p.total, grid);
+    const int count = (int)(item_begin(blockIdx.x + 1, p.total, grid) - i0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSR; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], 4);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    if (warp == MMA_COMPUTE_WARPS) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t pol = make_evict_first_policy();
+            int tile = (int)(i0 / nb), sb = (int)(i0 % nb);
+            for (int g = 0; g < count; ++g) {
+                const int slot = g % NSR;
+                const uint32_t ph = (uint32_t)(g / NSR) & 1u;
+                if (!mbar_wait(&raw_empty[slot], ph ^ 1u)) break;
+                uint8_t *st = ring + slot * STAGE;
+                mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)STAGE);
+                tma_load_2d(st, &wmap, sb * 144, (int)tile_row0(tile, p.n_ff), &raw_full[slot]);
+                if (g == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+                bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NBP>(), (uint32_t)btile_bytes<NBP>(),
+                              &raw_full[slot], pol);
+                if (++sb == nb) { sb = 0; ++tile; }
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps ----------------
+    const int q = warp >> 2, r4 = warp & 3;
+    const int g8 = lane >> 2, tig = lane & 3;
+    float yacc[MT][4][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) yacc[mt][nt][0] = yacc[mt][nt][1] = 0.f;
+    bool dead = false;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // before any store of y or partials
+    const int first_tile = (int)(i0 / nb);
+    int tile = first_tile, sb = (int)(i0 % nb);
+    for (int g = 0; g < count; ++g) {
+        if ((g & (MMA_GROUPS - 1)) == q) {
+            const int slot = g % NSR;
+            const uint32_t ph = (uint32_t)(g / NSR) & 1u;
+            if (!dead && !mbar_wait(&raw_full[slot], ph)) dead = true;
+            const uint8_t *st = ring + slot * STAGE;
+            const uint8_t *xt = st + RAW_BYTES;
+            if (!dead) {
+                // B rows of this thread: 32 r4 + 8 nt + g8, 1152 bytes apart
+                const uint8_t *rb = st + (32 * r4 + g8) * 144;
+                uint32_t scw[4][2], mnw[4][2];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(rb + nt * 1152);
+                    // 6-bit scales and mins of sub-blocks 0-3 and 4-7
+                    scw[nt][0] = hd.y & 0x3F3F3F3Fu;
+                    scw[nt][1] = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+                    mnw[nt][0] = hd.z & 0x3F3F3F3Fu;
+                    mnw[nt][1] = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+                }
+                float acc[MT][4][4];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    // scale pairs of sub-blocks 2c (low nibbles) and 2c+1 (high):
+                    // (1024+q)*sc - 1024*sc and (1024+16q)*sc/16 - 64*sc
+                    uint32_t Slo[4], Clo[4], Shi[4], Chi[4];
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const uint32_t w = scw[nt][c >> 1];
+                        const uint32_t lo = byte_h2(w, 2 * (c & 1)), hi = byte_h2(w, 2 * (c & 1) + 1);
+                        Slo[nt] = lo;
+                        Clo[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&lo), __float2half2_rn(-1024.0f)));
+                        Shi[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&hi), __float2half2_rn(0.0625f)));
+                        Chi[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&hi), __float2half2_rn(-64.0f)));
+                    }
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int slo = 4 * c + pp, shi = slo + 2;
+                        uint4 alo[MT], ahi[MT];
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            alo[mt] = *reinterpret_cast<const uint4 *>(xt + ((size_t)(slo * MT + mt) * 32 + lane) * 16);
+                            ahi[mt] = *reinterpret_cast<const uint4 *>(xt + ((size_t)(shi * MT + mt) * 32 + lane) * 16);
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(rb + nt * 1152 + 16 + 32 * c + 16 * pp + 4 * tig);
+                            const uint32_t s8 = w >> 8;
+                            const uint32_t b0 = hfma2_u((w & 0x000F000Fu) | 0x64006400u, Slo[nt], Clo[nt]);
+                            const uint32_t b1 = hfma2_u((s8 & 0x000F000Fu) | 0x64006400u, Slo[nt], Clo[nt]);
+                            const uint32_t b2 = hfma2_u((w & 0x00F000F0u) | 0x64006400u, Shi[nt], Chi[nt]);
+                            const uint32_t b3 = hfma2_u((s8 & 0x00F000F0u) | 0x64006400u, Shi[nt], Chi[nt]);
+#pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                mma_16816(acc[mt][nt], alo[mt], b0, b1);
+                                mma_16816(acc[mt][nt], ahi[mt], b2, b3);
+                            }
+                        }
+                    }
+                }
+                // mins: K slots 2tig, 2tig+1 = sub-blocks 2tig, 2tig+1; slots 8..15 zero
+                float mins[MT][4][4];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint2 am = *reinterpret_cast<const uint2 *>(xt + xmain_bytes<NBP>() + ((size_t)mt * 32 + lane) * 8);
+                    const uint4 a = make_uint4(am.x, am.y, 0u, 0u);
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        mins[mt][nt][0] = mins[mt][nt][1] = mins[mt][nt][2] = mins[mt][nt][3] = 0.f;
+                        const uint32_t bm = bytes_h2(mnw[nt][tig >> 1], 2 * (tig & 1));
+                        mma_16816(mins[mt][nt], a, bm, 0u);
+                    }
+                }
+                // y += 2^-e * (d * main - dmin * mins) for rows 2tig, 2tig+1 of each n8 block
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int rc = 32 * r4 + 8 * nt + 2 * tig;
+                    const uint32_t dd0 = *reinterpret_cast<const uint32_t *>(st + rc * 144);
+                    const uint32_t dd1 = *reinterpret_cast<const uint32_t *>(st + (rc + 1) * 144);
+                    const float d0 = h2f(dd0), m0 = h2f(dd0 >> 16), d1 = h2f(dd1), m1 = h2f(dd1 >> 16);
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const float undo = *reinterpret_cast<const float *>(xt + xscale_off<NBP>() + 4 * (8 * mt + g8));
+                        const float v0 = fmaf(d0, acc[mt][nt][0] + acc[mt][nt][2], -m0 * (mins[mt][nt][0] + mins[mt][nt][2]));
+                        const float v1 = fmaf(d1, acc[mt][nt][1] + acc[mt][nt][3], -m1 * (mins[mt][nt][1] + mins[mt][nt][3]));
+                        yacc[mt][nt][0] = fmaf(v0, undo, yacc[mt][nt][0]);
+                        yacc[mt][nt][1] = fmaf(v1, undo, yacc[mt][nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[slot]);
+        }
+
+        if (sb == nb - 1 || g == count - 1) {
+            // the CTA's part of this tile is complete: add the groups' sums
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int rc = 32 * r4 + 8 * nt + 2 * tig, col = 8 * mt + g8;
+                    red[((size_t)q * TM + rc) * NBP + col] = yacc[mt][nt][0];
+                    red[((size_t)q * TM + rc + 1) * NBP + col] = yacc[mt][nt][1];
+                    yacc[mt][nt][0] = yacc[mt][nt][1] = 0.f;
+                }
+            named_sync(1, MMA_COMPUTE_WARPS * 32);
+            const long long t0i = (long long)tile * nb;
+            const int cf = item_owner(t0i, p.total, grid), cl = item_owner(t0i + nb - 1, p.total, grid);
+            for (int idx = threadIdx.x; idx < TM * NBP; idx += MMA_COMPUTE_WARPS * 32) {
+                const int r = idx / NBP, b = idx % NBP;
+                float v = red[(size_t)r * NBP + b];
+#pragma unroll
+                for (int qq = 1; qq < MMA_GROUPS; ++qq) v += red[((size_t)qq * TM + r) * NBP + b];
+                if (cf == cl && p.n_ff > 0) {
+                    p.ytmp[((size_t)tile * TM + r) * NBP + b] = v;
+                } else if (cf == cl) {
+                    const int row = tile * TM + r;
+                    if (row < p.n_out && b < p.nb_cols)
+                        p.y[(size_t)b * p.ldy + row] = p.bias ? v + p.bias[row] : v;
+                } else {
+                    const int side = tile == first_tile ? 0 : 1;
+                    p.partials[((size_t)(blockIdx.x * 2 + side) * TM + r) * NBP + b] = v;
+                }
+            }
+            named_sync(1, MMA_COMPUTE_WARPS * 32);
+        }
+        if (++sb == nb) { sb = 0; ++tile; }
+    }
+}
+
 // Split-K finish: block c adds up the tile whose first contributor is CTA c
 // (the last tile of c's range, when later CTAs share it), parts in CTA order.
 // Launched after the main kernel with programmatic dependent launch: it can be
@@ -856,9 +1190,19 @@ template <int NBP> size_t scratch_bytes_epi(int64_t n_out, int64_t k, int grid, 
     return scratch_bytes<NBP>(k, grid) + (epi.kind == kEpiSwiGLU ? (size_t)tc_tiles(n_out, epi) * TM * NBP * 4 : 0);
 }
 
+// The register-operand kernel for 1-8 columns (PQ_TC_MMA=0 builds the
+// tensor-memory kernel there instead); 9-32 columns take the tensor-memory
+// kernel (at 16 columns the register-operand kernel is slower: 24.6 against
+// 19.3 us at 14336x4096, its accumulators spill at 96 registers).
+#ifndef PQ_TC_MMA
+#define PQ_TC_MMA 1
+#endif
+template <int NBP> constexpr bool use_mma() { return PQ_TC_MMA && NBP == 8; }
+
 template <int NBP>
 cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch, float *y,
                        int64_t ldy, cudaStream_t s, int grid, uint8_t *scratch, const Epilogue &epi = Epilogue{}) {
+    constexpr bool MMA = use_mma<NBP>();
     const int nb = (int)(k / 256);
     uint8_t *img = scratch;
     float *partials = reinterpret_cast<float *>(scratch + scratch_img_bytes<NBP>(k));
@@ -874,7 +1218,11 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
     pcfg.stream = s;
     pcfg.attrs = attr;
     pcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&pcfg, prep_x_tc<NBP>, x, (int)k, batch, img);
+    cudaError_t e;
+    if constexpr (MMA)
+        e = cudaLaunchKernelEx(&pcfg, prep_x_mma<NBP>, x, (int)k, batch, img);
+    else
+        e = cudaLaunchKernelEx(&pcfg, prep_x_tc<NBP>, x, (int)k, batch, img);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -892,7 +1240,12 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
 
     static PerDeviceOnce configured;
     e = configured.run([] {
-        return cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NBP>());
+        if constexpr (MMA)
+            return cudaFuncSetAttribute(gemv_mma_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        mma_smem_bytes<NBP>());
+        else
+            return cudaFuncSetAttribute(gemv_tc_q4_k<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes<NBP>());
     });
     static_assert(tc_threads<NBP>() <= 1024, "block size");
     if (e != cudaSuccess) return e;
@@ -902,12 +1255,15 @@ cudaError_t launch_nbp(const uint8_t *w, int64_t n_out, int64_t k, const float *
                epi.kind == kEpiBias ? epi.bias : nullptr, n_ff, swiglu ? ytmp : nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(tc_threads<NBP>());
-    cfg.dynamicSmemBytes = (size_t)smem_bytes<NBP>();
+    cfg.blockDim = dim3(MMA ? MMA_THREADS : tc_threads<NBP>());
+    cfg.dynamicSmemBytes = (size_t)(MMA ? mma_smem_bytes<NBP>() : smem_bytes<NBP>());
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
+    if constexpr (MMA)
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_q4_k<NBP>, map, p);
+    else
+        e = cudaLaunchKernelEx(&cfg, gemv_tc_q4_k<NBP>, map, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cfg.blockDim = dim3(TM);
