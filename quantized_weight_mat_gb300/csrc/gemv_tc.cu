@@ -788,20 +788,45 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint4 &a, uint32_
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
+// fp16 pairs as bit patterns, so that the arithmetic below takes them as
+// immediates: 1024, -1024, 1/16, -64
+constexpr uint32_t kH2_1024 = 0x64006400u, kH2_M1024 = 0xE400E400u, kH2_16TH = 0x2C002C00u, kH2_M64 = 0xD400D400u;
+__device__ __forceinline__ __half2 h2_of(uint32_t bits) { return *reinterpret_cast<const __half2 *>(&bits); }
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(h2_of(a), h2_of(b))); }
+
 // byte i (0..3) of v as an exact fp16 value, duplicated in both halves
 __device__ __forceinline__ uint32_t byte_h2(uint32_t v, int i) {
     // (0x64 << 8 | byte) is the fp16 1024 + byte; subtracting 1024 is exact
     const uint32_t sel = (uint32_t)i | 0x40u | ((uint32_t)i << 8) | 0x4000u;
     const uint32_t p = __byte_perm(v, 0x64646464u, sel);
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&p), __float2half2_rn(1024.0f));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    return h2_bits(__hsub2(h2_of(p), h2_of(kH2_1024)));
 }
-// bytes i and i+1 of v as exact fp16 values (low half: byte i)
-__device__ __forceinline__ uint32_t bytes_h2(uint32_t v, int i) {
-    const uint32_t sel = (uint32_t)i | 0x40u | ((uint32_t)(i + 1) << 8) | 0x4000u;
+// bytes i and i+1 of v as exact fp16 values (low half: byte i); i may vary
+__device__ __forceinline__ uint32_t bytes_h2(uint32_t v, uint32_t i) {
+    const uint32_t sel = i | 0x40u | ((i + 1u) << 8) | 0x4000u;
     const uint32_t p = __byte_perm(v, 0x64646464u, sel);
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&p), __float2half2_rn(1024.0f));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    return h2_bits(__hsub2(h2_of(p), h2_of(kH2_1024)));
+}
+
+// Wait until the producer has issued item g (the counter it advances after
+// each issue), bounded like the mbarrier waits.  A group that takes every
+// fourth item may reach item g's slot while the slot still holds, or has not
+// yet been given, the item before it (the ring is not a multiple of four
+// stages); waiting on the full barrier's parity then would see that older
+// phase complete.  Once item g is issued, the slot's previous phase has
+// completed and the parity wait is exact.
+__device__ __forceinline__ bool wait_issued(const volatile int *issued, int g) {
+    if (*issued <= g) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (*issued <= g) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicAdd(&g_wait_timeouts, 1u);
+                return false;
+            }
+        }
+    }
+    __threadfence_block();   // pairs with the producer's fence before its store
+    return true;
 }
 
 template <int NBP>
@@ -813,6 +838,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t raw_full[NSR], raw_empty[NSR];
+    __shared__ int issued_sh;                                       // items the producer has issued
+    volatile int *issued = &issued_sh;
     uint8_t *ring = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     float *red = reinterpret_cast<float *>(ring + NSR * STAGE);
 
@@ -827,6 +854,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], 4);
         }
+        *issued = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -847,6 +875,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 if (g == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 bulk_g2s_hint(st + RAW_BYTES, p.x_img + (size_t)sb * btile_bytes<NBP>(), (uint32_t)btile_bytes<NBP>(),
                               &raw_full[slot], pol);
+                __threadfence_block();
+                *issued = g + 1;
                 if (++sb == nb) { sb = 0; ++tile; }
             }
         }
@@ -869,6 +899,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if ((g & (MMA_GROUPS - 1)) == q) {
             const int slot = g % NSR;
             const uint32_t ph = (uint32_t)(g / NSR) & 1u;
+            if (!dead && !wait_issued(issued, g)) dead = true;
             if (!dead && !mbar_wait(&raw_full[slot], ph)) dead = true;
             const uint8_t *st = ring + slot * STAGE;
             const uint8_t *xt = st + RAW_BYTES;
@@ -900,9 +931,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                         const uint32_t w = scw[nt][c >> 1];
                         const uint32_t lo = byte_h2(w, 2 * (c & 1)), hi = byte_h2(w, 2 * (c & 1) + 1);
                         Slo[nt] = lo;
-                        Clo[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&lo), __float2half2_rn(-1024.0f)));
-                        Shi[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&hi), __float2half2_rn(0.0625f)));
-                        Chi[nt] = h2_bits(__hmul2(*reinterpret_cast<const __half2 *>(&hi), __float2half2_rn(-64.0f)));
+                        Clo[nt] = hmul2_u(lo, kH2_M1024);
+                        Shi[nt] = hmul2_u(hi, kH2_16TH);
+                        Chi[nt] = hmul2_u(hi, kH2_M64);
                     }
 #pragma unroll
                     for (int pp = 0; pp < 2; ++pp) {
@@ -938,7 +969,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt) {
                         mins[mt][nt][0] = mins[mt][nt][1] = mins[mt][nt][2] = mins[mt][nt][3] = 0.f;
-                        const uint32_t bm = bytes_h2(mnw[nt][tig >> 1], 2 * (tig & 1));
+                        const uint32_t bm = bytes_h2((tig >> 1) ? mnw[nt][1] : mnw[nt][0], 2u * (uint32_t)(tig & 1));
                         mma_16816(mins[mt][nt], a, bm, 0u);
                     }
                 }
