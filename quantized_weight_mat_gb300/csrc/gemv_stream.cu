@@ -2154,6 +2154,266 @@ inline bool takes(int64_t k, int64_t n_out, int batch) {
 }
 }  // namespace rows6
 
+// ---------------------------------------------------------------------------
+// Q6_K at batch 2-4 for k = 4096 (the output head's shape): the products on
+// mma.sync (m16n8k16, fp16 in, f32 accumulate) with both operands in
+// registers, one kernel per call.
+//
+// Stages are runs of 16 whole rows (one bulk copy each).  Compute warp w owns
+// super-block w of every row, so each warp covers a K range of 256 = 16 MMA
+// steps, and a step is exactly one 16-weight sub-block of one scale.
+//   B (x): built once per call by each warp for its own super-block: the
+//     hi and lo fp16 halves of x' = 2^e x (e per super-block and column, as
+//     in the tensor-core kernels), 8 MMA columns = 4 x columns x {hi, lo};
+//     a thread holds its 4 positions of every step, 32 registers.
+//   A (weights): rows g and g+8 of the 16-row stage, the 4 positions 4i..4i+3
+//     of the step (lane = 4g + i), decoded from the ql nibble and the qh bit
+//     pair to the exact fp16 q - 32.
+//   Per step the product of 16 rows x 8 columns is scaled by the signed
+//     sub-block scale of each row and added in f32; at the end of the stage
+//     the row's d and the column's 2^-e are applied and the 16 warps' sums
+//     are added in warp order through shared memory.
+namespace q6mma {
+constexpr int CWARPS = 16;                   // compute warps = super-blocks per row
+constexpr int THREADS = (CWARPS + 1) * 32;
+constexpr int RS = 16;                       // rows per stage
+constexpr int NS = 4;                        // stages
+constexpr int K = 4096;
+constexpr int ROWB = (K / 256) * 210;        // 3360 bytes per row
+constexpr int STAGE = RS * ROWB;
+constexpr int RED = 2 * CWARPS * RS * 4;     // floats: two stages of [warp][row][column]
+constexpr int kSmem = NS * STAGE + RED * 4 + 128;
+static_assert(kSmem <= kSmemBudget - 512, "shared memory per CTA");
+static_assert(STAGE % 16 == 0, "bulk-copy size");
+
+struct Params {
+    const uint8_t *w;
+    const float *x;
+    float *y;
+    long long ldy;
+    int n_out;
+    int nb_cols;     // 1..4
+    int early_w;     // stream weights before waiting on the previous kernel
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// bytes (i, j) of the 6-bit codes word q as the fp16 pair (q_i - 32, q_j - 32):
+// 0x64 above a byte is the fp16 1024 + byte, and 1056 is subtracted exactly
+__device__ __forceinline__ uint32_t codes_h2(uint32_t q, uint32_t sel) {
+    const uint32_t p = __byte_perm(q, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x64206420u));
+    return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemv_q6_k_mma(Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
+    float *red = reinterpret_cast<float *>(smem + NS * STAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
+    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
+    const int units = (nrows + RS - 1) / RS;
+    const uint32_t ring_s = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], CWARPS);
+        }
+        fence_mbar_init();
+    }
+    rowk::grid_dep_launch();
+    __syncthreads();
+
+    if (warp == CWARPS) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            if (!p.early_w) rowk::grid_dep_wait();   // the weights may be the previous kernel's output
+            const uint64_t pol = make_evict_first_policy();
+            const uint8_t *src = p.w + r0 * (int64_t)ROWB;
+            for (int u = 0; u < units; ++u) {
+                const int slot = u % NS;
+                const uint32_t ph = (uint32_t)(u / NS) & 1u;
+                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
+                const uint32_t bytes = (uint32_t)rows * ROWB;
+                if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&full_bar[slot], bytes);
+                bulk_g2s_hint(smem + (size_t)slot * STAGE, src, bytes, &full_bar[slot], pol);
+                src += (size_t)RS * ROWB;
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps: super-block w of every row ----------------
+    const int g = lane >> 2, i4 = lane & 3;
+    bool dead = false;
+    rowk::grid_dep_wait();                         // x is the previous kernel's output
+    // B fragments: MMA column n = g is x column g/2, part g%2 (hi, lo);
+    // register pair s holds positions 4 i4 + {0, 2} and 4 i4 + {1, 3} of step s
+    uint32_t xb[16][2];
+    float undo;
+    {
+        const int col = g >> 1;
+        float v[16][4];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (col < p.nb_cols) a = ldg_f4(p.x + (size_t)col * K + warp * 256 + 16 * s + 4 * i4);
+            v[s][0] = a.x; v[s][1] = a.y; v[s][2] = a.z; v[s][3] = a.w;
+        }
+        uint32_t mb = 0;
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mb = max(mb, __float_as_uint(v[s][j]) & 0x7fffffffu);
+        // the column's eight lanes (4 positions x hi/lo copies) cover its 256 values
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+        const int e = tc_scale_exponent(mb);
+        const float mult = __uint_as_float((uint32_t)(127 + e) << 23);
+        const float und = __uint_as_float((uint32_t)(127 - e) << 23);
+        const bool lo_part = g & 1;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            uint32_t hv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float sx = v[s][j] * mult;
+                const __half hi = __float2half_rn(sx);
+                const __half part = lo_part ? __float2half_rn(sx - __half2float(hi)) : hi;
+                hv[j] = __half_as_ushort(part);
+            }
+            xb[s][0] = hv[0] | (hv[2] << 16);
+            xb[s][1] = hv[1] | (hv[3] << 16);
+        }
+        // the C columns of this thread are 2 i4 (hi) and 2 i4 + 1 (lo) of x column i4
+        undo = __shfl_sync(0xffffffffu, und, 8 * i4);
+    }
+
+    // this warp's super-block in a stage row: 2-byte aligned; word loads from
+    // the aligned address below it, realigned by one byte permute
+    const uint32_t blk0 = (uint32_t)warp * 210u;
+    const uint32_t delta = blk0 & 2u;
+    const uint32_t sel = delta ? 0x5432u : 0x3210u;
+    const uint32_t dsh = delta ? 16u : 0u;
+    auto ldw = [&](uint32_t a) {                     // realigned word at byte offset a - delta + delta
+        return __byte_perm(rowk::lds32(a), rowk::lds32(a + 4u), sel);
+    };
+
+    for (int u = 0; u < units; ++u) {
+        const int slot = u % NS;
+        const uint32_t ph = (uint32_t)(u / NS) & 1u;
+        if (!dead && !mbar_wait(&full_bar[slot], ph)) dead = true;
+        const uint32_t st = ring_s + (uint32_t)slot * STAGE;
+        const uint32_t ra = st + (uint32_t)g * ROWB + blk0 - delta;          // row g, aligned
+        const uint32_t rb = ra + 8u * ROWB;                                  // row g + 8
+        float acc0 = 0.f, acc1 = 0.f;
+        float d0 = 0.f, d1 = 0.f;
+        if (!dead) {
+            uint32_t sc0[4], sc1[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sc0[j] = ldw(ra + 192u + 4u * j);
+                sc1[j] = ldw(rb + 192u + 4u * j);
+            }
+            d0 = h2f(rowk::lds32(ra + 208u) >> dsh);
+            d1 = h2f(rowk::lds32(rb + 208u) >> dsh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int sp = 0; sp < 2; ++sp) {
+                    // qh word of positions 16 sp + 4 i4 of half h: bit pairs of runs 0-3
+                    const uint32_t oh = 128u + 32u * h + 16u * sp + 4u * i4;
+                    const uint32_t qh0 = ldw(ra + oh), qh1 = ldw(rb + oh);
+#pragma unroll
+                    for (int t1 = 0; t1 < 2; ++t1) {
+                        // ql word of runs t1 (low nibbles) and t1 + 2 (high nibbles)
+                        const uint32_t ol = 64u * h + 32u * t1 + 16u * sp + 4u * i4;
+                        const uint32_t ql0 = ldw(ra + ol), ql1 = ldw(rb + ol);
+#pragma unroll
+                        for (int hn = 0; hn < 2; ++hn) {
+                            const int t = t1 + 2 * hn;                      // run 0..3
+                            const int s = 8 * h + 2 * t + sp;               // step = scale index
+                            const uint32_t lo0 = (hn ? (ql0 >> 4) : ql0) & 0x0F0F0F0Fu;
+                            const uint32_t lo1 = (hn ? (ql1 >> 4) : ql1) & 0x0F0F0F0Fu;
+                            const uint32_t hb0 = (t < 3 ? (qh0 << (4 - 2 * t)) : (qh0 >> 2)) & 0x30303030u;
+                            const uint32_t hb1 = (t < 3 ? (qh1 << (4 - 2 * t)) : (qh1 >> 2)) & 0x30303030u;
+                            const uint32_t q0 = lo0 | hb0, q1 = lo1 | hb1;
+                            float c[4];
+                            mma16816(c, codes_h2(q0, 0x4240u), codes_h2(q1, 0x4240u), codes_h2(q0, 0x4341u),
+                                     codes_h2(q1, 0x4341u), xb[s][0], xb[s][1]);
+                            const int sa = (int)(int8_t)(sc0[s >> 2] >> (8 * (s & 3)));
+                            const int sb = (int)(int8_t)(sc1[s >> 2] >> (8 * (s & 3)));
+                            acc0 = fmaf((float)sa, c[0] + c[1], acc0);
+                            acc1 = fmaf((float)sb, c[2] + c[3], acc1);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        // this warp's part of rows g, g+8 of the stage, x column i4
+        float *rw = red + (size_t)(u & 1) * CWARPS * RS * 4 + (size_t)warp * RS * 4;
+        rw[g * 4 + i4] = d0 * undo * acc0;
+        rw[(g + 8) * 4 + i4] = d1 * undo * acc1;
+        named_sync(1, CWARPS * 32);
+        if (threadIdx.x < RS * 4) {
+            const int row = threadIdx.x >> 2, col = threadIdx.x & 3;
+            const float *rr = red + (size_t)(u & 1) * CWARPS * RS * 4 + row * 4 + col;
+            float sum = rr[0];
+#pragma unroll
+            for (int w2 = 1; w2 < CWARPS; ++w2) sum += rr[(size_t)w2 * RS * 4];
+            const int n_here = nrows - u * RS < RS ? nrows - u * RS : RS;
+            if (row < n_here && col < p.nb_cols) p.y[(size_t)col * p.ldy + r0 + (int64_t)u * RS + row] = sum;
+        }
+    }
+}
+
+cudaError_t launch(const uint8_t *w, int64_t n_out, const float *x, int nb_cols, float *y, int64_t ldy, int grid,
+                   cudaStream_t s, int early_w) {
+    static PerDeviceOnce configured;
+    const cudaError_t ce = configured.run([] {
+        return cudaFuncSetAttribute(gemv_q6_k_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    });
+    if (ce != cudaSuccess) return ce;
+    Params p{w, x, y, (long long)ldy, (int)n_out, nb_cols, early_w};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)kSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_q6_k_mma, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Whether this kernel runs Q6_K (k, n_out) at `batch` columns: k = 4096,
+// batch 3-4, and at least one 16-row stage per CTA on a full GPU (smaller
+// matrices keep the CUDA-core kernel).  At batch 2 the CUDA-core kernel is
+// faster (output head 128256x4096: 83.7 against 96.2 us; at batch 4 this one
+// takes 96.9 against 124).
+inline bool takes(int64_t k, int64_t n_out, int batch) {
+    return k == K && batch >= 3 && batch <= 4 && n_out >= 152 * RS;
+}
+}  // namespace q6mma
+
 }  // namespace
 
 unsigned stream_wait_timeouts(bool reset) {
@@ -2205,6 +2465,8 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
         return launch_gemv_stream_epi(fmt, w, n_out, k, x, y, s, dev, Epilogue{});
     if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
         return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);
+    if (fmt == PQ_Q6_K && q6mma::takes(k, n_out, batch))
+        return q6mma::launch(w, n_out, x, batch, y, ldy, grid, s, weight_prefetch());
     if (fmt == PQ_Q6_K)
         return batch == 2 ? rows6::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s)
                           : rows6::launch<4>(w, n_out, k, x, batch, y, ldy, grid, s);

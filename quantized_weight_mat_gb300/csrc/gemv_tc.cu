@@ -131,19 +131,8 @@ __host__ __device__ constexpr int kmaj_off(int n, int K, int sbo) {
 // are complete even when the previous kernel wrote them; the main kernel waits
 // for this one only before its first x tile.
 //
-// Scale of column b: with E the binary exponent of m = max|x| over the
-// super-block's 256 values of the column (m in [2^E, 2^(E+1))), x' = 2^e * x
-// with e = 9 - E, capped at 126 so that 2^e and 2^-e are normal f32 numbers
-// (a cap that only applies when m < 2^-117); e = 0 when m is 0, inf or NaN
-// (non-finite values then reach y as they would unscaled).  Scaling by a power
-// of two is exact, so x' = x_hi + x_lo holds x to a relative 2^-21 plus an
-// absolute 2^-25 in scaled units, i.e. about 2^-34 of the column's maximum.
-__device__ __forceinline__ int tc_scale_exponent(uint32_t max_abs_bits) {
-    const int eb = (int)(max_abs_bits >> 23);           // biased exponent; 0 for zero and subnormals
-    if (max_abs_bits == 0u || eb == 255) return 0;
-    const int e = 9 - ((eb > 0 ? eb : 1) - 127);
-    return e < 126 ? e : 126;
-}
+// Scale of column b: x' = 2^e * x with e = tc_scale_exponent(max|x| over the
+// super-block's 256 values of the column); see that function.
 
 template <int NBP>
 __global__ void __launch_bounds__(256) prep_x_tc(const float *__restrict__ x, int k, int nb_cols,

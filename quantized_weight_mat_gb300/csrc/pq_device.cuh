@@ -27,6 +27,22 @@ __device__ __forceinline__ float4 ldg_f4(const float *p) {
     return __ldg(reinterpret_cast<const float4 *>(p));
 }
 
+// Power-of-two scale of x for the fp16 operands of the tensor-core kernels.
+// With E the binary exponent of m = max|x| over a block of x (m in
+// [2^E, 2^(E+1))), x' = 2^e * x with e = 9 - E, capped at 126 so that 2^e and
+// 2^-e are normal f32 numbers (a cap that only applies when m < 2^-117);
+// e = 0 when m is 0, inf or NaN (non-finite values then reach y as they would
+// unscaled).  Scaling by a power of two is exact, so x' = x_hi + x_lo (two
+// fp16 halves) holds x to a relative 2^-21 plus an absolute 2^-25 in scaled
+// units, i.e. about 2^-34 of the block's maximum; every x' and every sum of
+// 32 of them fits fp16's range.  Argument: the bits of m (sign cleared).
+__device__ __forceinline__ int tc_scale_exponent(uint32_t max_abs_bits) {
+    const int eb = (int)(max_abs_bits >> 23);           // biased exponent; 0 for zero and subnormals
+    if (max_abs_bits == 0u || eb == 255) return 0;
+    const int e = 9 - ((eb > 0 ? eb : 1) - 127);
+    return e < 126 ? e : 126;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
