@@ -2155,36 +2155,29 @@ inline bool takes(int64_t k, int64_t n_out, int batch) {
 }  // namespace rows6
 
 // ---------------------------------------------------------------------------
-// Q6_K at batch 2-4 for k = 4096 (the output head's shape): the products on
+// Q4_K and Q6_K at batch 3-8 for k = 4096 (the decode layer's QKV, O,
+// gate+up and 14336-row shapes, and the output head): the products on
 // mma.sync (m16n8k16, fp16 in, f32 accumulate) with both operands in
-// registers, one kernel per call.
+// registers, one launch per call.
 //
-// Stages are runs of 16 whole rows (one bulk copy each).  Compute warp w owns
-// super-block w of every row, so each warp covers a K range of 256 = 16 MMA
-// steps, and a step is exactly one 16-weight sub-block of one scale.
-//   B (x): built once per call by each warp for its own super-block: the
-//     hi and lo fp16 halves of x' = 2^e x (e per super-block and column, as
-//     in the tensor-core kernels), 8 MMA columns = 4 x columns x {hi, lo};
-//     a thread holds its 4 positions of every step, 32 registers.
-//   A (weights): rows g and g+8 of the 16-row stage, the 4 positions 4i..4i+3
-//     of the step (lane = 4g + i), decoded from the ql nibble and the qh bit
-//     pair to the exact fp16 q - 32.
-//   Per step the product of 16 rows x 8 columns is scaled by the signed
-//     sub-block scale of each row and added in f32; at the end of the stage
-//     the row's d and the column's 2^-e are applied and the 16 warps' sums
-//     are added in warp order through shared memory.
-namespace q6mma {
-constexpr int CWARPS = 16;                   // compute warps = super-blocks per row
-constexpr int THREADS = (CWARPS + 1) * 32;
+// Stages are runs of 16 whole rows (one bulk copy per row, rows PITCH bytes
+// apart so that the eight rows a warp's lanes read fall in different
+// shared-memory banks).  Warp w of the 16 owns super-block w of every row: a
+// K range of 256 = 16 MMA steps of 16 positions.
+//   B (x): built once per call by each warp for its own super-block: the hi
+//     and lo fp16 halves of x' = 2^e x (e per super-block and column, see
+//     tc_scale_exponent); per 8 MMA columns (4 x columns x {hi, lo}) a thread
+//     holds its 4 positions of every step in 32 registers.
+//   A (weights): rows g and g+8 of the stage, positions 4i..4i+3 of the step
+//     (lane = 4g + i), in the K slot order of the B fragment.
+//   The 16 warps' sums of a stage are added in warp order through shared
+//   memory after one barrier (by warps 0-1); after it the last warp's first
+//   thread refills the stage's ring slot, which no warp reads any more.
+namespace rmma {
+constexpr int CWARPS = 16;
+constexpr int THREADS = CWARPS * 32;
 constexpr int RS = 16;                       // rows per stage
-constexpr int NS = 4;                        // stages
 constexpr int K = 4096;
-constexpr int ROWB = (K / 256) * 210;        // 3360 bytes per row
-constexpr int STAGE = RS * ROWB;
-constexpr int RED = 2 * CWARPS * RS * 4;     // floats: two stages of [warp][row][column]
-constexpr int kSmem = NS * STAGE + RED * 4 + 128;
-static_assert(kSmem <= kSmemBudget - 512, "shared memory per CTA");
-static_assert(STAGE % 16 == 0, "bulk-copy size");
 
 struct Params {
     const uint8_t *w;
@@ -2192,8 +2185,10 @@ struct Params {
     float *y;
     long long ldy;
     int n_out;
-    int nb_cols;     // 1..4
+    int nb_cols;     // real columns (the others are zero)
     int early_w;     // stream weights before waiting on the previous kernel
+    int epi;         // kEpiNone, kEpiBias (bias[n_out]) or kEpiSwiGLU (n_out = 2 * pairs, gate rows first)
+    const float *bias;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -2204,26 +2199,295 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-
-// bytes (i, j) of the 6-bit codes word q as the fp16 pair (q_i - 32, q_j - 32):
-// 0x64 above a byte is the fp16 1024 + byte, and 1056 is subtracted exactly
-__device__ __forceinline__ uint32_t codes_h2(uint32_t q, uint32_t sel) {
-    const uint32_t p = __byte_perm(q, 0x64646464u, sel);
+__device__ __forceinline__ void mma16816_acc(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(0x64206420u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
     return r;
 }
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// two bytes of v chosen by sel (byte_perm nibbles i, 4, j, 4) as the fp16 pair
+// (v_i - off, v_j - off): 0x64 above a byte is the fp16 1024 + byte, and the
+// subtraction of OFF (an fp16 pair, 1024 + off) is exact
+template <uint32_t OFF>
+__device__ __forceinline__ uint32_t bytes_h2(uint32_t v, uint32_t sel) {
+    const uint32_t p = __byte_perm(v, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(p), "r"(OFF));
+    return r;
+}
+__host__ __device__ constexpr uint32_t pair_sel(uint32_t i, uint32_t j) { return i | 0x40u | (j << 8) | 0x4000u; }
 
-__global__ void __launch_bounds__(THREADS, 1) gemv_q6_k_mma(Params p) {
+// Stage u (rows_u rows) of this CTA into ring slot `slot`.
+template <int ROWB, int PITCH, int STAGE>
+__device__ __forceinline__ void issue_stage(uint8_t *smem, uint64_t *full, const uint8_t *src, int rows,
+                                            uint64_t pol) {
+    mbar_arrive_expect_tx(full, (uint32_t)rows * ROWB);
+    for (int r = 0; r < rows; ++r)
+        bulk_g2s_hint(smem + (size_t)r * PITCH, src + (size_t)r * ROWB, (uint32_t)ROWB, full, pol);
+}
+
+// B fragments of x columns 4t..4t+3 for this warp's super-block (see above);
+// optionally the sub-block sums of x' as the fp16 B fragment of the mins
+// product (K slots 2i, 2i+1 = sub-blocks 2i, 2i+1).  undo: 2^-e of the
+// thread's C column 4t + i.
+template <bool XSUMS>
+__device__ __forceinline__ void build_x(const Params &p, int t, int warp, int lane, uint32_t (&xb)[16][2],
+                                        uint32_t &xsb, float &undo) {
+    const int g = lane >> 2, i4 = lane & 3;
+    const int col = 4 * t + (g >> 1);
+    const bool lo_part = g & 1;
+    float v[16][4];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < p.nb_cols) a = ldg_f4(p.x + (size_t)col * K + warp * 256 + 16 * s + 4 * i4);
+        v[s][0] = a.x; v[s][1] = a.y; v[s][2] = a.z; v[s][3] = a.w;
+    }
+    uint32_t mb = 0;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mb = max(mb, __float_as_uint(v[s][j]) & 0x7fffffffu);
+    // the column's eight lanes (4 position groups x hi/lo copies) cover its 256 values
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+    const int e = tc_scale_exponent(mb);
+    const float mult = __uint_as_float((uint32_t)(127 + e) << 23);
+    const float und = __uint_as_float((uint32_t)(127 - e) << 23);
+    float xs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) xs[j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        uint32_t hv[4];
+        float ps = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float sx = v[s][j] * mult;
+            ps += sx;
+            const __half hi = __float2half_rn(sx);
+            const __half part = lo_part ? __float2half_rn(sx - __half2float(hi)) : hi;
+            hv[j] = __half_as_ushort(part);
+        }
+        if (XSUMS) xs[s >> 1] += ps;             // sub-block s/2 = steps 2j, 2j+1
+        xb[s][0] = hv[0] | (hv[2] << 16);
+        xb[s][1] = hv[1] | (hv[3] << 16);
+    }
+    if (XSUMS) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            xs[j] += __shfl_xor_sync(0xffffffffu, xs[j], 1);
+            xs[j] += __shfl_xor_sync(0xffffffffu, xs[j], 2);
+        }
+        // |x'| < 2^10, so a sum of 32 fits fp16's range
+        const float xa = (i4 >> 1) ? ((i4 & 1) ? xs[6] : xs[4]) : ((i4 & 1) ? xs[2] : xs[0]);
+        const float xc = (i4 >> 1) ? ((i4 & 1) ? xs[7] : xs[5]) : ((i4 & 1) ? xs[3] : xs[1]);
+        const __half ha = __float2half_rn(xa), hc = __float2half_rn(xc);
+        const __half pa = lo_part ? __float2half_rn(xa - __half2float(ha)) : ha;
+        const __half pc = lo_part ? __float2half_rn(xc - __half2float(hc)) : hc;
+        xsb = (uint32_t)__half_as_ushort(pa) | ((uint32_t)__half_as_ushort(pc) << 16);
+    }
+    // the C columns of this thread are 2i (hi) and 2i+1 (lo): x column 4t + i
+    undo = __shfl_sync(0xffffffffu, und, 8 * i4);
+}
+
+// Format policies: ROWB bytes per row, the ring depth for NT B tiles, and the
+// products of one stage for this warp's super-block (rows g, g+8 at aligned
+// shared addresses ra, rb), giving v[t][0..1] = y parts of rows g, g+8.
+struct Q4 {
+    static constexpr int ROWB = (K / 256) * 144;          // 2304
+    static constexpr int PITCH = ROWB + 16;
+    static constexpr bool XSUMS = true;
+    template <int NT> static constexpr int stages() { return 5; }
+    // sc*q exact: (1024+q)*sc - 1024*sc (low nibbles, sub-block 2c) and
+    // (1024+16q)*sc/16 - 64*sc (high nibbles, sub-block 2c+1); the mins
+    // through one product of the 6-bit mins with the sub-block sums;
+    // y += 2^-e * (d * (A.x') - dmin * (m.XS'))
+    template <int NT>
+    static __device__ __forceinline__ void stage(uint32_t ra, uint32_t rb, int warp, int lane,
+                                                 const uint32_t (&xb)[NT][16][2], const uint32_t (&xsb)[NT],
+                                                 const float (&undo)[NT], float (&v)[NT][2]) {
+        (void)warp;
+        const int i4 = lane & 3;
+        const uint4 ha = lds128(ra), hb = lds128(rb);
+        const uint32_t sca[2] = {ha.y & 0x3F3F3F3Fu, (ha.w & 0x0F0F0F0Fu) | ((ha.y >> 2) & 0x30303030u)};
+        const uint32_t scb[2] = {hb.y & 0x3F3F3F3Fu, (hb.w & 0x0F0F0F0Fu) | ((hb.y >> 2) & 0x30303030u)};
+        float c[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) c[t][0] = c[t][1] = c[t][2] = c[t][3] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t sw = (uint32_t)(2 * (cc & 1));
+            const uint32_t Sla = bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw, sw));
+            const uint32_t Slb = bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw, sw));
+            const uint32_t Sha = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x2C002C00u);
+            const uint32_t Shb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x2C002C00u);
+            const uint32_t Cla = hmul2_bits(Sla, 0xE400E400u), Clb = hmul2_bits(Slb, 0xE400E400u);
+            const uint32_t Cha = hmul2_bits(Sha, 0xE400E400u), Chb = hmul2_bits(Shb, 0xE400E400u);
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                const uint32_t off = 16u + 32u * cc + 16u * pp + 4u * i4;
+                const uint32_t wa = rowk::lds32(ra + off), wb = rowk::lds32(rb + off);
+                const uint32_t sa = wa >> 8, sb = wb >> 8;
+                const uint32_t l0 = hfma2_bits((wa & 0x000F000Fu) | 0x64006400u, Sla, Cla);
+                const uint32_t l1 = hfma2_bits((wb & 0x000F000Fu) | 0x64006400u, Slb, Clb);
+                const uint32_t l2 = hfma2_bits((sa & 0x000F000Fu) | 0x64006400u, Sla, Cla);
+                const uint32_t l3 = hfma2_bits((sb & 0x000F000Fu) | 0x64006400u, Slb, Clb);
+                const uint32_t h0 = hfma2_bits((wa & 0x00F000F0u) | 0x64006400u, Sha, Cha);
+                const uint32_t h1 = hfma2_bits((wb & 0x00F000F0u) | 0x64006400u, Shb, Chb);
+                const uint32_t h2 = hfma2_bits((sa & 0x00F000F0u) | 0x64006400u, Sha, Cha);
+                const uint32_t h3 = hfma2_bits((sb & 0x00F000F0u) | 0x64006400u, Shb, Chb);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    mma16816_acc(c[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
+                    mma16816_acc(c[t], h0, h1, h2, h3, xb[t][4 * cc + pp + 2][0], xb[t][4 * cc + pp + 2][1]);
+                }
+            }
+        }
+        // mins: K slots 2i, 2i+1 = sub-blocks 2i, 2i+1 of rows g, g+8
+        const uint32_t mwa = (i4 >> 1) ? (((ha.w >> 4) & 0x0F0F0F0Fu) | ((ha.z >> 2) & 0x30303030u)) : (ha.z & 0x3F3F3F3Fu);
+        const uint32_t mwb = (i4 >> 1) ? (((hb.w >> 4) & 0x0F0F0F0Fu) | ((hb.z >> 2) & 0x30303030u)) : (hb.z & 0x3F3F3F3Fu);
+        const uint32_t ms = (uint32_t)(2 * (i4 & 1));
+        const uint32_t ma = bytes_h2<0x64006400u>(mwa, pair_sel(ms, ms + 1));
+        const uint32_t mbb = bytes_h2<0x64006400u>(mwb, pair_sel(ms, ms + 1));
+        const float da = h2f(ha.x), dma = h2f(ha.x >> 16), db = h2f(hb.x), dmb = h2f(hb.x >> 16);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float cm[4];
+            mma16816(cm, ma, mbb, 0u, 0u, xsb[t], 0u);
+            v[t][0] = undo[t] * fmaf(da, c[t][0] + c[t][1], -dma * (cm[0] + cm[1]));
+            v[t][1] = undo[t] * fmaf(db, c[t][2] + c[t][3], -dmb * (cm[2] + cm[3]));
+        }
+    }
+};
+
+struct Q6 {
+    static constexpr int ROWB = (K / 256) * 210;          // 3360
+    static constexpr int PITCH = ROWB + 16;
+    static constexpr bool XSUMS = false;
+    template <int NT> static constexpr int stages() { return NT == 1 ? 4 : 3; }
+    // q - 32 exact from the ql nibble and the qh bit pair; a step is one
+    // 16-weight sub-block, so each product is scaled by its signed 8-bit
+    // scale as it is added; y += 2^-e * d * sum(sc * (A.x'))
+    template <int NT>
+    static __device__ __forceinline__ void stage(uint32_t ra, uint32_t rb, int warp, int lane,
+                                                 const uint32_t (&xb)[NT][16][2], const uint32_t (&xsb)[NT],
+                                                 const float (&undo)[NT], float (&v)[NT][2]) {
+        (void)xsb;
+        const int i4 = lane & 3;
+        // the super-block starts 2-byte aligned (ra, rb are the aligned
+        // addresses below it): word loads realigned by one byte permute
+        const uint32_t delta = ((uint32_t)warp * 210u) & 2u;
+        const uint32_t sel = delta ? 0x5432u : 0x3210u;
+        auto ldw = [&](uint32_t a) { return __byte_perm(rowk::lds32(a), rowk::lds32(a + 4u), sel); };
+        uint32_t sc0[4], sc1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            sc0[j] = ldw(ra + 192u + 4u * j);
+            sc1[j] = ldw(rb + 192u + 4u * j);
+        }
+        const float d0 = h2f(rowk::lds32(ra + 208u) >> (delta ? 16u : 0u));
+        const float d1 = h2f(rowk::lds32(rb + 208u) >> (delta ? 16u : 0u));
+        float acc[NT][2];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int sp = 0; sp < 2; ++sp) {
+                const uint32_t oh = 128u + 32u * h + 16u * sp + 4u * i4;
+                const uint32_t qh0 = ldw(ra + oh), qh1 = ldw(rb + oh);
+#pragma unroll
+                for (int t1 = 0; t1 < 2; ++t1) {
+                    const uint32_t ol = 64u * h + 32u * t1 + 16u * sp + 4u * i4;
+                    const uint32_t ql0 = ldw(ra + ol), ql1 = ldw(rb + ol);
+#pragma unroll
+                    for (int hn = 0; hn < 2; ++hn) {
+                        const int r = t1 + 2 * hn;                      // run 0..3 of the half
+                        const int s = 8 * h + 2 * r + sp;               // step = scale index
+                        const uint32_t lo0 = (hn ? (ql0 >> 4) : ql0) & 0x0F0F0F0Fu;
+                        const uint32_t lo1 = (hn ? (ql1 >> 4) : ql1) & 0x0F0F0F0Fu;
+                        const uint32_t hb0 = (r < 3 ? (qh0 << (4 - 2 * r)) : (qh0 >> 2)) & 0x30303030u;
+                        const uint32_t hb1 = (r < 3 ? (qh1 << (4 - 2 * r)) : (qh1 >> 2)) & 0x30303030u;
+                        const uint32_t q0 = lo0 | hb0, q1 = lo1 | hb1;
+                        // (q - 32) pairs: subtract the fp16 1056 = 1024 + 32
+                        const uint32_t a0 = bytes_h2<0x64206420u>(q0, pair_sel(0, 2));
+                        const uint32_t a1 = bytes_h2<0x64206420u>(q1, pair_sel(0, 2));
+                        const uint32_t a2 = bytes_h2<0x64206420u>(q0, pair_sel(1, 3));
+                        const uint32_t a3 = bytes_h2<0x64206420u>(q1, pair_sel(1, 3));
+                        const float sa = (float)(int)(int8_t)(sc0[s >> 2] >> (8 * (s & 3)));
+                        const float sb = (float)(int)(int8_t)(sc1[s >> 2] >> (8 * (s & 3)));
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            float c[4];
+                            mma16816(c, a0, a1, a2, a3, xb[t][s][0], xb[t][s][1]);
+                            acc[t][0] = fmaf(sa, c[0] + c[1], acc[t][0]);
+                            acc[t][1] = fmaf(sb, c[2] + c[3], acc[t][1]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            v[t][0] = d0 * undo[t] * acc[t][0];
+            v[t][1] = d1 * undo[t] * acc[t][1];
+        }
+    }
+};
+
+template <class F, int NT> constexpr int stage_bytes() { return RS * F::PITCH; }
+template <int NT> constexpr int red_floats() { return 2 * CWARPS * RS * 4 * NT; }
+template <class F, int NT> constexpr int smem_bytes() {
+    return F::template stages<NT>() * stage_bytes<F, NT>() + red_floats<NT>() * 4 + 128;
+}
+static_assert(smem_bytes<Q4, 2>() <= kSmemBudget - 512 && smem_bytes<Q6, 1>() <= kSmemBudget - 512 &&
+                  smem_bytes<Q6, 2>() <= kSmemBudget - 512,
+              "shared memory per CTA");
+
+// With 4 columns (NT = 1) a producer warp streams the stages, released by
+// per-slot empty barriers, and the block has 17 warps (96 registers each);
+// with 8 (NT = 2) the x fragments need 128 registers, so the block has the
+// 16 compute warps only and a thread of the last warp refills each slot
+// after the stage's barrier.
+template <int NT> constexpr bool has_producer() { return NT == 1; }
+template <int NT> constexpr int block_threads() { return has_producer<NT>() ? THREADS + 32 : THREADS; }
+
+template <class F, int NT>
+__global__ void __launch_bounds__(block_threads<NT>(), 1) gemv_rows_mma(Params p) {
+    constexpr int NS = F::template stages<NT>();
+    constexpr int STAGE = stage_bytes<F, NT>();
+    constexpr int NB = 4 * NT;                   // x columns
+    constexpr bool PROD = has_producer<NT>();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[NS], empty_bar[NS];
     float *red = reinterpret_cast<float *>(smem + NS * STAGE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r0 = (int64_t)p.n_out * blockIdx.x / gridDim.x;
-    const int nrows = (int)((int64_t)p.n_out * (blockIdx.x + 1) / gridDim.x - r0);
-    const int units = (nrows + RS - 1) / RS;
+    const int g = lane >> 2, i4 = lane & 3;
+    // items: rows, or for SwiGLU (gate, up) row pairs, RS/2 pairs per stage
+    // (gate rows in stage rows 0-7, their up rows in 8-15)
+    const bool sw = p.epi == kEpiSwiGLU;
+    const int64_t n_items = sw ? p.n_out / 2 : p.n_out;
+    const int per_stage = sw ? RS / 2 : RS;
+    const int64_t r0 = n_items * blockIdx.x / gridDim.x;
+    const int nrows = (int)(n_items * (blockIdx.x + 1) / gridDim.x - r0);
+    const int units = (nrows + per_stage - 1) / per_stage;
     const uint32_t ring_s = smem_u32(smem);
+    uint64_t pol = 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -2234,185 +2498,144 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_q6_k_mma(Params p) {
     }
     rowk::grid_dep_launch();
     __syncthreads();
-
-    if (warp == CWARPS) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            if (!p.early_w) rowk::grid_dep_wait();   // the weights may be the previous kernel's output
-            const uint64_t pol = make_evict_first_policy();
-            const uint8_t *src = p.w + r0 * (int64_t)ROWB;
-            for (int u = 0; u < units; ++u) {
-                const int slot = u % NS;
-                const uint32_t ph = (uint32_t)(u / NS) & 1u;
-                const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
-                const uint32_t bytes = (uint32_t)rows * ROWB;
-                if (!mbar_wait(&empty_bar[slot], ph ^ 1u)) break;
-                mbar_arrive_expect_tx(&full_bar[slot], bytes);
-                bulk_g2s_hint(smem + (size_t)slot * STAGE, src, bytes, &full_bar[slot], pol);
-                src += (size_t)RS * ROWB;
+    auto fill = [&](int u) {                     // stage u into slot u % NS
+        const int rows = nrows - u * per_stage < per_stage ? nrows - u * per_stage : per_stage;
+        uint8_t *dst = smem + (size_t)(u % NS) * STAGE;
+        const uint8_t *src = p.w + (r0 + (int64_t)u * per_stage) * F::ROWB;
+        if (!sw) {
+            issue_stage<F::ROWB, F::PITCH, STAGE>(dst, &full_bar[u % NS], src, rows, pol);
+        } else {
+            mbar_arrive_expect_tx(&full_bar[u % NS], (uint32_t)(2 * rows) * F::ROWB);
+            const size_t up = (size_t)(p.n_out / 2) * F::ROWB;
+            for (int r = 0; r < rows; ++r) {
+                bulk_g2s_hint(dst + (size_t)r * F::PITCH, src + (size_t)r * F::ROWB, (uint32_t)F::ROWB,
+                              &full_bar[u % NS], pol);
+                bulk_g2s_hint(dst + (size_t)(r + RS / 2) * F::PITCH, src + up + (size_t)r * F::ROWB,
+                              (uint32_t)F::ROWB, &full_bar[u % NS], pol);
             }
         }
-        return;
-    }
-
-    // ---------------- compute warps: super-block w of every row ----------------
-    const int g = lane >> 2, i4 = lane & 3;
-    bool dead = false;
-    rowk::grid_dep_wait();                         // x is the previous kernel's output
-    // B fragments: MMA column n = g is x column g/2, part g%2 (hi, lo);
-    // register pair s holds positions 4 i4 + {0, 2} and 4 i4 + {1, 3} of step s
-    uint32_t xb[16][2];
-    float undo;
-    {
-        const int col = g >> 1;
-        float v[16][4];
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (col < p.nb_cols) a = ldg_f4(p.x + (size_t)col * K + warp * 256 + 16 * s + 4 * i4);
-            v[s][0] = a.x; v[s][1] = a.y; v[s][2] = a.z; v[s][3] = a.w;
-        }
-        uint32_t mb = 0;
-#pragma unroll
-        for (int s = 0; s < 16; ++s)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) mb = max(mb, __float_as_uint(v[s][j]) & 0x7fffffffu);
-        // the column's eight lanes (4 positions x hi/lo copies) cover its 256 values
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-        const int e = tc_scale_exponent(mb);
-        const float mult = __uint_as_float((uint32_t)(127 + e) << 23);
-        const float und = __uint_as_float((uint32_t)(127 - e) << 23);
-        const bool lo_part = g & 1;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            uint32_t hv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float sx = v[s][j] * mult;
-                const __half hi = __float2half_rn(sx);
-                const __half part = lo_part ? __float2half_rn(sx - __half2float(hi)) : hi;
-                hv[j] = __half_as_ushort(part);
-            }
-            xb[s][0] = hv[0] | (hv[2] << 16);
-            xb[s][1] = hv[1] | (hv[3] << 16);
-        }
-        // the C columns of this thread are 2 i4 (hi) and 2 i4 + 1 (lo) of x column i4
-        undo = __shfl_sync(0xffffffffu, und, 8 * i4);
-    }
-
-    // this warp's super-block in a stage row: 2-byte aligned; word loads from
-    // the aligned address below it, realigned by one byte permute
-    const uint32_t blk0 = (uint32_t)warp * 210u;
-    const uint32_t delta = blk0 & 2u;
-    const uint32_t sel = delta ? 0x5432u : 0x3210u;
-    const uint32_t dsh = delta ? 16u : 0u;
-    auto ldw = [&](uint32_t a) {                     // realigned word at byte offset a - delta + delta
-        return __byte_perm(rowk::lds32(a), rowk::lds32(a + 4u), sel);
     };
+    // PROD: the producer warp's first thread issues every copy; else the first
+    // thread of the last compute warp
+    constexpr int FILLER = PROD ? THREADS : THREADS - 32;
+    if (threadIdx.x == FILLER) {
+        pol = make_evict_first_policy();
+        // the weights may be the previous kernel's output unless the caller
+        // declared them static (pq_set_weight_prefetch)
+        if (!p.early_w) rowk::grid_dep_wait();
+        if (PROD) {
+            for (int u = 0; u < units; ++u) {
+                if (u >= NS && !mbar_wait(&empty_bar[u % NS], ((uint32_t)(u / NS) & 1u) ^ 1u)) break;
+                fill(u);
+            }
+        } else {
+            for (int u = 0; u < NS && u < units; ++u) fill(u);
+        }
+    }
+    if (PROD && warp == CWARPS) return;
+    rowk::grid_dep_wait();                       // x is the previous kernel's output
+    uint32_t xb[NT][16][2], xsb[NT] = {};
+    float undo[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) build_x<F::XSUMS>(p, t, warp, lane, xb[t], xsb[t], undo[t]);
 
+    bool dead = false;
+    const uint32_t blk = (uint32_t)warp * (uint32_t)(F::ROWB / 16);   // this warp's super-block in a row
     for (int u = 0; u < units; ++u) {
         const int slot = u % NS;
         const uint32_t ph = (uint32_t)(u / NS) & 1u;
         if (!dead && !mbar_wait(&full_bar[slot], ph)) dead = true;
-        const uint32_t st = ring_s + (uint32_t)slot * STAGE;
-        const uint32_t ra = st + (uint32_t)g * ROWB + blk0 - delta;          // row g, aligned
-        const uint32_t rb = ra + 8u * ROWB;                                  // row g + 8
-        float acc0 = 0.f, acc1 = 0.f;
-        float d0 = 0.f, d1 = 0.f;
-        if (!dead) {
-            uint32_t sc0[4], sc1[4];
+        const uint32_t ra = (ring_s + (uint32_t)slot * STAGE + (uint32_t)g * F::PITCH + blk) & ~3u;
+        const uint32_t rb = ra + 8u * F::PITCH;
+        float v[NT][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sc0[j] = ldw(ra + 192u + 4u * j);
-                sc1[j] = ldw(rb + 192u + 4u * j);
-            }
-            d0 = h2f(rowk::lds32(ra + 208u) >> dsh);
-            d1 = h2f(rowk::lds32(rb + 208u) >> dsh);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int sp = 0; sp < 2; ++sp) {
-                    // qh word of positions 16 sp + 4 i4 of half h: bit pairs of runs 0-3
-                    const uint32_t oh = 128u + 32u * h + 16u * sp + 4u * i4;
-                    const uint32_t qh0 = ldw(ra + oh), qh1 = ldw(rb + oh);
-#pragma unroll
-                    for (int t1 = 0; t1 < 2; ++t1) {
-                        // ql word of runs t1 (low nibbles) and t1 + 2 (high nibbles)
-                        const uint32_t ol = 64u * h + 32u * t1 + 16u * sp + 4u * i4;
-                        const uint32_t ql0 = ldw(ra + ol), ql1 = ldw(rb + ol);
-#pragma unroll
-                        for (int hn = 0; hn < 2; ++hn) {
-                            const int t = t1 + 2 * hn;                      // run 0..3
-                            const int s = 8 * h + 2 * t + sp;               // step = scale index
-                            const uint32_t lo0 = (hn ? (ql0 >> 4) : ql0) & 0x0F0F0F0Fu;
-                            const uint32_t lo1 = (hn ? (ql1 >> 4) : ql1) & 0x0F0F0F0Fu;
-                            const uint32_t hb0 = (t < 3 ? (qh0 << (4 - 2 * t)) : (qh0 >> 2)) & 0x30303030u;
-                            const uint32_t hb1 = (t < 3 ? (qh1 << (4 - 2 * t)) : (qh1 >> 2)) & 0x30303030u;
-                            const uint32_t q0 = lo0 | hb0, q1 = lo1 | hb1;
-                            float c[4];
-                            mma16816(c, codes_h2(q0, 0x4240u), codes_h2(q1, 0x4240u), codes_h2(q0, 0x4341u),
-                                     codes_h2(q1, 0x4341u), xb[s][0], xb[s][1]);
-                            const int sa = (int)(int8_t)(sc0[s >> 2] >> (8 * (s & 3)));
-                            const int sb = (int)(int8_t)(sc1[s >> 2] >> (8 * (s & 3)));
-                            acc0 = fmaf((float)sa, c[0] + c[1], acc0);
-                            acc1 = fmaf((float)sb, c[2] + c[3], acc1);
-                        }
-                    }
-                }
-            }
+        for (int t = 0; t < NT; ++t) v[t][0] = v[t][1] = 0.f;
+        if (!dead) F::template stage<NT>(ra, rb, warp, lane, xb, xsb, undo, v);
+        if (PROD) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-        // this warp's part of rows g, g+8 of the stage, x column i4
-        float *rw = red + (size_t)(u & 1) * CWARPS * RS * 4 + (size_t)warp * RS * 4;
-        rw[g * 4 + i4] = d0 * undo * acc0;
-        rw[(g + 8) * 4 + i4] = d1 * undo * acc1;
-        named_sync(1, CWARPS * 32);
-        if (threadIdx.x < RS * 4) {
-            const int row = threadIdx.x >> 2, col = threadIdx.x & 3;
-            const float *rr = red + (size_t)(u & 1) * CWARPS * RS * 4 + row * 4 + col;
+        float *rw = red + (size_t)(u & 1) * CWARPS * RS * NB + (size_t)warp * RS * NB;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            rw[g * NB + 4 * t + i4] = v[t][0];
+            rw[(g + 8) * NB + 4 * t + i4] = v[t][1];
+        }
+        named_sync(1, THREADS);
+        // !PROD: every warp is done with the slot: refill it (after ordering
+        // those reads before the copy engine's writes)
+        if (!PROD && threadIdx.x == FILLER && u + NS < units) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fill(u + NS);
+        }
+        if (threadIdx.x < per_stage * NB) {
+            const int row = threadIdx.x / NB, col = threadIdx.x % NB;
+            const float *rr = red + (size_t)(u & 1) * CWARPS * RS * NB + row * NB + col;
             float sum = rr[0];
 #pragma unroll
-            for (int w2 = 1; w2 < CWARPS; ++w2) sum += rr[(size_t)w2 * RS * 4];
-            const int n_here = nrows - u * RS < RS ? nrows - u * RS : RS;
-            if (row < n_here && col < p.nb_cols) p.y[(size_t)col * p.ldy + r0 + (int64_t)u * RS + row] = sum;
+            for (int w2 = 1; w2 < CWARPS; ++w2) sum += rr[(size_t)w2 * RS * NB];
+            const int n_here = nrows - u * per_stage < per_stage ? nrows - u * per_stage : per_stage;
+            const int64_t item = r0 + (int64_t)u * per_stage + row;
+            if (sw) {
+                // the up row of the pair: stage row row + 8
+                const float *ru = rr + (RS / 2) * NB;
+                float up = ru[0];
+#pragma unroll
+                for (int w2 = 1; w2 < CWARPS; ++w2) up += ru[(size_t)w2 * RS * NB];
+                sum = rowk::silu(sum) * up;
+            } else if (p.epi == kEpiBias) {
+                if (row < n_here) sum += p.bias[item];
+            }
+            if (row < n_here && col < p.nb_cols) p.y[(size_t)col * p.ldy + item] = sum;
         }
     }
 }
 
-cudaError_t launch(const uint8_t *w, int64_t n_out, const float *x, int nb_cols, float *y, int64_t ldy, int grid,
-                   cudaStream_t s, int early_w) {
+template <class F, int NT>
+cudaError_t launch_t(const uint8_t *w, int64_t n_out, const float *x, int nb_cols, float *y, int64_t ldy, int grid,
+                     cudaStream_t s, int early_w, const Epilogue &epi) {
     static PerDeviceOnce configured;
     const cudaError_t ce = configured.run([] {
-        return cudaFuncSetAttribute(gemv_q6_k_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        return cudaFuncSetAttribute(gemv_rows_mma<F, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_bytes<F, NT>());
     });
     if (ce != cudaSuccess) return ce;
-    Params p{w, x, y, (long long)ldy, (int)n_out, nb_cols, early_w};
+    Params p{w, x, y, (long long)ldy, (int)n_out, nb_cols, early_w, epi.kind,
+             epi.kind == kEpiBias ? epi.bias : nullptr};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = (size_t)kSmem;
+    cfg.blockDim = dim3(block_threads<NT>());
+    cfg.dynamicSmemBytes = (size_t)smem_bytes<F, NT>();
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_q6_k_mma, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_mma<F, NT>, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Whether this kernel runs Q6_K (k, n_out) at `batch` columns: k = 4096,
-// batch 3-4, and at least one 16-row stage per CTA on a full GPU (smaller
-// matrices keep the CUDA-core kernel).  At batch 2 the CUDA-core kernel is
-// faster (output head 128256x4096: 83.7 against 96.2 us; at batch 4 this one
-// takes 96.9 against 124).
-inline bool takes(int64_t k, int64_t n_out, int batch) {
-    return k == K && batch >= 3 && batch <= 4 && n_out >= 152 * RS;
+// grid: CTAs, at most one per row (per row pair for SwiGLU).
+cudaError_t launch(int fmt, const uint8_t *w, int64_t n_out, const float *x, int nb_cols, float *y, int64_t ldy,
+                   int grid, cudaStream_t s, int early_w, const Epilogue &epi = Epilogue{}) {
+    if (fmt == PQ_Q4_K)
+        return nb_cols <= 4 ? launch_t<Q4, 1>(w, n_out, x, nb_cols, y, ldy, grid, s, early_w, epi)
+                            : launch_t<Q4, 2>(w, n_out, x, nb_cols, y, ldy, grid, s, early_w, epi);
+    return nb_cols <= 4 ? launch_t<Q6, 1>(w, n_out, x, nb_cols, y, ldy, grid, s, early_w, epi)
+                        : launch_t<Q6, 2>(w, n_out, x, nb_cols, y, ldy, grid, s, early_w, epi);
 }
-}  // namespace q6mma
+
+// Whether this kernel runs (fmt, k, n_out) at `batch` columns.  Q4_K: k =
+// 4096, batch 2-8; Q6_K: k = 4096, batch 3-8, and at least one 16-row stage
+// per CTA on a full GPU (at batch 2, and on small matrices, the CUDA-core
+// kernel is faster: output head 83.5 against 93 us at batch 2).
+inline bool takes(int fmt, int64_t k, int64_t n_out, int batch) {
+    if (k != K || batch < 2 || batch > 8 || n_out < 1) return false;
+    if (fmt == PQ_Q4_K) return true;
+    return fmt == PQ_Q6_K && batch >= 3 && n_out >= 152 * RS;
+}
+}  // namespace rmma
 
 }  // namespace
 
@@ -2427,22 +2650,27 @@ unsigned stream_wait_timeouts(bool reset) {
 }
 
 bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kind) {
+    if (batch > 1) return rmma::takes(fmt, k, n_out, batch);
     return batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out, kind == kEpiSwiGLU);
 }
 
+bool stream_mma_takes(int fmt, int64_t n_out, int64_t k, int batch) { return rmma::takes(fmt, k, n_out, batch); }
+
 bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch) {
     if (batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out)) return true;
+    if (rmma::takes(fmt, k, n_out, batch)) return true;
     if (fmt == PQ_Q6_K && batch >= 2) return rows6::takes(k, n_out, batch);
     if (fmt != PQ_Q4_K || batch < 1 || batch > 4 || n_out < 1) return false;
     if (k % 256 || k > (INT64_C(1) << 20)) return false;
     return plan_stages(k, batch) >= 2;
 }
 
-cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
-                                   cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi) {
-    if (!stream_epilogue_fused(fmt, n_out, k, 1, epi.kind)) return cudaErrorInvalidValue;
+cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
+                                   float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi) {
+    if (!stream_epilogue_fused(fmt, n_out, k, batch, epi.kind)) return cudaErrorInvalidValue;
     const int64_t items = epi.kind == kEpiSwiGLU ? n_out / 2 : n_out;
     const int grid = (int)(items < dev.sm_count ? items : dev.sm_count);
+    if (batch > 1) return rmma::launch(fmt, w, n_out, x, batch, y, ldy, grid, s, weight_prefetch(), epi);
     switch (fmt) {
     case PQ_Q4_K: return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q6_K: return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
@@ -2462,11 +2690,11 @@ cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t
     Params p{w, x, y, (long long)ldy, (int)n_out, (int)k, 0};
     const int grid = (int)(n_out < dev.sm_count ? n_out : dev.sm_count);
     if (batch == 1 && rowk::takes(fmt, k, n_out))
-        return launch_gemv_stream_epi(fmt, w, n_out, k, x, y, s, dev, Epilogue{});
+        return launch_gemv_stream_epi(fmt, w, n_out, k, x, 1, y, ldy, s, dev, Epilogue{});
+    if (rmma::takes(fmt, k, n_out, batch))
+        return rmma::launch(fmt, w, n_out, x, batch, y, ldy, grid, s, weight_prefetch());
     if (fmt == PQ_Q4_K && rowsnb::takes(k, n_out, batch))
         return rowsnb::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s);
-    if (fmt == PQ_Q6_K && q6mma::takes(k, n_out, batch))
-        return q6mma::launch(w, n_out, x, batch, y, ldy, grid, s, weight_prefetch());
     if (fmt == PQ_Q6_K)
         return batch == 2 ? rows6::launch<2>(w, n_out, k, x, 2, y, ldy, grid, s)
                           : rows6::launch<4>(w, n_out, k, x, batch, y, ldy, grid, s);

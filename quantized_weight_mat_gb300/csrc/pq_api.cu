@@ -132,6 +132,9 @@ int check_gemv(int fmt, const void *w, int n_out, int k, const float *x, int bat
 // CUDA-core kernels are slower: long rows (k >= 8192), and at batch 4 large
 // matrices (>= 2^25 weights); measured on 4096x14336, 14336x4096, 28672x4096.
 int choose(int fmt, int64_t n_out, int64_t k, int nb) {
+    // Q4_K / Q6_K at k = 4096, batch 3-8: the register-operand whole-row kernel
+    // (14336x4096 batch 4: 12.1 us against 17.4 for the tensor-core kernel)
+    if (nb <= 8 && stream_mma_takes(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
     const bool tc_pays = nb >= 5 || (nb >= 3 && k >= 8192) || (nb == 4 && n_out * k >= (INT64_C(1) << 25));
     if (tc_pays && tc_supported(fmt, n_out, k, nb)) return PQ_KERNEL_TC;
     if (nb <= 4 && stream_supported(fmt, n_out, k, nb)) return PQ_KERNEL_STREAM;
@@ -152,7 +155,9 @@ int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &
     for (int b0 = 0; b0 < batch;) {
         int nb = batch - b0 < 32 ? batch - b0 : 32;
         int kern = forced >= 0 ? forced : choose(fmt, n_out, k, nb);
-        if (kern != PQ_KERNEL_TC && nb > 4) nb = 4;
+        if (kern != PQ_KERNEL_TC && nb > 4 && !(kern == PQ_KERNEL_STREAM && stream_mma_takes(fmt, n_out, k, nb < 8 ? nb : 8)))
+            nb = 4;
+        if (kern == PQ_KERNEL_STREAM && nb > 8) nb = 8;
         // a streaming kernel that takes one column at a time runs column by column
         if (kern == PQ_KERNEL_STREAM && nb > 1 && !stream_supported(fmt, n_out, k, nb) &&
             stream_supported(fmt, n_out, k, 1))
@@ -188,7 +193,7 @@ int gemv_epi_impl(int fmt, const void *w_blocks, int n_out, int k, const float *
         if (kern == PQ_KERNEL_TC) {
             e = launch_gemv_tc(fmt, w, n_out, k, xb, nb, yb, ldy, stream, *dev, epi);
         } else if (kern == PQ_KERNEL_STREAM && stream_epilogue_fused(fmt, n_out, k, nb, epi.kind)) {
-            e = launch_gemv_stream_epi(fmt, w, n_out, k, xb, yb, stream, *dev, epi);
+            e = launch_gemv_stream_epi(fmt, w, n_out, k, xb, nb, yb, ldy, stream, *dev, epi);
         } else {
             // plain mat-vec, then the epilogue kernel
             float *out = yb;

@@ -73,16 +73,21 @@ cudaError_t launch_gemv_generic(int fmt, const uint8_t *w, int64_t n_out, int64_
                                 cudaStream_t s, int sm_count);
 
 // Streaming kernel (bulk-copy ring).  `supported` reports whether it can run
-// this case; the launcher handles batch <= 4.
+// this case; the launcher handles batch <= 4, and batch <= 8 where
+// `stream_mma_takes` (the register-operand whole-row kernel: Q4_K and Q6_K at
+// k = 4096, batch 3-8) holds.
 bool stream_supported(int fmt, int64_t n_out, int64_t k, int batch);
+bool stream_mma_takes(int fmt, int64_t n_out, int64_t k, int batch);
 cudaError_t launch_gemv_stream(int fmt, const uint8_t *w, int64_t n_out, int64_t k,
                                const float *x, int batch, float *y, int64_t ldy,
                                cudaStream_t s, const DeviceInfo &dev);
-// The batch-1 whole-row kernel with the epilogue fused into its stores
-// (Q4_K and Q6_K); `stream_epilogue_fused` says whether it takes the case.
+// The batch-1 whole-row kernel (every format with a whole-row policy) and
+// the register-operand whole-row kernel (batch 2-8) with the epilogue fused
+// into their stores; `stream_epilogue_fused` says whether one takes the case.
+// y has leading dimension ldy (for SwiGLU: n_out / 2 outputs per column).
 bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kind);
-cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, float *y,
-                                   cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi);
+cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int64_t k, const float *x, int batch,
+                                   float *y, int64_t ldy, cudaStream_t s, const DeviceInfo &dev, const Epilogue &epi);
 
 // Tensor-core kernel (tcgen05): Q4_K, batch chunks of 8 or 16.
 bool tc_supported(int fmt, int64_t n_out, int64_t k, int batch);

@@ -155,12 +155,14 @@ def test_q4_k_dispatch_matches_the_measured_winners():
     # the streaming kernels up to the batch where the tensor-core kernel wins,
     # the tensor-core kernel from batch 5 on
     S, T = pq.KERNEL_STREAM, pq.KERNEL_TC
+    # (at k = 4096 batch 3-8 is the register-operand whole-row kernel, a
+    # streaming kernel: one pass over W for up to 8 columns)
     table = {
-        (14336, 4096): [S, S, S, T, T, T, T],
+        (14336, 4096): [S, S, S, S, S, S, T],
         (4096, 14336): [S, S, T, T, T, T, T],
-        (28672, 4096): [S, S, S, T, T, T, T],
-        (6144, 4096): [S, S, S, S, T, T, T],
-        (4096, 4096): [S, S, S, S, T, T, T],
+        (28672, 4096): [S, S, S, S, S, S, T],
+        (6144, 4096): [S, S, S, S, S, S, T],
+        (4096, 4096): [S, S, S, S, S, S, T],
     }
     for (n, k), want in table.items():
         got = [pq.pq_gemv_choice("q4_k", n, k, b) for b in (1, 2, 3, 4, 5, 8, 16)]
@@ -169,10 +171,13 @@ def test_q4_k_dispatch_matches_the_measured_winners():
     for b, launches in ((17, 1), (32, 1), (33, 2), (64, 2), (65, 3)):
         assert pq.pq_gemv_choice("q4_k", 14336, 4096, b) == T
         assert pq.pq_gemv_launches("q4_k", 14336, 4096, b) == launches
-    # the Q6_K head streams W once per call for up to 4 columns, in passes of 4
+    # the Q6_K head streams W once per call for up to 8 columns, in passes of 8
     assert [pq.pq_gemv_choice("q6_k", 128256, 4096, b) for b in (1, 2, 3, 4, 8)] == [S] * 5
-    for b, launches in ((1, 1), (2, 1), (3, 1), (4, 1), (5, 2), (8, 2), (16, 4), (17, 5)):
+    for b, launches in ((1, 1), (2, 1), (3, 1), (4, 1), (5, 1), (8, 1), (16, 2), (17, 3)):
         assert pq.pq_gemv_launches("q6_k", 128256, 4096, b) == launches
+    # Q4_K at k = 4096: batches 5-8 in one streaming pass too, 9-16 on the tensor-core kernel
+    for b, launches in ((5, 1), (8, 1), (9, 1), (16, 1)):
+        assert pq.pq_gemv_launches("q4_k", 14336, 4096, b) == launches
     # rows that are not whole 16-byte units (k not a multiple of 2048) take
     # the generic kernel
     assert pq.pq_gemv_choice("q6_k", 4096, 768, 2) == pq.KERNEL_GENERIC
