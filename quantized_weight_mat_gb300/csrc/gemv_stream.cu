@@ -2242,63 +2242,85 @@ __device__ __forceinline__ void issue_stage(uint8_t *smem, uint64_t *full, const
 // optionally the sub-block sums of x' as the fp16 B fragment of the mins
 // product (K slots 2i, 2i+1 = sub-blocks 2i, 2i+1).  undo: 2^-e of the
 // thread's C column 4t + i.
+// The two lanes of a column (hi and lo part, lanes 4g+i and 4(g^1)+i) each
+// load half of the column's steps (the hi lane steps 0-7, the lo lane 8-15),
+// split their values into both halves, and swap the halves the other needs:
+// x is read once per CTA.
 template <bool XSUMS>
 __device__ __forceinline__ void build_x(const Params &p, int t, int warp, int lane, uint32_t (&xb)[16][2],
                                         uint32_t &xsb, float &undo) {
     const int g = lane >> 2, i4 = lane & 3;
     const int col = 4 * t + (g >> 1);
     const bool lo_part = g & 1;
-    float v[16][4];
+    const int s0 = lo_part ? 8 : 0;              // the steps this lane loads
+    float v[8][4];
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
+    for (int s = 0; s < 8; ++s) {
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (col < p.nb_cols) a = ldg_f4(p.x + (size_t)col * K + warp * 256 + 16 * s + 4 * i4);
+        if (col < p.nb_cols) a = ldg_f4(p.x + (size_t)col * K + warp * 256 + 16 * (s0 + s) + 4 * i4);
         v[s][0] = a.x; v[s][1] = a.y; v[s][2] = a.z; v[s][3] = a.w;
     }
-    uint32_t mb = 0;
+    float m = 0.f;
 #pragma unroll
-    for (int s = 0; s < 16; ++s)
+    for (int s = 0; s < 8; ++s)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mb = max(mb, __float_as_uint(v[s][j]) & 0x7fffffffu);
-    // the column's eight lanes (4 position groups x hi/lo copies) cover its 256 values
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(v[s][j]));
+    // NaN never wins fmaxf; a NaN anywhere still reaches y through the products
+    uint32_t mb = __float_as_uint(m);
+    // the column's eight lanes (4 position groups x the two halves of its steps)
     mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
     mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
     mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
     const int e = tc_scale_exponent(mb);
     const float mult = __uint_as_float((uint32_t)(127 + e) << 23);
     const float und = __uint_as_float((uint32_t)(127 - e) << 23);
-    float xs[8];
+    float xs[4] = {0.f, 0.f, 0.f, 0.f};          // sums over this lane's part of sub-blocks s0/2 .. s0/2+3
+    uint32_t own[8][2], other[8][2];             // this lane's half / the partner's half of the loaded steps
 #pragma unroll
-    for (int j = 0; j < 8; ++j) xs[j] = 0.f;
+    for (int s = 0; s < 8; ++s) {
+        float sx[4];
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        uint32_t hv[4];
-        float ps = 0.f;
+        for (int j = 0; j < 4; ++j) sx[j] = v[s][j] * mult;
+        if (XSUMS) xs[s >> 1] += (sx[0] + sx[1]) + (sx[2] + sx[3]);
+        // positions (0, 2) and (1, 3) as fp16 pairs: hi parts, then the rest
+        const __half2 h02 = __floats2half2_rn(sx[0], sx[2]), h13 = __floats2half2_rn(sx[1], sx[3]);
+        const float2 f02 = __half22float2(h02), f13 = __half22float2(h13);
+        const __half2 l02 = __floats2half2_rn(sx[0] - f02.x, sx[2] - f02.y);
+        const __half2 l13 = __floats2half2_rn(sx[1] - f13.x, sx[3] - f13.y);
+        const uint32_t hb0 = *reinterpret_cast<const uint32_t *>(&h02), hb1 = *reinterpret_cast<const uint32_t *>(&h13);
+        const uint32_t lb0 = *reinterpret_cast<const uint32_t *>(&l02), lb1 = *reinterpret_cast<const uint32_t *>(&l13);
+        own[s][0] = lo_part ? lb0 : hb0;
+        own[s][1] = lo_part ? lb1 : hb1;
+        other[s][0] = lo_part ? hb0 : lb0;
+        other[s][1] = lo_part ? hb1 : lb1;
+    }
+    // the partner (lane ^ 4) loaded the other eight steps: swap
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float sx = v[s][j] * mult;
-            ps += sx;
-            const __half hi = __float2half_rn(sx);
-            const __half part = lo_part ? __float2half_rn(sx - __half2float(hi)) : hi;
-            hv[j] = __half_as_ushort(part);
-        }
-        if (XSUMS) xs[s >> 1] += ps;             // sub-block s/2 = steps 2j, 2j+1
-        xb[s][0] = hv[0] | (hv[2] << 16);
-        xb[s][1] = hv[1] | (hv[3] << 16);
+    for (int s = 0; s < 8; ++s) {
+        const uint32_t r0 = __shfl_xor_sync(0xffffffffu, other[s][0], 4);
+        const uint32_t r1 = __shfl_xor_sync(0xffffffffu, other[s][1], 4);
+        // (register indices must be static: select instead of indexing by s0)
+        xb[s][0] = lo_part ? r0 : own[s][0];
+        xb[s][1] = lo_part ? r1 : own[s][1];
+        xb[8 + s][0] = lo_part ? own[s][0] : r0;
+        xb[8 + s][1] = lo_part ? own[s][1] : r1;
     }
     if (XSUMS) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
             xs[j] += __shfl_xor_sync(0xffffffffu, xs[j], 1);
             xs[j] += __shfl_xor_sync(0xffffffffu, xs[j], 2);
         }
-        // |x'| < 2^10, so a sum of 32 fits fp16's range
-        const float xa = (i4 >> 1) ? ((i4 & 1) ? xs[6] : xs[4]) : ((i4 & 1) ? xs[2] : xs[0]);
-        const float xc = (i4 >> 1) ? ((i4 & 1) ? xs[7] : xs[5]) : ((i4 & 1) ? xs[3] : xs[1]);
-        const __half ha = __float2half_rn(xa), hc = __float2half_rn(xc);
-        const __half pa = lo_part ? __float2half_rn(xa - __half2float(ha)) : ha;
-        const __half pc = lo_part ? __float2half_rn(xc - __half2float(hc)) : hc;
-        xsb = (uint32_t)__half_as_ushort(pa) | ((uint32_t)__half_as_ushort(pc) << 16);
+        // sub-blocks 2i, 2i+1: on the hi lane (sub-blocks 0-3) for i < 2, the
+        // lo lane (4-7) for i >= 2; |x'| < 2^10, so a sum of 32 fits fp16
+        const int jj = 2 * (i4 & 1);
+        const float a0 = jj ? xs[2] : xs[0], a1 = jj ? xs[3] : xs[1];
+        const int src = 4 * ((g & ~1) + (i4 >> 1)) + i4;
+        const float xa = __shfl_sync(0xffffffffu, a0, src), xc = __shfl_sync(0xffffffffu, a1, src);
+        const __half2 hp = __floats2half2_rn(xa, xc);
+        const float2 fp = __half22float2(hp);
+        const __half2 lp = __floats2half2_rn(xa - fp.x, xc - fp.y);
+        xsb = lo_part ? *reinterpret_cast<const uint32_t *>(&lp) : *reinterpret_cast<const uint32_t *>(&hp);
     }
     // the C columns of this thread are 2i (hi) and 2i+1 (lo): x column 4t + i
     undo = __shfl_sync(0xffffffffu, und, 8 * i4);
@@ -2568,6 +2590,8 @@ __global__ void __launch_bounds__(block_threads<NT>(), 1) gemv_rows_mma(Params p
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fill(u + NS);
         }
+        // warps 0-1 add the 16 warps' parts in warp order while the others go
+        // on with the next stage
         if (threadIdx.x < per_stage * NB) {
             const int row = threadIdx.x / NB, col = threadIdx.x % NB;
             const float *rr = red + (size_t)(u & 1) * CWARPS * RS * NB + row * NB + col;
