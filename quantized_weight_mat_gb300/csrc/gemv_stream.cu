@@ -95,6 +95,10 @@ int plan_stages(int64_t k, int nb_cols) {
 //     g4..g7: the same for xl
 //   meta of slice s at byte s*16: {XS_2c, XS_2c+1, u, 0}, XS_j = sum of 254*xh+xl.
 // Consecutive lanes read consecutive 16-byte groups: no bank conflicts.
+// PERM (the whole-row kernel, whose lane 2j+h reads slices 4j+2h and
+// 4j+2h+1): slice s is stored at position (s & 1)*S/2 + s/2 instead, so that
+// each of the lane's two reads is again consecutive across lanes.
+template <bool PERM = false>
 __device__ __forceinline__ void prep_x_vals(const float (&v)[8], uint8_t *img, uint8_t *meta,
                                             int q, int S, int lane) {
     // block maximum of |x|: the bit patterns of non-negative floats order like
@@ -135,7 +139,7 @@ __device__ __forceinline__ void prep_x_vals(const float (&v)[8], uint8_t *img, u
     xs += __shfl_xor_sync(0xffffffffu, xs, 1);
     xs += __shfl_xor_sync(0xffffffffu, xs, 2);
     const int j = lane >> 2, c = j >> 1, half = j & 1;
-    const int slice = 4 * q + c;
+    const int slice = PERM ? (c & 1) * (S >> 1) + 2 * q + (c >> 1) : 4 * q + c;
     const int g = 2 * half + ((lane & 3) >> 1);
     const int off8 = 8 * (lane & 1);
     *reinterpret_cast<uint2 *>(img + (g * S + slice) * 16 + off8) = make_uint2(h0, h1);
@@ -156,7 +160,7 @@ __device__ __forceinline__ void prep_x_block(const float *xb, uint8_t *img, uint
 // up to eight blocks are in flight before any of them is converted.  x is
 // read from global memory, or (FROM_SMEM) from a shared-memory copy; a null
 // xb stands for a column of zeros.
-template <bool FROM_SMEM = false>
+template <bool FROM_SMEM = false, bool PERM = false>
 __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_t *meta, int nb,
                                            int S, int first, int step, int lane) {
     for (int q0 = first; q0 < nb; q0 += 8 * step) {
@@ -178,7 +182,7 @@ __device__ __forceinline__ void prep_x_all(const float *xb, uint8_t *img, uint8_
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
             const int q = q0 + r * step;
-            if (q < nb) prep_x_vals(v[r], img, meta, q, S, lane);
+            if (q < nb) prep_x_vals<PERM>(v[r], img, meta, q, S, lane);
         }
     }
 }
@@ -409,20 +413,23 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 // per launch 8.15 -> 7.12 us (window 2; 7.4 us with 3, 7.9 us with 4).  The
 // producer polls the consumers' signal with mbarrier.test_wait: try_wait may
 // suspend the thread, which delayed the first weight copies.
-#ifndef PQ_ROWS_CW
-#define PQ_ROWS_CW 8
-#endif
+//
+// Consumer warps per CTA are a property of the format (kWarps): 12 where a
+// 24-row stage still leaves at least three ring slots and the decode is
+// heavy enough for the extra warps to pay (Q4_K, Q3_K, Q2_K: decode-layer
+// set 29.8 -> 29.0 us, 4096x14336 8.4 -> 8.2 us), 8 where 24-row stages
+// would leave two slots (Q6_K 14336x4096: 9.7 us with 8 warps, 11.2 with 12).
 #ifndef PQ_ROWS_MINB
 #define PQ_ROWS_MINB 1
 #endif
 namespace rowk {
-constexpr int CW = PQ_ROWS_CW;               // consumer warps
 constexpr int MINB = PQ_ROWS_MINB;           // CTAs per SM the kernel is sized for
 constexpr int kRowsSmem = MINB == 1 ? kSmemBudget : (228 * 1024) / MINB - 1024;
 constexpr int KW = 16;                       // super-blocks per warp segment
 constexpr int RPG = 2;                       // rows per row group per stage
-constexpr int THREADS = (CW + 1) * 32;
 constexpr int MAX_STAGES = 8;
+// consumer warps + the producer warp
+template <int CW> constexpr int threads_for() { return (CW + 1) * 32; }
 constexpr int kStatic = 512;                 // reserve for the kernel's static shared memory (barriers)
 #ifndef PQ_X_WINDOW
 #define PQ_X_WINDOW 2
@@ -463,7 +470,7 @@ inline int bias_bytes(const Params &p, bool bias) { return bias ? (p.rows_cap * 
 // 16 bytes for the bulk copy).
 // With `swiglu` the CTA's items are (gate, up) row pairs: a stage holds NG
 // gate rows, then the NG up rows of the same pairs, and n_out is 2 * pairs.
-inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, Params &p, bool swiglu = false,
+inline bool plan(int64_t k, int64_t n_out, int grid, int block_bytes, int CW, Params &p, bool swiglu = false,
                  bool row_scaled = false, bool bias = false) {
     if (k % 256 || grid < 1 || ((k / 256) * block_bytes) % 16) return false;
     const int G = segments(k);
@@ -501,15 +508,15 @@ __device__ __forceinline__ int byte_of(uint32_t v, int i) {
 // byte i of v as a signed value
 __device__ __forceinline__ int sbyte_of(uint32_t v, int i) { return (int)(int8_t)(v >> (8 * i)); }
 
-// The lane's 64 x limb words from the x image: chunks 2h, 2h+1 of super-block
-// kbc (slices 4kbc+2h, 4kbc+2h+1).  part[0..3] = the four runs of 32
-// positions, in order; meta gives the 32-position sums and the scale u.
+// The lane's 64 x limb words from the x image (PERM layout): chunks 2h, 2h+1
+// of super-block kbc (slices 4kbc+2h, 4kbc+2h+1).  part[0..3] = the four runs
+// of 32 positions, in order; meta gives the 32-position sums and the scale u.
 __device__ __forceinline__ void load_x_parts(uint32_t (&xh)[4][8], uint32_t (&xl)[4][8], int (&xs32)[4],
                                              float &u, const uint8_t *ximg, const uint8_t *xmeta,
                                              int S, int kbc, int hf) {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-        const int slice = 4 * kbc + 2 * hf + cc;
+        const int slice = cc * (S >> 1) + 2 * kbc + hf;   // slice 4kbc + 2hf + cc, permuted
         uint4 g[8];
 #pragma unroll
         for (int gi2 = 0; gi2 < 8; ++gi2)
@@ -535,6 +542,7 @@ struct Q4K {
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 144;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 12;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the 4 sub-blocks (32 positions each)
         int xs[4];                     // sum of X = 254*xh + xl per sub-block
@@ -596,6 +604,7 @@ struct Q6K {
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 210;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 8;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-position parts t = 0..3
         int xs[8];                     // sum of X over the 8 sub-blocks of 16
@@ -691,6 +700,7 @@ struct Q80 {
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 272;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 8;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-weight blocks
         float u;
@@ -742,6 +752,7 @@ struct Q80 {
 struct I8R {
     static constexpr int kBlockBytes = 256;
     static constexpr bool kRowScaled = true;
+    static constexpr int kWarps = 8;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i8row_scale_offset(n_out, k); }
     struct X {
         uint32_t xh[8][4], xl[8][4];   // limbs of chunk (c + lane) mod 8, 16 positions each
@@ -797,6 +808,7 @@ struct Q5K {
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     static constexpr int kBlockBytes = 176;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 8;
     struct X {
         uint32_t xh[4][8], xl[4][8];
         int xs[4];
@@ -862,6 +874,7 @@ struct Q5K {
 struct I4R {
     static constexpr int kBlockBytes = 128;
     static constexpr bool kRowScaled = true;
+    static constexpr int kWarps = 8;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i4row_scale_offset(n_out, k); }
     struct X {
         uint32_t eh[4][4], el[4][4], oh[4][4], ol[4][4];   // chunk (c + lane/2) mod 4: even / odd limbs
@@ -925,6 +938,7 @@ struct I4R {
 struct Q2K {
     static constexpr int kBlockBytes = 84;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 12;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -991,6 +1005,7 @@ struct Q2K {
 struct Q3K {
     static constexpr int kBlockBytes = 110;
     static constexpr bool kRowScaled = false;
+    static constexpr int kWarps = 12;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -1104,7 +1119,8 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // in one step measured 3 us per step slower (instruction fetch); one
 // run-time instance for everything 0.4 us slower on the plain step.
 template <class F, bool RT>
-__global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
+__global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Params p) {
+    constexpr int CW = F::kWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
     __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
@@ -1199,7 +1215,7 @@ __global__ void __launch_bounds__(THREADS, MINB) gemv_rows(Params p) {
             if (F::kRowScaled && SW) v1 = __ldg(p.rscale + p.n_ff + r0 + i0v);
         }
     }
-    prep_x_all(p.x, ximg, xmeta, nb, S, warp, CW, lane);
+    prep_x_all<false, true>(p.x, ximg, xmeta, nb, S, warp, CW, lane);
     if (kVec) {
         float *dst = F::kRowScaled ? rsc : bsm;
         if (i0v < nrows) {
@@ -1338,7 +1354,7 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
                    cudaStream_t s, int early_w, const float *bias, int epi_kind) {
     const float *rscale = F::kRowScaled ? reinterpret_cast<const float *>(w + F::scale_offset(n_out, k)) : nullptr;
     Params p{w, x, y, (int)n_out, (int)k, 0, 0, 0, 0, 0, early_w, (int)(n_out / 2), bias, rscale, epi_kind};
-    if (!plan(k, n_out, grid, F::kBlockBytes, p, epi_kind == kEpiSwiGLU, F::kRowScaled, epi_kind == kEpiBias))
+    if (!plan(k, n_out, grid, F::kBlockBytes, F::kWarps, p, epi_kind == kEpiSwiGLU, F::kRowScaled, epi_kind == kEpiBias))
         return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * F::kBlockBytes + x_image_bytes(k, 1) + red_bytes(p) +
                      rsc_bytes(p, F::kRowScaled, epi_kind == kEpiSwiGLU) + bias_bytes(p, epi_kind == kEpiBias);
@@ -1354,7 +1370,7 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, f
     if (ce != cudaSuccess) return ce;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(threads_for<F::kWarps>());
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1380,14 +1396,14 @@ inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
     const int64_t items = swiglu ? n_out / 2 : n_out;
     const int grid = (int)(items < grid_est ? items : grid_est);
     if (swiglu && (n_out % 2 || items < 1)) return false;
-    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, p, swiglu);
-    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, p, swiglu);
-    if (fmt == PQ_Q8_0) return k % 256 == 0 && plan(k, n_out, grid, Q80::kBlockBytes, p, swiglu);
-    if (fmt == PQ_I8_ROW) return k % 256 == 0 && plan(k, n_out, grid, I8R::kBlockBytes, p, swiglu, true);
-    if (fmt == PQ_Q5_K) return plan(k, n_out, grid, Q5K::kBlockBytes, p, swiglu);
-    if (fmt == PQ_I4_ROW) return k % 256 == 0 && plan(k, n_out, grid, I4R::kBlockBytes, p, swiglu, true);
-    if (fmt == PQ_Q2_K) return plan(k, n_out, grid, Q2K::kBlockBytes, p, swiglu);
-    if (fmt == PQ_Q3_K) return plan(k, n_out, grid, Q3K::kBlockBytes, p, swiglu);
+    if (fmt == PQ_Q4_K) return plan(k, n_out, grid, Q4K::kBlockBytes, Q4K::kWarps, p, swiglu);
+    if (fmt == PQ_Q6_K) return plan(k, n_out, grid, Q6K::kBlockBytes, Q6K::kWarps, p, swiglu);
+    if (fmt == PQ_Q8_0) return k % 256 == 0 && plan(k, n_out, grid, Q80::kBlockBytes, Q80::kWarps, p, swiglu);
+    if (fmt == PQ_I8_ROW) return k % 256 == 0 && plan(k, n_out, grid, I8R::kBlockBytes, I8R::kWarps, p, swiglu, true);
+    if (fmt == PQ_Q5_K) return plan(k, n_out, grid, Q5K::kBlockBytes, Q5K::kWarps, p, swiglu);
+    if (fmt == PQ_I4_ROW) return k % 256 == 0 && plan(k, n_out, grid, I4R::kBlockBytes, I4R::kWarps, p, swiglu, true);
+    if (fmt == PQ_Q2_K) return plan(k, n_out, grid, Q2K::kBlockBytes, Q2K::kWarps, p, swiglu);
+    if (fmt == PQ_Q3_K) return plan(k, n_out, grid, Q3K::kBlockBytes, Q3K::kWarps, p, swiglu);
     return false;
 }
 }  // namespace rowk
