@@ -406,13 +406,28 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 // load of x issued behind the whole ring's worth of weight copies would wait
 // for all of them (several microseconds at this SM's share of the HBM
 // bandwidth).  Until the consumers have converted x, the producer therefore
-// keeps at most kXWindow stages in flight (issued, not landed); after that
+// keeps at most a window of stages in flight (issued, not landed); after that
 // only the ring depth limits it.  Measured per-CTA timelines (%globaltimer)
 // of 14336x4096 launched back to back: x ready 2.8 us after the wait returned
-// with the whole ring in flight ahead of it, about 1.2 us with this limit;
-// per launch 8.15 -> 7.12 us (window 2; 7.4 us with 3, 7.9 us with 4).  The
+// with the whole ring in flight ahead of it, about 1.2 us with a window of
+// two stages; per launch 8.15 -> 7.12 us (7.4 us with 3, 7.9 us with 4).  The
 // producer polls the consumers' signal with mbarrier.test_wait: try_wait may
 // suspend the thread, which delayed the first weight copies.
+//
+// The ring (three to five stages) cannot hold a CTA's rows, and between the
+// release and the first dot product (release latency, x conversion, the x
+// limbs loaded into registers: about 2.4 us) HBM would idle once the window
+// has landed.  So, for rows of one warp segment (k <= 4096), the producer
+// also asks L2 to prefetch the CTA's next kL2PrefetchBytes of rows
+// (cp.async.bulk.prefetch.L2) right after issuing the window: HBM keeps
+// streaming into L2 through that time, no shared memory is held, and no data
+// comes back to the SM ahead of x; the later stage copies then hit L2.  With
+// the prefetch a window of one stage is best unless the CTA has many stages
+// (kWideWindowUnits).  Q4_K, launched back to back: 14336x4096 7.01 -> 6.73
+// us, 28672x4096 11.14 -> 10.07 us, decode-layer set 29.0 -> 28.1 us.
+// Prefetching for longer rows as well made the set slower (28.7 us).  A
+// format opts out with kL2Prefetch = false (per-row int4: 14336x4096 6.9 ->
+// 7.4 us with the prefetch, whatever the window).
 //
 // Consumer warps per CTA are a property of the format (kWarps): 12 where a
 // 24-row stage still leaves at least three ring slots and the decode is
@@ -435,6 +450,8 @@ constexpr int kStatic = 512;                 // reserve for the kernel's static 
 #define PQ_X_WINDOW 2
 #endif
 constexpr int kXWindow = PQ_X_WINDOW;        // stages in flight at most until x is converted
+constexpr int kWideWindowUnits = 8;          // ... for CTAs with at least this many stages; one stage below
+constexpr uint32_t kL2PrefetchBytes = 128 * 1024;   // rows prefetched into L2 after the window (one segment)
 
 struct Params {
     const uint8_t *w;
@@ -543,6 +560,7 @@ struct Q4K {
     static constexpr int kBlockBytes = 144;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
+    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the 4 sub-blocks (32 positions each)
         int xs[4];                     // sum of X = 254*xh + xl per sub-block
@@ -605,6 +623,7 @@ struct Q6K {
     static constexpr int kBlockBytes = 210;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
+    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-position parts t = 0..3
         int xs[8];                     // sum of X over the 8 sub-blocks of 16
@@ -701,6 +720,7 @@ struct Q80 {
     static constexpr int kBlockBytes = 272;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
+    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-weight blocks
         float u;
@@ -753,6 +773,7 @@ struct I8R {
     static constexpr int kBlockBytes = 256;
     static constexpr bool kRowScaled = true;
     static constexpr int kWarps = 8;
+    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i8row_scale_offset(n_out, k); }
     struct X {
         uint32_t xh[8][4], xl[8][4];   // limbs of chunk (c + lane) mod 8, 16 positions each
@@ -809,6 +830,7 @@ struct Q5K {
     static constexpr int kBlockBytes = 176;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
+    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];
         int xs[4];
@@ -875,6 +897,7 @@ struct I4R {
     static constexpr int kBlockBytes = 128;
     static constexpr bool kRowScaled = true;
     static constexpr int kWarps = 8;
+    static constexpr bool kL2Prefetch = false;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i4row_scale_offset(n_out, k); }
     struct X {
         uint32_t eh[4][4], el[4][4], oh[4][4], ol[4][4];   // chunk (c + lane/2) mod 4: even / odd limbs
@@ -939,6 +962,7 @@ struct Q2K {
     static constexpr int kBlockBytes = 84;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
+    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -1006,6 +1030,7 @@ struct Q3K {
     static constexpr int kBlockBytes = 110;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
+    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -1164,7 +1189,8 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
             if (!p.early_w) grid_dep_wait();   // the weights may be the previous kernel's output
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
-            const int window = kXWindow < NS ? kXWindow : NS;
+            const int wsel = (!F::kL2Prefetch || units >= kWideWindowUnits) ? kXWindow : 1;
+            const int window = wsel < NS ? wsel : NS;
             bool x_in = false;         // the consumers have converted x
             int landed = 0, lslot = 0; // stages known to have landed; slot of the next one
             uint32_t lph = 0;
@@ -1195,6 +1221,13 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
                     bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
                 }
                 src += (size_t)IPS * rowbytes;
+                if (F::kL2Prefetch && G == 1 && u + 1 == window && u + 1 < units) {
+                    // the rows after the window (a multiple of 16 bytes: rows are)
+                    uint64_t pfb = (uint64_t)(nrows - (u + 1) * IPS) * rowbytes;
+                    if (pfb > kL2PrefetchBytes) pfb = kL2PrefetchBytes;
+                    bulk_prefetch_l2(src, (uint32_t)pfb);
+                    if (SW) bulk_prefetch_l2(src + (size_t)p.n_ff * rowbytes, (uint32_t)pfb);
+                }
                 if (++slot == NS) { slot = 0; ph ^= 1u; }
             }
         }
