@@ -998,8 +998,9 @@ struct Q2K {
             int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t c0 = (q[i] >> (2 * t)) & 0x03030303u;
-                const uint32_t c1 = (q[4 + i] >> (2 * t)) & 0x03030303u;
+                // the codes of part t in place, i.e. 4^t times their value
+                const uint32_t c0 = q[i] & (0x03030303u << (2 * t));
+                const uint32_t c1 = q[4 + i] & (0x03030303u << (2 * t));
                 dh0 = dp4a_us(c0, R.xh[t][i], dh0);
                 dl0 = dp4a_us(c0, R.xl[t][i], dl0);
                 dh1 = dp4a_us(c1, R.xh[t][4 + i], dh1);
@@ -1007,12 +1008,13 @@ struct Q2K {
             }
             const uint32_t sw = t < 2 ? s0 : s1;
             const int g0 = byte_of(sw, 2 * (t & 1)), g1 = byte_of(sw, 2 * (t & 1) + 1);
-            H += (g0 & 15) * dh0 + (g1 & 15) * dh1;
-            L += (g0 & 15) * dl0 + (g1 & 15) * dl1;
+            // times 4^(3-t): every part of H and L then carries 64 (|H|, |L| < 2^26)
+            H += ((g0 & 15) * dh0 + (g1 & 15) * dh1) << (6 - 2 * t);
+            L += ((g0 & 15) * dl0 + (g1 & 15) * dl1) << (6 - 2 * t);
             M += (g0 >> 4) * R.xs[2 * t] + (g1 >> 4) * R.xs[2 * t + 1];
         }
         const float d = h2f(dd), dmin = h2f(dd >> 16);
-        return R.u * (d * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
+        return R.u * (d * (1.0f / 64.0f) * fmaf(254.0f, (float)H, (float)L) - dmin * (float)M);
     }
 };
 
