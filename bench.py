@@ -57,6 +57,9 @@ NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 # that code makes the figure stale (reported as null).
 NCU_TRAFFIC = {"f3c237399babbd6c": 66_157_568, "e7a438cff78acc04": 66_132_736, "50834bf8c36ec992": 66_137_344,
                "265e2c4bb8164730": 66_135_296}
+# The same launch under ncu, cold and alone (gpu__time_duration.sum in us,
+# dram__throughput.avg.pct_of_peak_sustained_elapsed), from the same capture.
+NCU_ISOLATED = {"265e2c4bb8164730": {"us": 16.864, "dram_throughput_pct": 49.58}}
 
 
 def set_bytes():
@@ -493,6 +496,7 @@ def run_ours(args):
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else float("nan")
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(src_hash)
+    ncu_isolated = NCU_ISOLATED.get(src_hash)
     result = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -538,7 +542,10 @@ def run_ours(args):
                      "traffic": traffic, "algorithmic_bytes": dom_bytes,
                      "method": f"dominant GEMV alone, {args.dominant_launches} launches back to back "
                                f"in one CUDA graph, weights of {L} layers rotating, CUDA events",
-                     "kernel_source": src_hash},
+                     "kernel_source": src_hash,
+                     "ncu_isolated": None if ncu_isolated is None else dict(
+                         ncu_isolated, frac=round(dom_bytes / (ncu_isolated["us"] * 1e-6) / 1e9 / peak, 4),
+                         method="the same launch under ncu, cold and alone (no neighbour to overlap)")},
         "clocks": clocks.summary(),
     }
     if configs is not None:
