@@ -1097,8 +1097,12 @@ struct Q3K {
             int dh0 = 0, dl0 = 0, dh1 = 0, dl1 = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t c0 = ((q[i] >> (2 * t)) & 0x03030303u) | (((hm[i] >> t) & 0x01010101u) << 2);
-                const uint32_t c1 = ((q[4 + i] >> (2 * t)) & 0x03030303u) | (((hm[4 + i] >> t) & 0x01010101u) << 2);
+                // parts 0-2: the 3-bit codes assembled in place (4^t times their
+                // value, at most 112); part 3 shifted down (7 * 64 is no byte)
+                const uint32_t c0 = t < 3 ? (q[i] & (0x03030303u << (2 * t))) | ((hm[i] << (t + 2)) & (0x04040404u << (2 * t)))
+                                          : ((q[i] >> 6) & 0x03030303u) | (((hm[i] >> 3) & 0x01010101u) << 2);
+                const uint32_t c1 = t < 3 ? (q[4 + i] & (0x03030303u << (2 * t))) | ((hm[4 + i] << (t + 2)) & (0x04040404u << (2 * t)))
+                                          : ((q[4 + i] >> 6) & 0x03030303u) | (((hm[4 + i] >> 3) & 0x01010101u) << 2);
                 dh0 = dp4a_us(c0, R.xh[t][i], dh0);
                 dl0 = dp4a_us(c0, R.xl[t][i], dl0);
                 dh1 = dp4a_us(c1, R.xh[t][4 + i], dh1);
@@ -1110,13 +1114,15 @@ struct Q3K {
                 const int lo4 = byte_of(g < 4 ? lo : lo2, g & 3);
                 const int hi2 = (byte_of(hi, g & 3) >> (2 * (g >> 2))) & 3;
                 const int scg = (lo4 | (hi2 << 4)) - 32;
-                H += scg * (e ? dh1 : dh0);
-                L += scg * (e ? dl1 : dl0);
+                // every part of H and L carries 64 (|H|, |L| < 2^28)
+                const int sh = t < 3 ? 6 - 2 * t : 6;
+                H += (scg * (e ? dh1 : dh0)) << sh;
+                L += (scg * (e ? dl1 : dl0)) << sh;
                 M += scg * R.xs[g];
             }
         }
         // sum of value * X = sum of (value + 4) * X - 4 * sum of X, per group
-        return R.u * h2f(dw) * (fmaf(254.0f, (float)H, (float)L) - 4.0f * (float)M);
+        return R.u * h2f(dw) * (fmaf(254.0f, (float)H, (float)L) * (1.0f / 64.0f) - 4.0f * (float)M);
     }
 };
 
