@@ -58,7 +58,7 @@ def test_dequant_bit_exact(fmt, n_out, k, kind):
 
 GEMV_SHAPES = {
     "q8_0": [(1, 32), (7, 96), (129, 896), (300, 4096), (1000, 768)],
-    "q4_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (37, 14336)],
+    "q4_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (37, 14336), (1000, 8192), (333, 6144)],
     "q6_k": [(1, 256), (7, 768), (129, 4096), (300, 2048), (9, 14336), (1000, 4096), (2001, 2048)],
     "i8_row": [(1, 1), (7, 13), (129, 100), (300, 4096), (33, 2048), (1000, 768)],
     "q5_k": [(1, 256), (7, 768), (129, 4096), (9, 14336), (1000, 4096)],
