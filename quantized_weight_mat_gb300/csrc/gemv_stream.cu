@@ -1471,6 +1471,15 @@ inline bool takes(int fmt, int64_t k, int64_t n_out, bool swiglu = false) {
 // prep_x_nb only before its x copy.
 namespace rowsnb {
 constexpr int CW = 15;                       // consumer warps (with the producer: 512 threads, 128 registers)
+// Rows up to kNbConvertMaxK long: the consumer warps convert x themselves
+// after the dependency wait (the producer keeps kNbXWindow stages in flight
+// until they have), so a call is one launch with no scratch; longer rows
+// take the x image from prep_x_nb, which converts it once for all CTAs.
+// Batch 2, Q4_K, launched back to back: 4096x14336 13.9 -> 13.0 us,
+// 4096x8192 10.4 -> 8.7 us; at 8192x28672 (224 blocks of x per CTA) the
+// prep kernel is faster, 30.3 against 32.0 us.
+constexpr int64_t kNbConvertMaxK = 16384;
+constexpr int kNbXWindow = 2;
 constexpr int THREADS = (CW + 1) * 32;
 constexpr int MAX_STAGES = 8;
 constexpr int kStatic = 512;
@@ -1488,7 +1497,8 @@ inline __host__ __device__ int col_bytes(int64_t k) { return (int)(2 * k + (k / 
 
 struct Params {
     const uint8_t *w;
-    const uint8_t *x_img;   // NB columns of col_bytes(k), from prep_x_nb
+    const uint8_t *x_img;   // NB columns of col_bytes(k), from prep_x_nb; null: x is converted in the kernel
+    const float *x;         // with a null x_img: NB columns of k values (nb_cols real)
     float *y;
     long long ldy;
     int n_out;
@@ -1605,17 +1615,27 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_nb(Params p) {
     if (warp == CW) {
         // ---------------- producer: one contiguous copy per stage ----------------
         if (lane == 0) {
-            // the first ring's worth of weights, then (after prep_x_nb) the x image
-            const int early = units < NS ? units : NS;
+            // with the x image from prep_x_nb: the first ring's worth of weights
+            // (the preceding kernel is prep_x_nb, which waited for the caller's
+            // kernel), then the image; with x converted here: a window of
+            // kNbXWindow stages, then the rest once the consumers have converted x
+            const bool img = p.x_img != nullptr;
+            if (!img && !p.early_w) rowk::grid_dep_wait();   // the weights may be the previous kernel's output
+            const int cap = img ? NS : (kNbXWindow < NS ? kNbXWindow : NS);
+            const int early = units < cap ? units : cap;
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
             int slot = 0;
             uint32_t ph = 0;
             for (int u = 0; u <= units; ++u) {
                 if (u == early) {
-                    rowk::grid_dep_wait();
-                    mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
-                    bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                    if (img) {
+                        rowk::grid_dep_wait();
+                        mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
+                        bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                    } else if (u < units && !mbar_wait(&x_bar, 0)) {
+                        break;
+                    }
                 }
                 if (u == units) break;
                 const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
@@ -1630,9 +1650,21 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_nb(Params p) {
         return;
     }
 
-    if (warp >= CA) return;
     bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
-    if (!mbar_wait(&x_bar, 0)) dead = true;
+    if (p.x_img) {
+        if (warp >= CA) return;
+        if (!mbar_wait(&x_bar, 0)) dead = true;
+    } else {
+        // x of the NB columns to limbs in shared memory, by every consumer warp
+        rowk::grid_dep_wait();                   // x may be the previous kernel's output
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            prep_x_all(b < p.nb_cols ? p.x + (size_t)b * p.k : nullptr, ximg + (size_t)b * CB,
+                       ximg + (size_t)b * CB + 2 * p.k, nb, S, warp, CW, lane);
+        named_sync(1, CW * 32);
+        if (threadIdx.x == 0) mbar_arrive(&x_bar);   // the producer may stream past its window
+        if (warp >= CA) return;
+    }
 
     const int gi = warp / G, seg = warp - gi * G;
     const int part = lane % Gm::LPB;
@@ -1813,7 +1845,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_rows_nb(Params p) {
 template <int NB>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int nb_cols, float *y, int64_t ldy,
                    int grid, cudaStream_t s) {
-    Params p{w, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
+    Params p{w, nullptr, x, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, weight_prefetch()};
     if (!plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * 144 + NB * col_bytes(k) + red_bytes<NB>(p);
     static PerDeviceOnce configured;
@@ -1826,15 +1858,27 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, i
                                     kSmemBudget - kStatic);
     });
     if (ce != cudaSuccess) return ce;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (k <= kNbConvertMaxK) {
+        // x converted by the kernel itself: one launch, no scratch
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_rows_nb<NB>, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
     void *img = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&img, (size_t)NB * col_bytes(k), pool, s);
     if (e != cudaSuccess) return e;
     p.x_img = static_cast<const uint8_t *>(img);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t pcfg = {};
     pcfg.gridDim = dim3((unsigned)((k / 256 + 7) / 8), NB);
     pcfg.blockDim = dim3(256);
@@ -2160,7 +2204,7 @@ __global__ void __launch_bounds__(threads<NB>(), 1) gemv_q6_k_nb(Params p) {
 template <int NB>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int nb_cols, float *y, int64_t ldy,
                    int grid, cudaStream_t s) {
-    Params p{w, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
+    Params p{w, nullptr, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
     if (!rows6::plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * BB + NB * col_bytes(k) + rows6::red_bytes<NB>(p);
     static PerDeviceOnce configured;

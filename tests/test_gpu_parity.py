@@ -195,14 +195,15 @@ def test_workload_dequant_output_head_sampled():
         assert np.array_equal(o[r].cpu().numpy().view(np.uint32), ref.view(np.uint32)), r
 
 
-@pytest.mark.parametrize("batch", [1, 8])
+@pytest.mark.parametrize("batch", [1, 2, 8])
 @pytest.mark.parametrize("prefetch", [False, True])
 def test_chained_calls_respect_stream_order(prefetch, batch):
     # y1 = W1 x, y2 = W2 y1, y3 = W3 y2 issued back to back on one stream: each
     # call must read its predecessor's finished output, also when its kernel is
-    # scheduled while the predecessor is still running.  At batch 8 the three
-    # shapes run the tensor-core kernel with whole tiles (14336 x 4096) and
-    # split-K with the finishing kernel (4096 x 14336, 4096 x 4096).
+    # scheduled while the predecessor is still running.  At batch 2 the long
+    # rows (4096 x 14336) run the two-column kernel that converts x itself; at
+    # batch 8 the three shapes run the register-operand kernel (k = 4096) and
+    # the tensor-core item kernel with its finishing kernel (4096 x 14336).
     import torch
     shapes = [(14336, 4096), (4096, 14336), (4096, 4096)]
     ws = [weights("q4_k", n, k, "quantized", 60 + j) for j, (n, k) in enumerate(shapes)]
@@ -228,12 +229,13 @@ def test_chained_calls_respect_stream_order(prefetch, batch):
         pq.pq_set_weight_prefetch(bool(old))
 
 
-@pytest.mark.parametrize("batch", [1, 8])
-def test_weights_written_by_the_preceding_kernel(batch):
+@pytest.mark.parametrize("batch,k", [(1, 4096), (8, 4096), (2, 8192)])
+def test_weights_written_by_the_preceding_kernel(batch, k):
     # with prefetch off (the default), a kernel that writes the weight buffer
-    # right before pq_gemv must be fully visible to it (batch 8: tensor core)
+    # right before pq_gemv must be fully visible to it (batch 8: the
+    # register-operand kernel; batch 2 at k = 8192: the two-column kernel)
     import torch
-    n, k = 2048, 4096
+    n = 2048
     wa, wb = weights("q4_k", n, k, "random", 70), weights("q4_k", n, k, "random", 71)
     da, db = dev(wa), dev(wb)
     mask = torch.bitwise_xor(da, db)
