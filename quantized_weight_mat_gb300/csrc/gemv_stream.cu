@@ -2007,17 +2007,26 @@ __global__ void __launch_bounds__(threads<NB>(), 1) gemv_q6_k_nb(Params p) {
     if (warp == CW) {
         // ---------------- producer: one contiguous copy per stage ----------------
         if (lane == 0) {
-            // the first ring's worth of weights, then (after prep_x_nb) the x image
-            const int early = units < NS ? units : NS;
+            // as in rowsnb::gemv_rows_nb: with the x image from prep_x_nb, the
+            // first ring's worth of weights, then the image; with x converted
+            // here, a window of stages until the consumers have converted it
+            const bool img = p.x_img != nullptr;
+            if (!img && !p.early_w) rowk::grid_dep_wait();   // the weights may be the previous kernel's output
+            const int cap = img ? NS : (rowsnb::kNbXWindow < NS ? rowsnb::kNbXWindow : NS);
+            const int early = units < cap ? units : cap;
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
             int slot = 0;
             uint32_t ph = 0;
             for (int u = 0; u <= units; ++u) {
                 if (u == early) {
-                    rowk::grid_dep_wait();
-                    mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
-                    bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                    if (img) {
+                        rowk::grid_dep_wait();
+                        mbar_arrive_expect_tx(&x_bar, (uint32_t)(NB * CB));
+                        bulk_g2s(ximg, p.x_img, (uint32_t)(NB * CB), &x_bar);
+                    } else if (u < units && !mbar_wait(&x_bar, 0)) {
+                        break;
+                    }
                 }
                 if (u == units) break;
                 const int rows = nrows - u * RS < RS ? nrows - u * RS : RS;
@@ -2032,9 +2041,20 @@ __global__ void __launch_bounds__(threads<NB>(), 1) gemv_q6_k_nb(Params p) {
         return;
     }
 
-    if (warp >= CA) return;
     bool dead = false;   // a wait ran out: stop waiting, keep going so every warp finishes
-    if (!mbar_wait(&x_bar, 0)) dead = true;
+    if (p.x_img) {
+        if (warp >= CA) return;
+        if (!mbar_wait(&x_bar, 0)) dead = true;
+    } else {
+        rowk::grid_dep_wait();                   // x may be the previous kernel's output
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            prep_x_all(b < p.nb_cols ? p.x + (size_t)b * p.k : nullptr, ximg + (size_t)b * CB,
+                       ximg + (size_t)b * CB + 2 * p.k, nb, S, warp, CW, lane);
+        named_sync(1, CW * 32);
+        if (threadIdx.x == 0) mbar_arrive(&x_bar);   // the producer may stream past its window
+        if (warp >= CA) return;
+    }
 
     const int gi = warp / G, seg = warp - gi * G;
     const int part = lane % LPB;
@@ -2204,7 +2224,7 @@ __global__ void __launch_bounds__(threads<NB>(), 1) gemv_q6_k_nb(Params p) {
 template <int NB>
 cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, int nb_cols, float *y, int64_t ldy,
                    int grid, cudaStream_t s) {
-    Params p{w, nullptr, nullptr, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, 0};
+    Params p{w, nullptr, x, y, (long long)ldy, (int)n_out, (int)k, nb_cols, 0, 0, 0, 0, 0, weight_prefetch()};
     if (!rows6::plan<NB>(k, n_out, grid, p)) return cudaErrorInvalidValue;
     const int smem = p.nstages * p.RS * (int)(k / 256) * BB + NB * col_bytes(k) + rows6::red_bytes<NB>(p);
     static PerDeviceOnce configured;
@@ -2217,15 +2237,29 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, i
                                     kSmemBudget - kStatic);
     });
     if (ce != cudaSuccess) return ce;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (NB == 2 && k <= rowsnb::kNbConvertMaxK) {
+        // x converted by the kernel itself (two columns: Q6_K head 83.5 -> 80.7
+        // us, 4096x14336 17.4 -> 16.3 us; four columns convert more slowly than
+        // prep_x_nb: 2000x4096 batch 3 9.1 -> 10.1 us, so they keep it)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads<NB>());
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_q6_k_nb<NB>, p);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     cudaMemPool_t pool = scratch_pool();
     if (!pool) return cudaErrorMemoryAllocation;
     void *img = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&img, (size_t)NB * col_bytes(k), pool, s);
     if (e != cudaSuccess) return e;
     p.x_img = static_cast<const uint8_t *>(img);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t pcfg = {};
     pcfg.gridDim = dim3((unsigned)((k / 256 + 7) / 8), NB);
     pcfg.blockDim = dim3(256);
