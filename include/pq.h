@@ -193,19 +193,21 @@ int pq_gemv_choice(pq_fmt fmt, int n_out, int k, int batch);
  * Number of batch slices one pq_gemv call with these arguments runs (slices
  * of up to 32 columns for the tensor-core kernel, up to 4 or 1 otherwise), each
  * with one kernel choice.  A slice is one launch of its kernel, plus, for the
- * tensor-core and the batch-2 long-row kernels, one small x-conversion launch
- * before it, and for the tensor-core kernel one split-K finishing launch after
- * it when CTAs share a row tile.
+ * tensor-core kernels, and for the two-column kernels at rows longer than
+ * 16384 (and the Q6_K kernel at 3-4 columns), one small x-conversion launch
+ * before it, and for the tensor-core kernels one split-K finishing launch
+ * after it when CTAs share a row tile.
  */
 int pq_gemv_launches(pq_fmt fmt, int n_out, int k, int batch);
 
 /*
  * Weight prefetch across kernel boundaries (process-wide, default off).
- * pq_gemv's batch-1 kernel is launched with programmatic dependent launch: it
- * may be scheduled while the preceding kernel on the stream is still
- * finishing, and it always waits for that kernel before reading x or writing
- * y.  With prefetch enabled it also starts streaming w_blocks before that
- * wait.  Enable it only when no kernel that runs immediately before a
+ * pq_gemv's whole-row kernels (batch 1, the register-operand kernel at batch
+ * 2-8 and the two-column kernels) are launched with programmatic dependent
+ * launch: each may be scheduled while the preceding kernel on the stream is
+ * still finishing, and always waits for that kernel before reading x or
+ * writing y.  With prefetch enabled they also start streaming w_blocks
+ * before that wait.  Enable it only when no kernel that runs immediately before a
  * pq_gemv on its stream writes that call's w_blocks (the usual case: weights
  * loaded once, then only read).  Copies (cudaMemcpy*) are always waited for.
  * Returns the previous setting.

@@ -229,6 +229,36 @@ def test_chained_calls_respect_stream_order(prefetch, batch):
         pq.pq_set_weight_prefetch(bool(old))
 
 
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_chained_q6_k_calls_at_batch_2(prefetch):
+    # the Q6_K two-column kernel converts x itself after the dependency wait
+    # (and streams weights before it when they are declared static): a chain
+    # whose every x is the previous call's y must still read finished outputs
+    import torch
+    shapes = [(4096, 2048), (2048, 4096), (1000, 2048)]
+    ws = [weights("q6_k", n, k, "quantized", 80 + j) for j, (n, k) in enumerate(shapes)]
+    wd = [dev(w) for w in ws]
+    x = x_for(2, shapes[0][1], 83)
+    ys = [torch.empty(2 * n, dtype=torch.float32, device="cuda") for n, _ in shapes]
+    old = pq.pq_set_weight_prefetch(prefetch)
+    try:
+        for rep in range(3):
+            cur = dev(x)
+            for j, (n, k) in enumerate(shapes):
+                pq.pq_gemv("q6_k", wd[j], n, k, cur, 2, ys[j])
+                cur = ys[j]
+            torch.cuda.synchronize()
+            prev = x
+            for j, (n, k) in enumerate(shapes):
+                got = ys[j].cpu().numpy().reshape(2, n)
+                ref = oracle.gemv("q6_k", ws[j], n, k, prev)
+                ok, err, bound = tolerance_ok(got, ref)
+                assert ok, (rep, j, err, bound)
+                prev = got.astype(np.float32)
+    finally:
+        pq.pq_set_weight_prefetch(bool(old))
+
+
 @pytest.mark.parametrize("batch,k", [(1, 4096), (8, 4096), (2, 8192)])
 def test_weights_written_by_the_preceding_kernel(batch, k):
     # with prefetch off (the default), a kernel that writes the weight buffer
