@@ -125,6 +125,11 @@ __device__ __forceinline__ uint64_t make_evict_first_policy() {
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Arrive on named barrier `id` without waiting (the threads that bar.sync on
+// it see this thread's earlier memory writes once it completes).
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // 4-way byte dot products, accumulated in 32-bit integers.
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
