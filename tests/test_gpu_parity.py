@@ -259,6 +259,52 @@ def test_chained_q6_k_calls_at_batch_2(prefetch):
         pq.pq_set_weight_prefetch(bool(old))
 
 
+@pytest.mark.parametrize("batch", [1, 3, 6])
+@pytest.mark.parametrize("n_out,k", [(896, 896), (129, 896), (7, 128), (1000, 1024), (33, 512)])
+def test_q8_0_short_rows_with_static_weights(n_out, k, batch):
+    # with the weights declared static, Q8_0 rows of at most 1024 run the
+    # short-row kernel (weights read before the dependency wait)
+    import torch
+    w = weights("q8_0", n_out, k, "quantized", 90 + n_out)
+    x = x_for(batch, k, 91 + batch)
+    old = pq.pq_set_weight_prefetch(True)
+    try:
+        y = torch.empty(batch * n_out, dtype=torch.float32, device="cuda")
+        pq.pq_gemv("q8_0", dev(w), n_out, k, dev(x), batch, y)
+        torch.cuda.synchronize()
+    finally:
+        pq.pq_set_weight_prefetch(bool(old))
+    ok, err, bound = tolerance_ok(y.cpu().numpy().reshape(batch, n_out), oracle.gemv("q8_0", w, n_out, k, x))
+    assert ok, (err, bound)
+
+
+def test_chained_q8_0_short_rows():
+    # each call's x is the previous call's y; the short-row kernel may be
+    # resident before its predecessor ends and must wait before reading x
+    import torch
+    n = k = 896
+    ws = [weights("q8_0", n, k, "quantized", 95 + j) for j in range(4)]
+    wd = [dev(w) for w in ws]
+    x = x_for(1, k, 99)
+    ys = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in ws]
+    old = pq.pq_set_weight_prefetch(True)
+    try:
+        for rep in range(3):
+            cur = dev(x)
+            for j in range(len(ws)):
+                pq.pq_gemv("q8_0", wd[j], n, k, cur, 1, ys[j])
+                cur = ys[j]
+            torch.cuda.synchronize()
+            prev = x
+            for j in range(len(ws)):
+                got = ys[j].cpu().numpy().reshape(1, n)
+                ok, err, bound = tolerance_ok(got, oracle.gemv("q8_0", ws[j], n, k, prev))
+                assert ok, (rep, j, err, bound)
+                prev = got.astype(np.float32)
+    finally:
+        pq.pq_set_weight_prefetch(bool(old))
+
+
 @pytest.mark.parametrize("batch,k", [(1, 4096), (8, 4096), (2, 8192)])
 def test_weights_written_by_the_preceding_kernel(batch, k):
     # with prefetch off (the default), a kernel that writes the weight buffer
