@@ -418,10 +418,14 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 // release and the first dot product (release latency, x conversion, the x
 // limbs loaded into registers: about 2.4 us) HBM would idle once the window
 // has landed.  So, for rows of one warp segment (k <= 4096), the producer
-// also asks L2 to prefetch the CTA's next kL2PrefetchBytes of rows
-// (cp.async.bulk.prefetch.L2) right after issuing the window: HBM keeps
-// streaming into L2 through that time, no shared memory is held, and no data
-// comes back to the SM ahead of x; the later stage copies then hit L2.  With
+// also asks L2 to prefetch 40 % of the CTA's remaining rows, at most
+// kL2PrefetchBytes (cp.async.bulk.prefetch.L2), right after issuing the
+// window: HBM keeps streaming into L2 through that time, no shared memory is
+// held, and no data comes back to the SM ahead of x; the next stage copies
+// then hit L2.  Prefetching all the remaining rows front-loads HBM at the
+// moment the x loads and the last-started CTAs' first copies need it
+// (14336x4096: 6.65 us with all of them, 6.67 with 30 %, 6.40 with 40 %,
+// 6.47 with 50 %; 28672x4096 and the Q6_K head meet the byte cap either way).  With
 // the prefetch a window of one stage is best unless the CTA has many stages
 // (kWideWindowUnits).  Q4_K, launched back to back: 14336x4096 7.01 -> 6.73
 // us, 28672x4096 11.14 -> 10.07 us, decode-layer set 29.0 -> 28.1 us.
@@ -454,6 +458,7 @@ constexpr int kStatic = 512;                 // reserve for the kernel's static 
 constexpr int kXWindow = PQ_X_WINDOW;        // stages in flight at most until x is converted
 constexpr int kWideWindowUnits = 8;          // ... for CTAs with at least this many stages; one stage below
 constexpr uint32_t kL2PrefetchBytes = 128 * 1024;   // rows prefetched into L2 after the window (one segment)
+constexpr uint64_t kL2PrefetchPercent = 40;         // ... as a share of the CTA's remaining rows
 
 struct Params {
     const uint8_t *w;
@@ -1242,9 +1247,11 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
                 }
                 src += (size_t)IPS * rowbytes;
                 if (F::kL2Prefetch && G == 1 && u + 1 == window && u + 1 < units) {
-                    // the rows after the window (a multiple of 16 bytes: rows are);
-                    // SwiGLU splits the budget between its gate and up rows
+                    // kL2PrefetchPercent of the rows after the window, rounded up to
+                    // 16 bytes, at most kL2PrefetchBytes; SwiGLU splits the budget
+                    // between its gate and up rows
                     uint64_t pfb = (uint64_t)(nrows - (u + 1) * IPS) * rowbytes;
+                    pfb = (pfb * kL2PrefetchPercent / 100 + 15) / 16 * 16;
                     const uint64_t cap = SW ? kL2PrefetchBytes / 2 : kL2PrefetchBytes;
                     if (pfb > cap) pfb = cap;
                     bulk_prefetch_l2(src, (uint32_t)pfb);
