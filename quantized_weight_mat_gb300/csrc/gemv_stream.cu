@@ -431,9 +431,7 @@ cudaError_t launch_nb(const Params &p0, int grid, cudaStream_t s) {
 // us, 28672x4096 11.14 -> 10.07 us, decode-layer set 29.0 -> 28.1 us.
 // Prefetching for longer rows as well made the set slower (28.7 us).  SwiGLU
 // stages read gate and up rows from two regions; the budget is split
-// between them (fused gate+up 12.2 -> 10.7 us against 128 KB each).  A
-// format opts out with kL2Prefetch = false (per-row int4: 14336x4096 6.9 ->
-// 7.4 us with the prefetch, whatever the window).
+// between them (fused gate+up 12.2 -> 10.7 us against 128 KB each).
 //
 // Consumer warps per CTA are a property of the format (kWarps): 12 where a
 // 24-row stage still leaves at least three ring slots and the decode is
@@ -567,7 +565,6 @@ struct Q4K {
     static constexpr int kBlockBytes = 144;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
-    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the 4 sub-blocks (32 positions each)
         int xs[4];                     // sum of X = 254*xh + xl per sub-block
@@ -630,7 +627,6 @@ struct Q6K {
     static constexpr int kBlockBytes = 210;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
-    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-position parts t = 0..3
         int xs[8];                     // sum of X over the 8 sub-blocks of 16
@@ -727,7 +723,6 @@ struct Q80 {
     static constexpr int kBlockBytes = 272;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
-    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];   // limbs of the four 32-weight blocks
         float u;
@@ -780,7 +775,6 @@ struct I8R {
     static constexpr int kBlockBytes = 256;
     static constexpr bool kRowScaled = true;
     static constexpr int kWarps = 8;
-    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i8row_scale_offset(n_out, k); }
     struct X {
         uint32_t xh[8][4], xl[8][4];   // limbs of chunk (c + lane) mod 8, 16 positions each
@@ -837,7 +831,6 @@ struct Q5K {
     static constexpr int kBlockBytes = 176;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 8;
-    static constexpr bool kL2Prefetch = true;
     struct X {
         uint32_t xh[4][8], xl[4][8];
         int xs[4];
@@ -904,7 +897,6 @@ struct I4R {
     static constexpr int kBlockBytes = 128;
     static constexpr bool kRowScaled = true;
     static constexpr int kWarps = 8;
-    static constexpr bool kL2Prefetch = false;
     static int64_t scale_offset(int64_t n_out, int64_t k) { return i4row_scale_offset(n_out, k); }
     struct X {
         uint32_t eh[4][4], el[4][4], oh[4][4], ol[4][4];   // chunk (c + lane/2) mod 4: even / odd limbs
@@ -969,7 +961,6 @@ struct Q2K {
     static constexpr int kBlockBytes = 84;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
-    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -1039,7 +1030,6 @@ struct Q3K {
     static constexpr int kBlockBytes = 110;
     static constexpr bool kRowScaled = false;
     static constexpr int kWarps = 12;
-    static constexpr bool kL2Prefetch = true;
     static int64_t scale_offset(int64_t, int64_t) { return 0; }
     struct X {
         uint32_t xh[4][8], xl[4][8];
@@ -1214,7 +1204,7 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
             if (!p.early_w) grid_dep_wait();   // the weights may be the previous kernel's output
             const uint64_t pol = make_evict_first_policy();
             const uint8_t *src = p.w + r0 * (int64_t)rowbytes;
-            const int wsel = (!F::kL2Prefetch || units >= kWideWindowUnits) ? kXWindow : 1;
+            const int wsel = units >= kWideWindowUnits ? kXWindow : 1;
             const int window = wsel < NS ? wsel : NS;
             bool x_in = false;         // the consumers have converted x
             int landed = 0, lslot = 0; // stages known to have landed; slot of the next one
@@ -1246,7 +1236,7 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
                     bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
                 }
                 src += (size_t)IPS * rowbytes;
-                if (F::kL2Prefetch && G == 1 && u + 1 == window && u + 1 < units) {
+                if (G == 1 && u + 1 == window && u + 1 < units) {
                     // kL2PrefetchPercent of the rows after the window, rounded up to
                     // 16 bytes, at most kL2PrefetchBytes; SwiGLU splits the budget
                     // between its gate and up rows
