@@ -1911,13 +1911,17 @@ cudaError_t launch(const uint8_t *w, int64_t n_out, int64_t k, const float *x, i
 
 // Whether this kernel runs Q4_K (k, n_out) at `batch` columns.  It is used at
 // batch 2 for long rows (k >= 8192), where it beats the chunked kernel
-// (4096x14336: 14.0 vs 18.6 us); at k = 4096 the chunked kernel is faster,
-// and at batch 3-4 (NB = 4) the chunked or tensor-core kernels are.
+// (4096x14336: 14.0 vs 18.6 us), and at k = 4096 for tall matrices
+// (kNbTallRows rows or more, 128 per CTA on a full GPU), where its streaming
+// beats the register-operand kernel's half-empty 4-column tiles (28672x4096:
+// 16.8 against 19.1 us; 14336x4096: 11.4 against 10.8, so shorter matrices
+// keep that kernel); at batch 3-4 (NB = 4) other kernels are faster.
+constexpr int64_t kNbTallRows = 19456;
 inline bool takes(int64_t k, int64_t n_out, int batch) {
     Params p{};
     const int grid_est = 132;      // fewer SMs than any sm_103 part: a conservative row count
     const int grid = (int)(n_out < grid_est ? n_out : grid_est);
-    return batch == 2 && k >= 8192 && plan<2>(k, n_out, grid, p);
+    return batch == 2 && (k >= 8192 || (k == 4096 && n_out >= kNbTallRows)) && plan<2>(k, n_out, grid, p);
 }
 }  // namespace rowsnb
 
@@ -2796,13 +2800,15 @@ cudaError_t launch(int fmt, const uint8_t *w, int64_t n_out, const float *x, int
                         : launch_t<Q6, 2>(w, n_out, x, nb_cols, y, ldy, grid, s, early_w, epi);
 }
 
-// Whether this kernel runs (fmt, k, n_out) at `batch` columns.  Q4_K: k =
-// 4096, batch 2-8; Q6_K: k = 4096, batch 3-8, and at least one 16-row stage
-// per CTA on a full GPU (at batch 2, and on small matrices, the CUDA-core
-// kernel is faster: output head 83.5 against 93 us at batch 2).
-inline bool takes(int fmt, int64_t k, int64_t n_out, int batch) {
+// Whether this kernel runs (fmt, k, n_out) at `batch` columns with epilogue
+// `kind`.  Q4_K: k = 4096, batch 2-8, except plain batch-2 calls on tall
+// matrices (rowsnb::kNbTallRows, the two-column kernel); Q6_K: k = 4096,
+// batch 3-8, and at least one 16-row stage per CTA on a full GPU (at batch
+// 2, and on small matrices, the CUDA-core kernel is faster: output head 83.5
+// against 93 us at batch 2).
+inline bool takes(int fmt, int64_t k, int64_t n_out, int batch, int kind = kEpiNone) {
     if (k != K || batch < 2 || batch > 8 || n_out < 1) return false;
-    if (fmt == PQ_Q4_K) return true;
+    if (fmt == PQ_Q4_K) return !(batch == 2 && kind == kEpiNone && n_out >= rowsnb::kNbTallRows);
     return fmt == PQ_Q6_K && batch >= 3 && n_out >= 152 * RS;
 }
 }  // namespace rmma
@@ -2820,7 +2826,7 @@ unsigned stream_wait_timeouts(bool reset) {
 }
 
 bool stream_epilogue_fused(int fmt, int64_t n_out, int64_t k, int batch, int kind) {
-    if (batch > 1) return rmma::takes(fmt, k, n_out, batch);
+    if (batch > 1) return rmma::takes(fmt, k, n_out, batch, kind);
     return batch == 1 && n_out >= 1 && k <= (INT64_C(1) << 20) && rowk::takes(fmt, k, n_out, kind == kEpiSwiGLU);
 }
 

@@ -151,6 +151,13 @@ def test_workload_q4_k_4096():
     full_case("q4_k", 4096, 4096, 1, 20, 21)
 
 
+@pytest.mark.parametrize("batch", [2, 3])
+def test_workload_gate_up_small_batch(batch):
+    # 28672 x 4096: at batch 2 the two-column dp4a kernel (tall matrices), at
+    # batch 3 the register-operand kernel
+    full_case("q4_k", 28672, 4096, batch, 24, 25)
+
+
 @pytest.mark.parametrize("j,n_out,k", [(0, 6144, 4096), (1, 4096, 4096), (2, 28672, 4096),
                                        (3, 4096, 14336)])
 def test_workload_decode_layer_set(j, n_out, k):
