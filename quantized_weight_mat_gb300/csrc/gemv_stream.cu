@@ -2480,6 +2480,10 @@ __device__ __forceinline__ void build_x(const Params &p, int t, int warp, int la
 // products of one stage for this warp's super-block (rows g, g+8 at aligned
 // shared addresses ra, rb), giving v[t][0..1] = y parts of rows g, g+8.
 struct Q4 {
+    // stages per CTA barrier (the partial sums of SPS stages are added after
+    // one barrier): 2 at 8 columns (14336x4096 batch 8 15.4 -> 14.8 us), 1 at
+    // 4 (batch 4 11.8 -> 12.0 us with 2)
+    template <int NT> static constexpr int sps() { return NT == 2 ? 2 : 1; }
     static constexpr int ROWB = (K / 256) * 144;          // 2304
     static constexpr int PITCH = ROWB + 16;
     static constexpr bool XSUMS = true;
@@ -2547,6 +2551,7 @@ struct Q4 {
 };
 
 struct Q6 {
+    template <int NT> static constexpr int sps() { return 1; }   // 2 at 8 columns: head 112 -> 115 us
     static constexpr int ROWB = (K / 256) * 210;          // 3360
     static constexpr int PITCH = ROWB + 16;
     static constexpr bool XSUMS = false;
@@ -2622,9 +2627,10 @@ struct Q6 {
 };
 
 template <class F, int NT> constexpr int stage_bytes() { return RS * F::PITCH; }
-template <int NT> constexpr int red_floats() { return 2 * CWARPS * RS * 4 * NT; }
+// partial-sum buffers: two groups of SPS stages, 16 warps x 16 rows x NB columns each
+template <int NT, int SPS = 1> constexpr int red_floats() { return 2 * SPS * CWARPS * RS * 4 * NT; }
 template <class F, int NT> constexpr int smem_bytes() {
-    return F::template stages<NT>() * stage_bytes<F, NT>() + red_floats<NT>() * 4 + 128;
+    return F::template stages<NT>() * stage_bytes<F, NT>() + red_floats<NT, F::template sps<NT>()>() * 4 + 128;
 }
 static_assert(smem_bytes<Q4, 2>() <= kSmemBudget - 512 && smem_bytes<Q6, 1>() <= kSmemBudget - 512 &&
                   smem_bytes<Q6, 2>() <= kSmemBudget - 512,
@@ -2727,29 +2733,35 @@ __global__ void __launch_bounds__(block_threads<NT>(), 1) gemv_rows_mma(Params p
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[slot]);
         }
-        float *rw = red + (size_t)(u & 1) * CWARPS * RS * NB + (size_t)warp * RS * NB;
+        constexpr int SPS = F::template sps<NT>();
+        float *rw = red + (size_t)(u & (2 * SPS - 1)) * CWARPS * RS * NB + (size_t)warp * RS * NB;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             rw[g * NB + 4 * t + i4] = v[t][0];
             rw[(g + 8) * NB + 4 * t + i4] = v[t][1];
         }
+        if (u % SPS != SPS - 1 && u != units - 1) continue;     // one barrier per SPS stages
         named_sync(1, THREADS);
-        // !PROD: every warp is done with the slot: refill it (after ordering
-        // those reads before the copy engine's writes)
-        if (!PROD && threadIdx.x == FILLER && u + NS < units) {
+        const int u0 = u - u % SPS;                             // the first stage since the last barrier
+        // !PROD: every warp is done with those stages' slots: refill them
+        // (after ordering the reads before the copy engine's writes)
+        if (!PROD && threadIdx.x == FILLER) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            fill(u + NS);
+            for (int uu = u0; uu <= u; ++uu)
+                if (uu + NS < units) fill(uu + NS);
         }
-        // warps 0-1 add the 16 warps' parts in warp order while the others go
-        // on with the next stage
-        if (threadIdx.x < per_stage * NB) {
-            const int row = threadIdx.x / NB, col = threadIdx.x % NB;
-            const float *rr = red + (size_t)(u & 1) * CWARPS * RS * NB + row * NB + col;
+        // the first warps add the 16 warps' parts in warp order (one thread
+        // per stage, row and column) while the others go on with the next stages
+        if ((int)threadIdx.x < (u - u0 + 1) * per_stage * NB) {
+            const int su = u0 + (int)threadIdx.x / (per_stage * NB);   // the stage this thread adds
+            const int tid = (int)threadIdx.x % (per_stage * NB);
+            const int row = tid / NB, col = tid % NB;
+            const float *rr = red + (size_t)(su & (2 * SPS - 1)) * CWARPS * RS * NB + row * NB + col;
             float sum = rr[0];
 #pragma unroll
             for (int w2 = 1; w2 < CWARPS; ++w2) sum += rr[(size_t)w2 * RS * NB];
-            const int n_here = nrows - u * per_stage < per_stage ? nrows - u * per_stage : per_stage;
-            const int64_t item = r0 + (int64_t)u * per_stage + row;
+            const int n_here = nrows - su * per_stage < per_stage ? nrows - su * per_stage : per_stage;
+            const int64_t item = r0 + (int64_t)su * per_stage + row;
             if (sw) {
                 // the up row of the pair: stage row row + 8
                 const float *ru = rr + (RS / 2) * NB;
