@@ -450,12 +450,10 @@ constexpr int MAX_STAGES = 8;
 // consumer warps + the producer warp
 template <int CW> constexpr int threads_for() { return (CW + 1) * 32; }
 constexpr int kStatic = 512;                 // reserve for the kernel's static shared memory (barriers)
-#ifndef PQ_X_WINDOW
-#define PQ_X_WINDOW 2
-#endif
-constexpr int kXWindow = PQ_X_WINDOW;        // stages in flight at most until x is converted
+constexpr int kXWindow = 2;                  // stages in flight at most until x is converted
 constexpr int kWideWindowUnits = 8;          // ... for CTAs with at least this many stages; one stage below
 constexpr uint32_t kL2PrefetchBytes = 128 * 1024;   // rows prefetched into L2 after the window (one segment)
+constexpr uint32_t kL2PrefetchBytesLong = 64 * 1024; // ... rows of several segments (k > 4096)
 constexpr uint64_t kL2PrefetchPercent = 40;         // ... as a share of the CTA's remaining rows
 
 struct Params {
@@ -1236,13 +1234,16 @@ __global__ void __launch_bounds__(threads_for<F::kWarps>(), MINB) gemv_rows(Para
                     bulk_g2s_hint(dst, src, bytes, &full_bar[slot], pol);
                 }
                 src += (size_t)IPS * rowbytes;
-                if (G == 1 && u + 1 == window && u + 1 < units) {
+                if (u + 1 == window && u + 1 < units) {
                     // kL2PrefetchPercent of the rows after the window, rounded up to
-                    // 16 bytes, at most kL2PrefetchBytes; SwiGLU splits the budget
-                    // between its gate and up rows
+                    // 16 bytes, at most kL2PrefetchBytes (kL2PrefetchBytesLong for
+                    // rows of several segments: 4096x14336 7.81 -> 7.54 us, where
+                    // 128 KB or 60 % slowed the decode-layer set); SwiGLU splits the
+                    // budget between its gate and up rows
                     uint64_t pfb = (uint64_t)(nrows - (u + 1) * IPS) * rowbytes;
                     pfb = (pfb * kL2PrefetchPercent / 100 + 15) / 16 * 16;
-                    const uint64_t cap = SW ? kL2PrefetchBytes / 2 : kL2PrefetchBytes;
+                    const uint64_t budget = G == 1 ? kL2PrefetchBytes : kL2PrefetchBytesLong;
+                    const uint64_t cap = SW ? budget / 2 : budget;
                     if (pfb > cap) pfb = cap;
                     bulk_prefetch_l2(src, (uint32_t)pfb);
                     if (SW) bulk_prefetch_l2(src + (size_t)p.n_ff * rowbytes, (uint32_t)pfb);
