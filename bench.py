@@ -52,21 +52,12 @@ NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from one ncu capture, keyed by the sha256 of the kernel source it was
-# taken on (code only, comments removed; the first two keys hash the whole
-# file, later ones the part up to the kernel's namespace end); any edit of
-# that code makes the figure stale (reported as null).
-NCU_TRAFFIC = {"f3c237399babbd6c": 66_157_568, "e7a438cff78acc04": 66_132_736, "50834bf8c36ec992": 66_137_344,
-               "265e2c4bb8164730": 66_135_296, "57741aaad287f9f8": 66_134_016, "4113ab643a6634df": 66_133_504,
-               "88c380a8096d1f3a": 66_134_272, "0ed8e9ccb44c3927": 66_134_528,
-               "fa12f136fc9b96c7": 66_134_272}
+# taken on (the code up to the kernel's namespace end, comments removed); any
+# edit of that code makes the figure stale (reported as null).
+NCU_TRAFFIC = {"7217d3a290f0653e": 66_158_080}
 # The same launch under ncu, cold and alone (gpu__time_duration.sum in us,
 # dram__throughput.avg.pct_of_peak_sustained_elapsed), from the same capture.
-NCU_ISOLATED = {"265e2c4bb8164730": {"us": 16.864, "dram_throughput_pct": 49.58},
-                "57741aaad287f9f8": {"us": 16.864, "dram_throughput_pct": 49.58},
-                "4113ab643a6634df": {"us": 16.896, "dram_throughput_pct": 49.57},
-                "88c380a8096d1f3a": {"us": 16.928, "dram_throughput_pct": 49.42},
-                "0ed8e9ccb44c3927": {"us": 16.736, "dram_throughput_pct": 49.96},
-                "fa12f136fc9b96c7": {"us": 16.416, "dram_throughput_pct": 50.86}}
+NCU_ISOLATED = {"7217d3a290f0653e": {"us": 18.24, "dram_throughput_pct": 45.90}}
 
 
 def set_bytes():
