@@ -173,7 +173,8 @@ int for_each_chunk(int fmt, int64_t n_out, int64_t k, int batch, int forced, F &
 
 // Mat-vec with an optional epilogue.  The kernel choice is pq_gemv's for the
 // n_out x k matrix (for SwiGLU the fused 2 * n_ff-row matrix); the batch-1
-// whole-row kernel and the tensor-core kernel fuse the epilogue into their
+// whole-row kernel, the register-operand kernel (Q4_K and Q6_K at k = 4096,
+// batch 2-8) and the tensor-core kernels fuse the epilogue into their
 // stores, the others run it as a small kernel afterwards (SwiGLU through a
 // pool buffer of batch x n_out outputs).
 int gemv_epi_impl(int fmt, const void *w_blocks, int n_out, int k, const float *x, int batch, float *y,

@@ -6,9 +6,11 @@ gate+up matrix (gate rows first); pq_gemv_bias: y = W x + bias (PESTI README,
 mat-vec's bar applied to the epilogue's output: the kernels' per-output error
 (about 2e-5 RMS on the batch-1 path) grows through silu(g) * u by a factor of
 about 20 at the worst output, well inside it.  Batch 1 runs the whole-row
-kernel with the epilogue in its stores, batch >= 5 the tensor-core kernel
-with it in the final store or the finishing kernel, the rest a plain kernel
-followed by a small epilogue kernel.
+kernel with the epilogue in its stores; Q4_K and Q6_K at k = 4096 and
+batch 2-8 the register-operand kernel, also with it in its stores; Q4_K at
+other k, and batch 9 and above, the tensor-core kernels with it in the final
+store or the finishing kernel; the rest a plain kernel followed by a small
+epilogue kernel.
 """
 import numpy as np
 import pytest
@@ -79,6 +81,20 @@ def test_bias_parity(n_out, k, fmt, batch):
     b = bias_for(n_out, 912)
     got = run_bias(fmt, w, n_out, k, x, b)
     ok, err, bound = tolerance_ok(got, oracle.gemv_bias(fmt, w, n_out, k, x, b))
+    assert ok, f"max err {err:.3g} > {bound:.3g}"
+
+
+@pytest.mark.parametrize("batch", [5, 8])
+@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+def test_swiglu_stage_groups(fmt, batch):
+    # 3500 pairs at k = 4096: 23 pairs per CTA, so three stages of 8, 8 and 7
+    # pairs; at 8 columns the Q4_K kernel adds the partial sums of two stages
+    # after one barrier, which leaves a group of one stage at the end
+    n_ff, k = 3500, 4096
+    w = weights(fmt, 2 * n_ff, k, "quantized", 36)
+    x = x_for(batch, k, 37)
+    got = run_swiglu(fmt, w, n_ff, k, x)
+    ok, err, bound = tolerance_ok(got, oracle.gemv_swiglu(fmt, w, n_ff, k, x))
     assert ok, f"max err {err:.3g} > {bound:.3g}"
 
 

@@ -151,6 +151,16 @@ def test_workload_q4_k_4096():
     full_case("q4_k", 4096, 4096, 1, 20, 21)
 
 
+@pytest.mark.parametrize("n_out,batch", [(7000, 5), (7000, 8), (6144, 8), (20000, 6), (2500, 7), (20000, 8)])
+def test_register_operand_stage_groups(n_out, batch):
+    # Q4_K at k = 4096 with 5-8 columns: the register-operand kernel adds the
+    # partial sums of two 16-row stages after one barrier.  Rows per CTA give
+    # odd stage counts with a partial last stage (7000: 46-47 rows, stages of
+    # 16, 16 and 14-15; 20000: 131-132 rows, nine stages) and CTAs of one or
+    # two stages (2500: 16-17 rows)
+    full_case("q4_k", n_out, 4096, batch, 60, 61)
+
+
 @pytest.mark.parametrize("batch", [2, 3])
 def test_workload_gate_up_small_batch(batch):
     # 28672 x 4096: at batch 2 the two-column dp4a kernel (tall matrices), at
