@@ -2358,11 +2358,6 @@ __device__ __forceinline__ void mma16816_acc(float (&c)[4], uint32_t a0, uint32_
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -2379,6 +2374,16 @@ __device__ __forceinline__ uint32_t bytes_h2(uint32_t v, uint32_t sel) {
     return r;
 }
 __host__ __device__ constexpr uint32_t pair_sel(uint32_t i, uint32_t j) { return i | 0x40u | (j << 8) | 0x4000u; }
+// Four bytes holding values 0-15 -> two fp16 pairs (bytes 0,1 and 2,3), each
+// value q as q * 2^-9 exactly: an e4m3 byte below 16 is q/8 * 2^-6 (q < 8,
+// subnormal) or (1 + (q-8)/8) * 2^-6 (8 <= q < 16), q * 2^-9 in both cases.
+__device__ __forceinline__ void nibble_bytes_h2(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    asm("{ .reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b; }"
+        : "=r"(lo), "=r"(hi) : "r"(v));
+}
 
 // Stage u (rows_u rows) of this CTA into ring slot `slot`.
 template <int ROWB, int PITCH, int STAGE>
@@ -2433,13 +2438,14 @@ __device__ __forceinline__ void build_x(const Params &p, int t, int warp, int la
 #pragma unroll
         for (int j = 0; j < 4; ++j) sx[j] = v[s][j] * mult;
         if (XSUMS) xs[s >> 1] += (sx[0] + sx[1]) + (sx[2] + sx[3]);
-        // positions (0, 2) and (1, 3) as fp16 pairs: hi parts, then the rest
-        const __half2 h02 = __floats2half2_rn(sx[0], sx[2]), h13 = __floats2half2_rn(sx[1], sx[3]);
-        const float2 f02 = __half22float2(h02), f13 = __half22float2(h13);
-        const __half2 l02 = __floats2half2_rn(sx[0] - f02.x, sx[2] - f02.y);
-        const __half2 l13 = __floats2half2_rn(sx[1] - f13.x, sx[3] - f13.y);
-        const uint32_t hb0 = *reinterpret_cast<const uint32_t *>(&h02), hb1 = *reinterpret_cast<const uint32_t *>(&h13);
-        const uint32_t lb0 = *reinterpret_cast<const uint32_t *>(&l02), lb1 = *reinterpret_cast<const uint32_t *>(&l13);
+        // positions (0, 1) and (2, 3) as fp16 pairs (K slots 2i, 2i+1 and
+        // 2i+8, 2i+9): hi parts, then the rest
+        const __half2 h01 = __floats2half2_rn(sx[0], sx[1]), h23 = __floats2half2_rn(sx[2], sx[3]);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(sx[0] - f01.x, sx[1] - f01.y);
+        const __half2 l23 = __floats2half2_rn(sx[2] - f23.x, sx[3] - f23.y);
+        const uint32_t hb0 = *reinterpret_cast<const uint32_t *>(&h01), hb1 = *reinterpret_cast<const uint32_t *>(&h23);
+        const uint32_t lb0 = *reinterpret_cast<const uint32_t *>(&l01), lb1 = *reinterpret_cast<const uint32_t *>(&l23);
         own[s][0] = lo_part ? lb0 : hb0;
         own[s][1] = lo_part ? lb1 : hb1;
         other[s][0] = lo_part ? hb0 : lb0;
@@ -2489,9 +2495,11 @@ struct Q4 {
     static constexpr int PITCH = ROWB + 16;
     static constexpr bool XSUMS = true;
     template <int NT> static constexpr int stages() { return 5; }
-    // sc*q exact: (1024+q)*sc - 1024*sc (low nibbles, sub-block 2c) and
-    // (1024+16q)*sc/16 - 64*sc (high nibbles, sub-block 2c+1); the mins
-    // through one product of the 6-bit mins with the sub-block sums;
+    // sc*q exact: the code bytes (low nibbles, sub-block 2c; high nibbles
+    // shifted down, sub-block 2c+1) become q * 2^-9 through the e4m3
+    // conversion, times sc * 2^9 (an fp16 integer, at most 32256): the exact
+    // product sc*q <= 945 is an fp16 integer.  The mins through one product
+    // of the 6-bit mins with the sub-block sums;
     // y += 2^-e * (d * (A.x') - dmin * (m.XS'))
     template <int NT>
     static __device__ __forceinline__ void stage(uint32_t ra, uint32_t rb, int warp, int lane,
@@ -2508,25 +2516,25 @@ struct Q4 {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             const uint32_t sw = (uint32_t)(2 * (cc & 1));
-            const uint32_t Sla = bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw, sw));
-            const uint32_t Slb = bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw, sw));
-            const uint32_t Sha = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x2C002C00u);
-            const uint32_t Shb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x2C002C00u);
-            const uint32_t Cla = hmul2_bits(Sla, 0xE400E400u), Clb = hmul2_bits(Slb, 0xE400E400u);
-            const uint32_t Cha = hmul2_bits(Sha, 0xE400E400u), Chb = hmul2_bits(Shb, 0xE400E400u);
+            // (sc * 2^9) pairs of sub-blocks 2c (l) and 2c+1 (h) of rows a, b
+            const uint32_t Sla = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
+            const uint32_t Slb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
+            const uint32_t Sha = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
+            const uint32_t Shb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
 #pragma unroll
             for (int pp = 0; pp < 2; ++pp) {
                 const uint32_t off = 16u + 32u * cc + 16u * pp + 4u * i4;
                 const uint32_t wa = rowk::lds32(ra + off), wb = rowk::lds32(rb + off);
-                const uint32_t sa = wa >> 8, sb = wb >> 8;
-                const uint32_t l0 = hfma2_bits((wa & 0x000F000Fu) | 0x64006400u, Sla, Cla);
-                const uint32_t l1 = hfma2_bits((wb & 0x000F000Fu) | 0x64006400u, Slb, Clb);
-                const uint32_t l2 = hfma2_bits((sa & 0x000F000Fu) | 0x64006400u, Sla, Cla);
-                const uint32_t l3 = hfma2_bits((sb & 0x000F000Fu) | 0x64006400u, Slb, Clb);
-                const uint32_t h0 = hfma2_bits((wa & 0x00F000F0u) | 0x64006400u, Sha, Cha);
-                const uint32_t h1 = hfma2_bits((wb & 0x00F000F0u) | 0x64006400u, Shb, Chb);
-                const uint32_t h2 = hfma2_bits((sa & 0x00F000F0u) | 0x64006400u, Sha, Cha);
-                const uint32_t h3 = hfma2_bits((sb & 0x00F000F0u) | 0x64006400u, Shb, Chb);
+                // positions 4i, 4i+1 (l0, l1, h0, h1) and 4i+2, 4i+3 (l2, l3, h2, h3)
+                uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+                nibble_bytes_h2(wa & 0x0F0F0F0Fu, l0, l2);
+                nibble_bytes_h2(wb & 0x0F0F0F0Fu, l1, l3);
+                nibble_bytes_h2((wa >> 4) & 0x0F0F0F0Fu, h0, h2);
+                nibble_bytes_h2((wb >> 4) & 0x0F0F0F0Fu, h1, h3);
+                l0 = hmul2_bits(l0, Sla); l2 = hmul2_bits(l2, Sla);
+                l1 = hmul2_bits(l1, Slb); l3 = hmul2_bits(l3, Slb);
+                h0 = hmul2_bits(h0, Sha); h2 = hmul2_bits(h2, Sha);
+                h1 = hmul2_bits(h1, Shb); h3 = hmul2_bits(h3, Shb);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     mma16816_acc(c[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
@@ -2602,10 +2610,10 @@ struct Q6 {
                         const uint32_t hb1 = (r < 3 ? (qh1 << (4 - 2 * r)) : (qh1 >> 2)) & 0x30303030u;
                         const uint32_t q0 = lo0 | hb0, q1 = lo1 | hb1;
                         // (q - 32) pairs: subtract the fp16 1056 = 1024 + 32
-                        const uint32_t a0 = bytes_h2<0x64206420u>(q0, pair_sel(0, 2));
-                        const uint32_t a1 = bytes_h2<0x64206420u>(q1, pair_sel(0, 2));
-                        const uint32_t a2 = bytes_h2<0x64206420u>(q0, pair_sel(1, 3));
-                        const uint32_t a3 = bytes_h2<0x64206420u>(q1, pair_sel(1, 3));
+                        const uint32_t a0 = bytes_h2<0x64206420u>(q0, pair_sel(0, 1));
+                        const uint32_t a1 = bytes_h2<0x64206420u>(q1, pair_sel(0, 1));
+                        const uint32_t a2 = bytes_h2<0x64206420u>(q0, pair_sel(2, 3));
+                        const uint32_t a3 = bytes_h2<0x64206420u>(q1, pair_sel(2, 3));
                         const float sa = (float)(int)(int8_t)(sc0[s >> 2] >> (8 * (s & 3)));
                         const float sb = (float)(int)(int8_t)(sc1[s >> 2] >> (8 * (s & 3)));
 #pragma unroll

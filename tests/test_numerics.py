@@ -5,6 +5,9 @@
    - 1024*sc for low nibbles and (1024+16q)*(sc/16) - 64*sc for high nibbles.
    Every operand is an exact fp16 value and the exact result sc*q <= 945 is
    an fp16 integer, so the single rounding of the fused operation is exact.
+   The register-operand kernel instead converts the code bytes as e4m3 values
+   (q * 2^-9 exactly for 0 <= q < 16) and multiplies by the fp16 integer
+   sc * 2^9: again one rounding of an exactly representable product.
 2. Tensor-core x operand: x' = x_hi + x_lo with x_hi = fp16(x') and x_lo =
    fp16(x' - x_hi) leaves a residual of at most 2^-21 |x'| + 2^-25 (x_lo turns
    subnormal below 2^-14, where fp16 has a fixed step of 2^-24); every
@@ -68,6 +71,31 @@ def test_fp16_bias_trick_is_exact(sc):
         assert f16_exact(a) and f16_exact(b) and f16_exact(c)
         exact = Fraction(a) * b + c
         assert exact == sc * q and f16_exact(exact)
+
+
+def e4m3_value(b: int) -> Fraction:
+    """An OCP e4m3 byte by its definition: sign, 4 exponent bits (bias 7), 3
+    mantissa bits, subnormals at exponent 0 (S.1111.111 is NaN)."""
+    sign = -1 if b & 0x80 else 1
+    e, m = (b >> 3) & 0xF, b & 7
+    assert not (e == 15 and m == 7), "NaN"
+    if e == 0:
+        return sign * Fraction(m, 8) * Fraction(1, 2 ** 6)
+    return sign * (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+@pytest.mark.parametrize("sc", range(64))
+def test_e4m3_nibble_decode_times_scale_is_exact(sc):
+    # the register-operand kernel: code bytes 0-15 through the e4m3 -> fp16
+    # conversion give q * 2^-9, multiplied by the fp16 sc * 2^9 in one rounding
+    s512 = sc * 512
+    assert f16_exact(s512)
+    for q in range(16):
+        v = e4m3_value(q)
+        assert v == Fraction(q, 512) and f16_exact(v)
+        assert v * s512 == sc * q and f16_exact(sc * q)
+        # the same product in numpy's fp16 arithmetic
+        assert float(np.float16(float(v)) * np.float16(s512)) == sc * q
 
 
 # ------------------------------------------------------------------ 2
