@@ -2374,16 +2374,6 @@ __device__ __forceinline__ uint32_t bytes_h2(uint32_t v, uint32_t sel) {
     return r;
 }
 __host__ __device__ constexpr uint32_t pair_sel(uint32_t i, uint32_t j) { return i | 0x40u | (j << 8) | 0x4000u; }
-// Four bytes holding values 0-15 -> two fp16 pairs (bytes 0,1 and 2,3), each
-// value q as q * 2^-9 exactly: an e4m3 byte below 16 is q/8 * 2^-6 (q < 8,
-// subnormal) or (1 + (q-8)/8) * 2^-6 (8 <= q < 16), q * 2^-9 in both cases.
-__device__ __forceinline__ void nibble_bytes_h2(uint32_t v, uint32_t &lo, uint32_t &hi) {
-    asm("{ .reg .b16 a, b;\n\t"
-        "mov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, b; }"
-        : "=r"(lo), "=r"(hi) : "r"(v));
-}
 
 // Stage u (rows_u rows) of this CTA into ring slot `slot`.
 template <int ROWB, int PITCH, int STAGE>

@@ -266,7 +266,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // hi/lo halves as prep_x_tc, stored in the order the warps load them as
 // mma.sync A fragments.  Per 16-position step s of the super-block and group
 // mt of 8 columns, lane L = 4g + i holds 16 bytes {a0, a1, a2, a3}: column
-// 8mt + g, positions 16s + 4i + {0, 2} (a0 hi, a1 lo) and + {1, 3} (a2 hi, a3
+// 8mt + g, positions 16s + 4i + {0, 1} (a0 hi, a1 lo) and + {2, 3} (a2 hi, a3
 // lo) -- the K slots 2i, 2i+1 and 2i+8, 2i+9 of the fragment, matching the
 // weights a thread decodes from one 4-byte qs word.  Then per group, lane L:
 // 8 bytes {hi, lo} of the sums over sub-blocks 2i and 2i+1 of column 8mt + g
@@ -312,10 +312,10 @@ __global__ void __launch_bounds__(256) prep_x_mma(const float *__restrict__ x, i
         undo[t] = __uint_as_float((uint32_t)(127 - e) << 23);    // 2^-e
     }
     __syncthreads();
-    // position t: step t/16, lane slot i = (t%16)/4, r = t%4 -> register 0/2
-    // (hi) or 1/3 (lo) for r even/odd, low half for r < 2
+    // position t: step t/16, lane slot i = (t%16)/4, r = t%4 -> registers
+    // 0 (hi) and 1 (lo) for r < 2, 2 and 3 for r >= 2, low half for r even
     const int st = t >> 4, i4 = (t >> 2) & 3, r = t & 3;
-    const int hreg = (r & 1) ? 2 : 0, half = r >> 1;
+    const int hreg = (r >> 1) ? 2 : 0, half = r & 1;
 #pragma unroll
     for (int b = 0; b < NBP; ++b) {
         const float sx = v[b] * mult[b];
@@ -753,8 +753,9 @@ __global__ void __launch_bounds__(tc_threads<NBP>(), 1)
 //           rows 32(w%4)..+31 of the item's 128-row tile, in four n8 blocks.
 //           Per item: the 256 K of the super-block in 16 steps; each qs word
 //           gives a thread's four weights of two steps (low and high
-//           nibbles), decoded with one LOP3 + one HFMA2 per two weights; one
-//           K=16 product of the mins per n8 block; then, per row and column,
+//           nibbles), decoded with one mask per four codes, the e4m3
+//           conversion (q * 2^-9) and one HMUL2 by sc * 2^9 per two weights;
+//           one K=16 product of the mins per n8 block; then, per row and column,
 //           y += 2^-e * (d*(x'.A) - dmin*(XS'.m)) in registers.
 //           At the end of a tile the four groups' sums are added in group
 //           order through shared memory and stored (or written as split-K
@@ -778,8 +779,8 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint4 &a, uint32_
 }
 
 // fp16 pairs as bit patterns, so that the arithmetic below takes them as
-// immediates: 1024, -1024, 1/16, -64
-constexpr uint32_t kH2_1024 = 0x64006400u, kH2_M1024 = 0xE400E400u, kH2_16TH = 0x2C002C00u, kH2_M64 = 0xD400D400u;
+// immediate: 1024
+constexpr uint32_t kH2_1024 = 0x64006400u;
 __device__ __forceinline__ __half2 h2_of(uint32_t bits) { return *reinterpret_cast<const __half2 *>(&bits); }
 __device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(h2_of(a), h2_of(b))); }
 
@@ -796,6 +797,7 @@ __device__ __forceinline__ uint32_t bytes_h2(uint32_t v, uint32_t i) {
     const uint32_t p = __byte_perm(v, 0x64646464u, sel);
     return h2_bits(__hsub2(h2_of(p), h2_of(kH2_1024)));
 }
+constexpr uint32_t kH2_512 = 0x60006000u;
 
 // Wait until the producer has issued item g (the counter it advances after
 // each issue), bounded like the mbarrier waits.  A group that takes every
@@ -912,17 +914,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                     for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    // scale pairs of sub-blocks 2c (low nibbles) and 2c+1 (high):
-                    // (1024+q)*sc - 1024*sc and (1024+16q)*sc/16 - 64*sc
-                    uint32_t Slo[4], Clo[4], Shi[4], Chi[4];
+                    // (sc * 2^9) pairs of sub-blocks 2c (low nibbles) and 2c+1
+                    // (high nibbles): the codes come as q * 2^-9 from the e4m3
+                    // conversion, and sc*q <= 945 is exact in fp16
+                    uint32_t Slo[4], Shi[4];
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt) {
                         const uint32_t w = scw[nt][c >> 1];
-                        const uint32_t lo = byte_h2(w, 2 * (c & 1)), hi = byte_h2(w, 2 * (c & 1) + 1);
-                        Slo[nt] = lo;
-                        Clo[nt] = hmul2_u(lo, kH2_M1024);
-                        Shi[nt] = hmul2_u(hi, kH2_16TH);
-                        Chi[nt] = hmul2_u(hi, kH2_M64);
+                        Slo[nt] = hmul2_u(byte_h2(w, 2 * (c & 1)), kH2_512);
+                        Shi[nt] = hmul2_u(byte_h2(w, 2 * (c & 1) + 1), kH2_512);
                     }
 #pragma unroll
                     for (int pp = 0; pp < 2; ++pp) {
@@ -936,11 +936,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 #pragma unroll
                         for (int nt = 0; nt < 4; ++nt) {
                             const uint32_t w = *reinterpret_cast<const uint32_t *>(rb + nt * 1152 + 16 + 32 * c + 16 * pp + 4 * tig);
-                            const uint32_t s8 = w >> 8;
-                            const uint32_t b0 = hfma2_u((w & 0x000F000Fu) | 0x64006400u, Slo[nt], Clo[nt]);
-                            const uint32_t b1 = hfma2_u((s8 & 0x000F000Fu) | 0x64006400u, Slo[nt], Clo[nt]);
-                            const uint32_t b2 = hfma2_u((w & 0x00F000F0u) | 0x64006400u, Shi[nt], Chi[nt]);
-                            const uint32_t b3 = hfma2_u((s8 & 0x00F000F0u) | 0x64006400u, Shi[nt], Chi[nt]);
+                            // positions 4tig, 4tig+1 (b0, b2) and 4tig+2, 4tig+3 (b1, b3)
+                            uint32_t b0, b1, b2, b3;
+                            nibble_bytes_h2(w & 0x0F0F0F0Fu, b0, b1);
+                            nibble_bytes_h2((w >> 4) & 0x0F0F0F0Fu, b2, b3);
+                            b0 = hmul2_u(b0, Slo[nt]);
+                            b1 = hmul2_u(b1, Slo[nt]);
+                            b2 = hmul2_u(b2, Shi[nt]);
+                            b3 = hmul2_u(b3, Shi[nt]);
 #pragma unroll
                             for (int mt = 0; mt < MT; ++mt) {
                                 mma_16816(acc[mt][nt], alo[mt], b0, b1);

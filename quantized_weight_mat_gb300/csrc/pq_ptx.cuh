@@ -132,6 +132,17 @@ __device__ __forceinline__ void named_arrive(int id, int threads) {
 }
 
 // 4-way byte dot products, accumulated in 32-bit integers.
+// Four bytes holding values 0-15 -> two fp16 pairs (bytes 0,1 and 2,3), each
+// value q as q * 2^-9 exactly: an e4m3 byte below 16 is q/8 * 2^-6 (q < 8,
+// subnormal) or (1 + (q-8)/8) * 2^-6 (8 <= q < 16), q * 2^-9 in both cases.
+__device__ __forceinline__ void nibble_bytes_h2(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    asm("{ .reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b; }"
+        : "=r"(lo), "=r"(hi) : "r"(v));
+}
+
 __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
     int d;
     asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
