@@ -110,10 +110,10 @@ template <int NBP> size_t scratch_bytes(int64_t k, int grid) {
 
 // K order inside a super-block: chunk e of A-column a (8 fp16 per 16 bytes)
 // holds weight position pos(a, e).  It follows how two qs words turn into
-// four half2 pairs: low nibbles of bytes (0,2), then (1,3), of each word.
-__host__ __device__ constexpr int perm8(int e) { return (e & 4) | ((e & 1) << 1) | ((e >> 1) & 1); }
+// four half2 pairs: bytes (0,1), then (2,3), of each word -- their low
+// nibbles in the chunk's first half, their high nibbles in the second.
 __host__ __device__ constexpr int kpos(int a, int e) {
-    return 64 * (a / 8) + 32 * ((a % 8) / 4) + 8 * (a % 4) + perm8(e);
+    return 64 * (a / 8) + 32 * ((a % 8) / 4) + 8 * (a % 4) + e;
 }
 
 // byte offset of element (n, K) in a K-major no-swizzle operand whose 8-row
@@ -388,12 +388,9 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-    const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b),
-                              *reinterpret_cast<const __half2 *>(&c));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<const uint32_t *>(&v); }
+__device__ __forceinline__ __half2 h2_of(uint32_t bits) { return *reinterpret_cast<const __half2 *>(&bits); }
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(h2_of(a), h2_of(b))); }
 
 // Each thread reads 16 consecutive 32-bit columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -682,28 +679,27 @@ __global__ void __launch_bounds__(tc_threads<NBP>(), 1)
             const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
             // 6-bit scales of sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
             const uint32_t sc4 = ((h ? hd.w : hd.y) & mA) | ((hd.y >> 2) & mB);
-            // scale pairs: low nibbles -> (1024+q)*sc - 1024*sc, high nibbles -> (1024+16q)*sc/16 - 64*sc
-            const __half slo = __int2half_rn((int)((sc4 >> (16 * cc)) & 0xFF));
-            const __half shi = __int2half_rn((int)((sc4 >> (16 * cc + 8)) & 0xFF));
+            // (sc * 2^9) pairs: the codes come as q * 2^-9 from the e4m3
+            // conversion, and sc*q <= 945 is exact in fp16
+            const __half slo = __int2half_rn((int)((sc4 >> (16 * cc)) & 0xFF) * 512);
+            const __half shi = __int2half_rn((int)((sc4 >> (16 * cc + 8)) & 0xFF) * 512);
             const uint32_t Slo = h2_bits(__halves2half2(slo, slo));
-            const uint32_t Clo = h2_bits(__hmul2(__halves2half2(slo, slo), __float2half2_rn(-1024.0f)));
-            const uint32_t Shi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(0.0625f)));
-            const uint32_t Chi = h2_bits(__hmul2(__halves2half2(shi, shi), __float2half2_rn(-64.0f)));
+            const uint32_t Shi = h2_bits(__halves2half2(shi, shi));
             const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
             // the chunk's 64 K values of row r: TMEM column j holds K = 2j, 2j+1
             uint32_t R[32];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 const uint32_t w0 = w[2 * a], w1 = w[2 * a + 1];
-                const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-                R[4 * a + 0] = hfma2_u((w0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                R[4 * a + 1] = hfma2_u((s0 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                R[4 * a + 2] = hfma2_u((w1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                R[4 * a + 3] = hfma2_u((s1 & 0x000F000Fu) | 0x64006400u, Slo, Clo);
-                R[16 + 4 * a + 0] = hfma2_u((w0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                R[16 + 4 * a + 1] = hfma2_u((s0 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                R[16 + 4 * a + 2] = hfma2_u((w1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
-                R[16 + 4 * a + 3] = hfma2_u((s1 & 0x00F000F0u) | 0x64006400u, Shi, Chi);
+                nibble_bytes_h2(w0 & 0x0F0F0F0Fu, R[4 * a + 0], R[4 * a + 1]);
+                nibble_bytes_h2(w1 & 0x0F0F0F0Fu, R[4 * a + 2], R[4 * a + 3]);
+                nibble_bytes_h2((w0 >> 4) & 0x0F0F0F0Fu, R[16 + 4 * a + 0], R[16 + 4 * a + 1]);
+                nibble_bytes_h2((w1 >> 4) & 0x0F0F0F0Fu, R[16 + 4 * a + 2], R[16 + 4 * a + 3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    R[4 * a + j] = hmul2_u(R[4 * a + j], Slo);
+                    R[16 + 4 * a + j] = hmul2_u(R[16 + 4 * a + j], Shi);
+                }
             }
             // this buffer's slots are free once the products of the super-block
             // that used them before are complete
@@ -781,8 +777,6 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint4 &a, uint32_
 // fp16 pairs as bit patterns, so that the arithmetic below takes them as
 // immediate: 1024
 constexpr uint32_t kH2_1024 = 0x64006400u;
-__device__ __forceinline__ __half2 h2_of(uint32_t bits) { return *reinterpret_cast<const __half2 *>(&bits); }
-__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(h2_of(a), h2_of(b))); }
 
 // byte i (0..3) of v as an exact fp16 value, duplicated in both halves
 __device__ __forceinline__ uint32_t byte_h2(uint32_t v, int i) {
