@@ -2485,12 +2485,12 @@ struct Q4 {
     static constexpr int PITCH = ROWB + 16;
     static constexpr bool XSUMS = true;
     template <int NT> static constexpr int stages() { return 5; }
-    // sc*q exact: the code bytes (low nibbles, sub-block 2c; high nibbles
-    // shifted down, sub-block 2c+1) become q * 2^-9 through the e4m3
-    // conversion, times sc * 2^9 (an fp16 integer, at most 32256): the exact
-    // product sc*q <= 945 is an fp16 integer.  The mins through one product
-    // of the 6-bit mins with the sub-block sums;
-    // y += 2^-e * (d * (A.x') - dmin * (m.XS'))
+    // The code bytes (low nibbles, sub-block 2c; high nibbles shifted down,
+    // sub-block 2c+1) become q * 2^-9 through the e4m3 conversion; at 8
+    // columns times sc * 2^9 (an fp16 integer, at most 32256), so that A is
+    // sc*q exactly (<= 945, an fp16 integer); at 4 columns sc multiplies the
+    // sub-block's f32 sums.  The mins through one product of the 6-bit mins
+    // with the sub-block sums; y += 2^-e * (d * (A.x') - dmin * (m.XS'))
     template <int NT>
     static __device__ __forceinline__ void stage(uint32_t ra, uint32_t rb, int warp, int lane,
                                                  const uint32_t (&xb)[NT][16][2], const uint32_t (&xsb)[NT],
@@ -2503,35 +2503,80 @@ struct Q4 {
         float c[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t) c[t][0] = c[t][1] = c[t][2] = c[t][3] = 0.f;
+        if constexpr (NT == 1) {
+            // 4 columns: each sub-block's two MMAs on the unscaled codes into
+            // their own f32 sums, scaled by sc in f32 afterwards (no fp16
+            // multiplies; 14336x4096 batch 2 / 4 10.14 / 10.55 -> 9.82 / 10.32
+            // us).  The 8-column instance has no registers for those sums.
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t sw = (uint32_t)(2 * (cc & 1));
-            // (sc * 2^9) pairs of sub-blocks 2c (l) and 2c+1 (h) of rows a, b
-            const uint32_t Sla = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
-            const uint32_t Slb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
-            const uint32_t Sha = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
-            const uint32_t Shb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t sw = (uint32_t)(2 * (cc & 1));
+                // 6-bit scales as f32: the byte under the exponent bits of 2^23, minus 2^23
+                const float fla = __uint_as_float(__byte_perm(sca[cc >> 1], 0x4B000000u, 0x7650u | sw)) - 8388608.0f;
+                const float fha = __uint_as_float(__byte_perm(sca[cc >> 1], 0x4B000000u, 0x7650u | (sw + 1))) - 8388608.0f;
+                const float flb = __uint_as_float(__byte_perm(scb[cc >> 1], 0x4B000000u, 0x7650u | sw)) - 8388608.0f;
+                const float fhb = __uint_as_float(__byte_perm(scb[cc >> 1], 0x4B000000u, 0x7650u | (sw + 1))) - 8388608.0f;
+                float cl[NT][4], ch[NT][4];
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-                const uint32_t off = 16u + 32u * cc + 16u * pp + 4u * i4;
-                const uint32_t wa = rowk::lds32(ra + off), wb = rowk::lds32(rb + off);
-                // positions 4i, 4i+1 (l0, l1, h0, h1) and 4i+2, 4i+3 (l2, l3, h2, h3)
-                uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
-                nibble_bytes_h2(wa & 0x0F0F0F0Fu, l0, l2);
-                nibble_bytes_h2(wb & 0x0F0F0F0Fu, l1, l3);
-                nibble_bytes_h2((wa >> 4) & 0x0F0F0F0Fu, h0, h2);
-                nibble_bytes_h2((wb >> 4) & 0x0F0F0F0Fu, h1, h3);
-                l0 = hmul2_bits(l0, Sla); l2 = hmul2_bits(l2, Sla);
-                l1 = hmul2_bits(l1, Slb); l3 = hmul2_bits(l3, Slb);
-                h0 = hmul2_bits(h0, Sha); h2 = hmul2_bits(h2, Sha);
-                h1 = hmul2_bits(h1, Shb); h3 = hmul2_bits(h3, Shb);
+                for (int pp = 0; pp < 2; ++pp) {
+                    const uint32_t off = 16u + 32u * cc + 16u * pp + 4u * i4;
+                    const uint32_t wa = rowk::lds32(ra + off), wb = rowk::lds32(rb + off);
+                    uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+                    nibble_bytes_h2(wa & 0x0F0F0F0Fu, l0, l2);
+                    nibble_bytes_h2(wb & 0x0F0F0F0Fu, l1, l3);
+                    nibble_bytes_h2((wa >> 4) & 0x0F0F0F0Fu, h0, h2);
+                    nibble_bytes_h2((wb >> 4) & 0x0F0F0F0Fu, h1, h3);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (pp == 0) {
+                            mma16816(cl[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
+                            mma16816(ch[t], h0, h1, h2, h3, xb[t][4 * cc + pp + 2][0], xb[t][4 * cc + pp + 2][1]);
+                        } else {
+                            mma16816_acc(cl[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
+                            mma16816_acc(ch[t], h0, h1, h2, h3, xb[t][4 * cc + pp + 2][0], xb[t][4 * cc + pp + 2][1]);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    mma16816_acc(c[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
-                    mma16816_acc(c[t], h0, h1, h2, h3, xb[t][4 * cc + pp + 2][0], xb[t][4 * cc + pp + 2][1]);
+                    c[t][0] = fmaf(fla, cl[t][0], fmaf(fha, ch[t][0], c[t][0]));
+                    c[t][1] = fmaf(fla, cl[t][1], fmaf(fha, ch[t][1], c[t][1]));
+                    c[t][2] = fmaf(flb, cl[t][2], fmaf(fhb, ch[t][2], c[t][2]));
+                    c[t][3] = fmaf(flb, cl[t][3], fmaf(fhb, ch[t][3], c[t][3]));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t sw = (uint32_t)(2 * (cc & 1));
+                // (sc * 2^9) pairs of sub-blocks 2c (l) and 2c+1 (h) of rows a, b
+                const uint32_t Sla = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
+                const uint32_t Slb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw, sw)), 0x60006000u);
+                const uint32_t Sha = hmul2_bits(bytes_h2<0x64006400u>(sca[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
+                const uint32_t Shb = hmul2_bits(bytes_h2<0x64006400u>(scb[cc >> 1], pair_sel(sw + 1, sw + 1)), 0x60006000u);
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const uint32_t off = 16u + 32u * cc + 16u * pp + 4u * i4;
+                    const uint32_t wa = rowk::lds32(ra + off), wb = rowk::lds32(rb + off);
+                    // positions 4i, 4i+1 (l0, l1, h0, h1) and 4i+2, 4i+3 (l2, l3, h2, h3)
+                    uint32_t l0, l1, l2, l3, h0, h1, h2, h3;
+                    nibble_bytes_h2(wa & 0x0F0F0F0Fu, l0, l2);
+                    nibble_bytes_h2(wb & 0x0F0F0F0Fu, l1, l3);
+                    nibble_bytes_h2((wa >> 4) & 0x0F0F0F0Fu, h0, h2);
+                    nibble_bytes_h2((wb >> 4) & 0x0F0F0F0Fu, h1, h3);
+                    l0 = hmul2_bits(l0, Sla); l2 = hmul2_bits(l2, Sla);
+                    l1 = hmul2_bits(l1, Slb); l3 = hmul2_bits(l3, Slb);
+                    h0 = hmul2_bits(h0, Sha); h2 = hmul2_bits(h2, Sha);
+                    h1 = hmul2_bits(h1, Shb); h3 = hmul2_bits(h3, Shb);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        mma16816_acc(c[t], l0, l1, l2, l3, xb[t][4 * cc + pp][0], xb[t][4 * cc + pp][1]);
+                        mma16816_acc(c[t], h0, h1, h2, h3, xb[t][4 * cc + pp + 2][0], xb[t][4 * cc + pp + 2][1]);
+                    }
                 }
             }
         }
+        const float cfix = NT == 1 ? 512.0f : 1.0f;   // the codes' 2^-9 (4 columns: not in the scales)
         // mins: K slots 2i, 2i+1 = sub-blocks 2i, 2i+1 of rows g, g+8
         const uint32_t mwa = (i4 >> 1) ? (((ha.w >> 4) & 0x0F0F0F0Fu) | ((ha.z >> 2) & 0x30303030u)) : (ha.z & 0x3F3F3F3Fu);
         const uint32_t mwb = (i4 >> 1) ? (((hb.w >> 4) & 0x0F0F0F0Fu) | ((hb.z >> 2) & 0x30303030u)) : (hb.z & 0x3F3F3F3Fu);
@@ -2543,8 +2588,8 @@ struct Q4 {
         for (int t = 0; t < NT; ++t) {
             float cm[4];
             mma16816(cm, ma, mbb, 0u, 0u, xsb[t], 0u);
-            v[t][0] = undo[t] * fmaf(da, c[t][0] + c[t][1], -dma * (cm[0] + cm[1]));
-            v[t][1] = undo[t] * fmaf(db, c[t][2] + c[t][3], -dmb * (cm[2] + cm[3]));
+            v[t][0] = undo[t] * fmaf(da * cfix, c[t][0] + c[t][1], -dma * (cm[0] + cm[1]));
+            v[t][1] = undo[t] * fmaf(db * cfix, c[t][2] + c[t][3], -dmb * (cm[2] + cm[3]));
         }
     }
 };
