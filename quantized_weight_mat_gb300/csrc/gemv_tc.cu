@@ -30,7 +30,8 @@
 //           brings one 128-row x 144-byte super-block column per stage, and a
 //           1-D bulk copy brings that super-block's x tile;
 //   warps 0-15 decoders: thread (c, r) turns the 64 weights of chunk c of
-//           row r into fp16 sc*q (one LOP3 + one HFMA2 per two weights) and
+//           row r into fp16 sc*q (one mask per four codes, their e4m3
+//           conversion to q * 2^-9, one HMUL2 by sc * 2^9 per two weights) and
 //           writes them straight into tensor memory (tcgen05.st; TMEM lane =
 //           row, two K values per column), a ring of eight slots (two
 //           super-blocks); the chunk-0 threads also write the row's mins;
