@@ -180,7 +180,7 @@ def test_workload_q6_k_output_head(batch):
     full_case("q6_k", 128256, 4096, batch, 40, 41)
 
 
-@pytest.mark.parametrize("batch", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8, 16])
 @pytest.mark.parametrize("n_out,k,j", [(14336, 4096, 0), (4096, 14336, 1)])
 def test_workload_small_batch(n_out, k, j, batch):
     full_case("q4_k", n_out, k, batch, 50 + 2 * j, 51 + 2 * j)

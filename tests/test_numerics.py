@@ -98,6 +98,14 @@ def test_e4m3_nibble_decode_times_scale_is_exact(sc):
         assert float(np.float16(float(v)) * np.float16(s512)) == sc * q
 
 
+def test_byte_under_2_pow_23_gives_the_byte():
+    # the 4-column register-operand path reads a 6-bit scale byte b as the
+    # f32 with bits 0x4B000000 | b (= 2^23 + b) minus 2^23
+    for b in range(256):
+        f = np.array([0x4B000000 | b], dtype=np.uint32).view(np.float32)[0]
+        assert float(np.float32(f) - np.float32(8388608.0)) == b
+
+
 # ------------------------------------------------------------------ 2
 
 
