@@ -2478,9 +2478,9 @@ __device__ __forceinline__ void build_x(const Params &p, int t, int warp, int la
 // shared addresses ra, rb), giving v[t][0..1] = y parts of rows g, g+8.
 struct Q4 {
     // stages per CTA barrier (the partial sums of SPS stages are added after
-    // one barrier): 2 at 8 columns (14336x4096 batch 8 15.4 -> 14.8 us), 1 at
-    // 4 (batch 4 11.8 -> 12.0 us with 2)
-    template <int NT> static constexpr int sps() { return NT == 2 ? 2 : 1; }
+    // one barrier): 2 (14336x4096 batch 8 15.4 -> 14.8 us; batch 2 9.81 ->
+    // 9.52 us once the decode had become cheaper)
+    template <int NT> static constexpr int sps() { return 2; }
     static constexpr int ROWB = (K / 256) * 144;          // 2304
     static constexpr int PITCH = ROWB + 16;
     static constexpr bool XSUMS = true;

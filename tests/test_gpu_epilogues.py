@@ -84,12 +84,12 @@ def test_bias_parity(n_out, k, fmt, batch):
     assert ok, f"max err {err:.3g} > {bound:.3g}"
 
 
-@pytest.mark.parametrize("batch", [5, 8])
+@pytest.mark.parametrize("batch", [2, 3, 5, 8])
 @pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
 def test_swiglu_stage_groups(fmt, batch):
     # 3500 pairs at k = 4096: 23 pairs per CTA, so three stages of 8, 8 and 7
-    # pairs; at 8 columns the Q4_K kernel adds the partial sums of two stages
-    # after one barrier, which leaves a group of one stage at the end
+    # pairs; the Q4_K kernel adds the partial sums of two stages after one
+    # barrier, which leaves a group of one stage at the end
     n_ff, k = 3500, 4096
     w = weights(fmt, 2 * n_ff, k, "quantized", 36)
     x = x_for(batch, k, 37)

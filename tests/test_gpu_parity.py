@@ -151,9 +151,10 @@ def test_workload_q4_k_4096():
     full_case("q4_k", 4096, 4096, 1, 20, 21)
 
 
-@pytest.mark.parametrize("n_out,batch", [(7000, 5), (7000, 8), (6144, 8), (20000, 6), (2500, 7), (20000, 8)])
+@pytest.mark.parametrize("n_out,batch", [(7000, 5), (7000, 8), (6144, 8), (20000, 6), (2500, 7), (20000, 8),
+                                         (7000, 3), (20000, 4), (2500, 2), (6144, 2)])
 def test_register_operand_stage_groups(n_out, batch):
-    # Q4_K at k = 4096 with 5-8 columns: the register-operand kernel adds the
+    # Q4_K at k = 4096 with 2-8 columns: the register-operand kernel adds the
     # partial sums of two 16-row stages after one barrier.  Rows per CTA give
     # odd stage counts with a partial last stage (7000: 46-47 rows, stages of
     # 16, 16 and 14-15; 20000: 131-132 rows, nine stages) and CTAs of one or
