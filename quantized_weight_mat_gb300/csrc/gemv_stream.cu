@@ -614,14 +614,6 @@ struct Q4K {
     }
 };
 
-// Q4_K with 8 consumer warps (16-row stages), for CTAs of at most 32 rows:
-// 27 rows as 16 + 11 instead of 24 + 3 (4096x4096 3.87 -> 3.67 us); from
-// about 40 rows on, 12 warps are faster.
-struct Q4K8 : Q4K {
-    static constexpr int kWarps = 8;
-};
-constexpr int64_t kQ4K8MaxRows = 32;   // rows per CTA
-
 // ---------------------------------------------------------------------------
 // Q6_K: lane owns half h of its super-block (weights 128h..128h+127): ql bytes
 // 64h..64h+63, qh bytes 32h..32h+31, scales 8h..8h+7.  Blocks are 210 bytes,
@@ -2912,10 +2904,7 @@ cudaError_t launch_gemv_stream_epi(int fmt, const uint8_t *w, int64_t n_out, int
     const int grid = (int)(items < dev.sm_count ? items : dev.sm_count);
     if (batch > 1) return rmma::launch(fmt, w, n_out, x, batch, y, ldy, grid, s, weight_prefetch(), epi);
     switch (fmt) {
-    case PQ_Q4_K:
-        if (epi.kind != kEpiSwiGLU && k <= 4096 && n_out <= rowk::kQ4K8MaxRows * grid)
-            return rowk::launch_epi<rowk::Q4K8>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
-        return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
+    case PQ_Q4_K: return rowk::launch_epi<rowk::Q4K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q6_K: return rowk::launch_epi<rowk::Q6K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q8_0: return rowk::launch_epi<rowk::Q80>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
     case PQ_Q5_K: return rowk::launch_epi<rowk::Q5K>(w, n_out, k, x, y, grid, s, weight_prefetch(), epi);
